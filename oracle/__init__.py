@@ -1,0 +1,190 @@
+"""CPU oracle for MoE dispatch / combine -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package. The product path (the CUDA library and its
+Python binding) never imports, links or runs it, and the two share no code.
+
+``oracle.c`` is a plain single-threaded C99 restatement of the method; this
+module compiles it with gcc and wraps it with ctypes over numpy arrays.
+``brute.py`` is a second, independent NumPy formulation used to pin it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_SO = os.path.join(_HERE, "liboracle.so")
+_LIB = None
+_LOCK = threading.Lock()
+
+OK, ERR_ARG, ERR_EXPERT = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (IEEE fp32, no contraction)."""
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fno-fast-math",
+               "-fno-strict-aliasing", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _lib():
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            build()
+            L = ctypes.CDLL(_SO)
+            P = ctypes.c_void_p
+            i64, i32 = ctypes.c_int64, ctypes.c_int
+            L.orc_layout.argtypes = [P, i64, i32, i32, i32, P, P, P, P, P]
+            L.orc_layout.restype = i32
+            L.orc_dispatch_bf16.argtypes = [P, i64, i32, P, i32, P, P, P, P]
+            L.orc_dispatch_bf16.restype = None
+            L.orc_dispatch_e4m3.argtypes = [P, i64, i32, P, i32, P, P, P, P, P]
+            L.orc_dispatch_e4m3.restype = None
+            L.orc_quant_row_e4m3.argtypes = [P, i32, P, P]
+            L.orc_quant_row_e4m3.restype = None
+            L.orc_combine_row.argtypes = [P, i32, P, P, i32, P]
+            L.orc_combine_row.restype = None
+            L.orc_combine.argtypes = [P, i32, P, i64, i32, P, P]
+            L.orc_combine.restype = None
+            L.orc_f32_to_bf16_array.argtypes = [P, i64, P]
+            L.orc_f32_to_e4m3_array.argtypes = [P, i64, P]
+            L.orc_e4m3_sweep.argtypes = [ctypes.c_uint32, ctypes.c_uint32, P]
+            L.orc_f32_to_e4m3.argtypes = [ctypes.c_float]
+            L.orc_f32_to_e4m3.restype = ctypes.c_uint8
+            L.orc_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+            L.orc_e4m3_to_f32.restype = ctypes.c_float
+            _LIB = L
+    return _LIB
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def layout(topk_idx: np.ndarray, E: int, R: int) -> dict:
+    """Routing layout (counts, masks, offsets, slot -> row map) of topk_idx [T, K]."""
+    idx = _c(topk_idx, np.int64)
+    T, K = idx.shape
+    out = dict(
+        num_tokens_per_expert=np.zeros(E, np.int32),
+        num_tokens_per_rank=np.zeros(R, np.int32),
+        is_token_in_rank=np.zeros((T, R), np.uint8),
+        expert_offsets=np.zeros(E + 1, np.int32),
+        row_of_slot=np.zeros((T, K), np.int32),
+    )
+    st = _lib().orc_layout(_p(idx), T, K, E, R, _p(out["num_tokens_per_expert"]),
+                           _p(out["num_tokens_per_rank"]), _p(out["is_token_in_rank"]),
+                           _p(out["expert_offsets"]), _p(out["row_of_slot"]))
+    out["status"] = int(st)
+    return out
+
+
+def dispatch_bf16(x: np.ndarray, row_of_slot: np.ndarray, num_rows: int,
+                  topk_weights: np.ndarray | None = None, fill: int = 0):
+    """recv_x [num_rows, H] (uint16 bf16 bits), recv_src_token [num_rows], recv_weights."""
+    x = _c(x, np.uint16)
+    rows = _c(row_of_slot, np.int32)
+    T, H = x.shape
+    K = rows.shape[1]
+    recv = np.full((num_rows, H), fill, np.uint16)
+    src = np.full(num_rows, -1, np.int32)
+    rw = np.full(num_rows, np.nan, np.float32) if topk_weights is not None else None
+    w = _c(topk_weights, np.float32) if topk_weights is not None else None
+    _lib().orc_dispatch_bf16(_p(x), T, H, _p(rows), K, _p(w), _p(recv), _p(src), _p(rw))
+    return recv, src, rw
+
+
+def dispatch_e4m3(x: np.ndarray, row_of_slot: np.ndarray, num_rows: int,
+                  topk_weights: np.ndarray | None = None):
+    """recv_q [num_rows, H] uint8, recv_scales [num_rows, H/128] fp32, recv_src_token, recv_weights."""
+    x = _c(x, np.uint16)
+    rows = _c(row_of_slot, np.int32)
+    T, H = x.shape
+    K = rows.shape[1]
+    q = np.zeros((num_rows, H), np.uint8)
+    s = np.full((num_rows, H // 128), np.nan, np.float32)
+    src = np.full(num_rows, -1, np.int32)
+    rw = np.full(num_rows, np.nan, np.float32) if topk_weights is not None else None
+    w = _c(topk_weights, np.float32) if topk_weights is not None else None
+    _lib().orc_dispatch_e4m3(_p(x), T, H, _p(rows), K, _p(w), _p(q), _p(s), _p(src), _p(rw))
+    return q, s, src, rw
+
+
+def quant_row_e4m3(xrow: np.ndarray):
+    xrow = _c(xrow, np.uint16)
+    H = xrow.shape[0]
+    q = np.zeros(H, np.uint8)
+    s = np.zeros(H // 128, np.float32)
+    _lib().orc_quant_row_e4m3(_p(xrow), H, _p(q), _p(s))
+    return q, s
+
+
+def combine(y: np.ndarray, row_of_slot: np.ndarray, topk_weights: np.ndarray | None):
+    """out [T, H] (uint16 bf16 bits) = bf16(sum_k w[t,k] * y[row(t,k)])."""
+    y = _c(y, np.uint16)
+    rows = _c(row_of_slot, np.int32)
+    T, K = rows.shape
+    H = y.shape[1]
+    w = _c(topk_weights, np.float32) if topk_weights is not None else None
+    out = np.zeros((T, H), np.uint16)
+    _lib().orc_combine(_p(y), H, _p(rows), T, K, _p(w), _p(out))
+    return out
+
+
+def combine_tokens(y: np.ndarray, row_of_slot: np.ndarray, topk_weights: np.ndarray | None,
+                   tokens) -> np.ndarray:
+    """The combine output rows of the listed tokens only ([len(tokens), H])."""
+    y = _c(y, np.uint16)
+    rows = _c(row_of_slot, np.int32)
+    K = rows.shape[1]
+    H = y.shape[1]
+    w = _c(topk_weights, np.float32) if topk_weights is not None else None
+    out = np.zeros((len(tokens), H), np.uint16)
+    L = _lib()
+    for i, t in enumerate(tokens):
+        r = np.ascontiguousarray(rows[t])
+        wt = None if w is None else np.ascontiguousarray(w[t])
+        o = out[i]
+        L.orc_combine_row(_p(y), H, _p(r), _p(wt), K, o.ctypes.data)
+    return out
+
+
+def f32_to_bf16(a: np.ndarray) -> np.ndarray:
+    a = _c(a, np.float32)
+    out = np.zeros(a.shape, np.uint16)
+    _lib().orc_f32_to_bf16_array(_p(a), a.size, _p(out))
+    return out
+
+
+def f32_to_e4m3(a: np.ndarray) -> np.ndarray:
+    a = _c(a, np.float32)
+    out = np.zeros(a.shape, np.uint8)
+    _lib().orc_f32_to_e4m3_array(_p(a), a.size, _p(out))
+    return out
+
+
+def e4m3_sweep(lo: int, hi: int) -> np.ndarray:
+    out = np.zeros(hi - lo, np.uint8)
+    _lib().orc_e4m3_sweep(lo, hi, _p(out))
+    return out
+
+
+def e4m3_to_f32(q: np.ndarray) -> np.ndarray:
+    L = _lib()
+    return np.array([L.orc_e4m3_to_f32(int(v)) for v in np.asarray(q).ravel()],
+                    np.float32).reshape(np.shape(q))

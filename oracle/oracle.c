@@ -1,0 +1,285 @@
+/*
+ * Oracle for MoE token dispatch / combine -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, single-threaded C99 restatement of what the hot path
+ * computes. Only the tests, the smoke check and the bench's CPU-baseline leg
+ * may load this library; the product path never does. It shares no code,
+ * header, table or helper with the CUDA library.
+ *
+ * Build: gcc -O2 -std=c99 -ffp-contract=off -fno-fast-math -shared -fPIC
+ * (no SIMD intrinsics, no threads; float arithmetic is IEEE binary32 with
+ * round-to-nearest-even, and fmaf is the correctly rounded fused multiply-add).
+ *
+ * Sources (page title, then section):
+ *  - "nccl_ep.cc" (NCCL EP host code mirrored in TheRock/rccl contrib),
+ *    struct ncclEpHandle: is_token_in_rank is the outbound [token, rank] mask;
+ *    num_tokens_for_experts counts a token once however many local experts it
+ *    reaches; sparse_to_dense_map uses -1 for "not routed".
+ *    ncclEpCreateHandle: topk_idx is int64 [T, K]; num_experts % num_ranks == 0;
+ *    experts per rank = num_experts / num_ranks.
+ *    ncclEpDispatch (low-latency branch): fp8 scales are fp32, one per 128
+ *    hidden channels, laid out [rows, hidden/128].
+ *    ncclEpCombine (low-latency branch): combine is weighted by fp32
+ *    topk_weights [T, K] and writes out [T, hidden] in the input's dtype.
+ *  - DeepEP API docs: "dispatch()" (do_expand: one received row per
+ *    (token, expert) pair) and "Prefix Sum Interpretation for Expert Token
+ *    Counts" (per-expert row ranges come from a prefix sum of counts).
+ *  - NeMo fused_a2a (HybridEPDispatch / HybridEPCombine): -1 marks an unused
+ *    top-k slot; combine returns rows in the original token order.
+ *
+ * Readings where the pages leave a step open (each also listed in the design
+ * notes): expert e belongs to rank e / (E/R); offsets are the exclusive scan
+ * [E+1]; rows inside one expert keep (token, k) order; an id outside [-1, E)
+ * is an error and its slot is treated as dropped; fp8 uses
+ * scale = amax / 448 and q = e4m3_rne_satfinite(x / scale), with an all-zero
+ * block giving scale 0 and zero bytes; combine accumulates fp32 fmaf in
+ * ascending k from +0 and rounds once to bf16 (nearest-even).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_ERR_ARG 1
+#define ORC_ERR_EXPERT 2
+
+/* ---------------------------------------------------------------- formats */
+
+/* bf16 -> fp32: a bf16 value is the top half of the fp32 with the same bits. */
+float orc_bf16_to_f32(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* fp32 -> bf16, round to nearest, ties to even. bf16 keeps fp32's sign and
+ * 8-bit exponent and the top 7 mantissa bits, so rounding acts on the low 16
+ * bits: above half goes up, below half goes down, exactly half goes to the
+ * neighbour whose last kept bit is 0. A carry out of the mantissa correctly
+ * bumps the exponent (up to infinity). NaN stays a quiet NaN. */
+uint16_t orc_f32_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if (isnan(f)) return (uint16_t)(((u >> 16) & 0x8000u) | 0x7FC0u);
+    uint32_t hi = u >> 16, lo = u & 0xFFFFu;
+    if (lo > 0x8000u || (lo == 0x8000u && (hi & 1u))) hi += 1u;
+    return (uint16_t)hi;
+}
+
+/* OCP FP8 E4M3 ("e4m3fn"): 1 sign, 4 exponent (bias 7), 3 mantissa bits; no
+ * infinities; S.1111.111 is NaN, so the largest finite is S.1111.110 = 448.
+ * Normal values (exponent field 1..15): 2^(e-7) * (1 + m/8).
+ * Subnormals (exponent field 0): m * 2^-9.
+ * Encoding rounds to nearest, ties to even, and saturates anything beyond 448
+ * to +-448 ("satfinite"). Zero keeps its sign. */
+uint8_t orc_f32_to_e4m3(float f) {
+    if (isnan(f)) return 0x7F;
+    uint8_t sign = signbit(f) ? 0x80 : 0x00;
+    double a = fabs((double)f);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal range: count steps of 2^-9; rint rounds half to even.
+         * 8 steps is 2^-6, the smallest normal, whose code is 0x08. */
+        double m = rint(a * 512.0);
+        return (uint8_t)(sign | (uint8_t)m);
+    }
+    int ex;
+    (void)frexp(a, &ex);            /* a = fr * 2^ex, fr in [0.5, 1) */
+    int E = ex - 1;                 /* a in [2^E, 2^(E+1)) */
+    double m = rint(ldexp(a, 3 - E)); /* 8..16 mantissa steps of 2^(E-3) */
+    if (m >= 16.0) { m = 8.0; E += 1; }
+    int field = E + 7;
+    int code = (field << 3) | ((int)m - 8);
+    if (code > 0x7E) code = 0x7E;   /* rounding up past 448 saturates */
+    return (uint8_t)(sign | code);
+}
+
+/* E4M3 byte -> value (used by tests for dequantisation bounds). */
+float orc_e4m3_to_f32(uint8_t q) {
+    int s = q >> 7, field = (q >> 3) & 0xF, m = q & 7;
+    double v;
+    if (field == 0xF && m == 7) return NAN;
+    if (field == 0) v = ldexp((double)m, -9);
+    else v = ldexp(1.0 + m / 8.0, field - 7);
+    return (float)(s ? -v : v);
+}
+
+/* ---------------------------------------------------------------- layout */
+
+/* Routing layout from topk_idx [T, K] (int64, -1 = unused slot).
+ *   num_tokens_per_expert[e] = number of slots naming e
+ *   is_token_in_rank[t, r]   = 1 if any slot of t names an expert of rank r
+ *   num_tokens_per_rank[r]   = number of tokens t with is_token_in_rank[t, r]
+ *   expert_offsets[E + 1]    = exclusive prefix sum of the expert counts
+ *   row_of_slot[t, k]        = receive row of slot (t, k), -1 if unused;
+ *                              rows of expert e are expert_offsets[e] .. in
+ *                              (t, k) order (a counting sort keyed by expert).
+ * Returns ORC_ERR_EXPERT if any id lies outside [-1, E) (that slot is then
+ * treated as unused), ORC_ERR_ARG for bad sizes. */
+int orc_layout(const int64_t* topk_idx, int64_t T, int K, int E, int R,
+               int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+               uint8_t* is_token_in_rank, int32_t* expert_offsets,
+               int32_t* row_of_slot) {
+    if (T < 0 || K <= 0 || E <= 0 || R <= 0 || E % R != 0) return ORC_ERR_ARG;
+    int L = E / R;
+    int status = ORC_OK;
+    int64_t* cnt64 = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+    int64_t* next = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+    if (!cnt64 || !next) { free(cnt64); free(next); return ORC_ERR_ARG; }
+    for (int r = 0; r < R; ++r) num_tokens_per_rank[r] = 0;
+
+    for (int64_t t = 0; t < T; ++t) {
+        uint8_t* mask = is_token_in_rank + t * R;
+        for (int r = 0; r < R; ++r) mask[r] = 0;
+        for (int k = 0; k < K; ++k) {
+            int64_t e = topk_idx[t * K + k];
+            if (e == -1) continue;
+            if (e < -1 || e >= E) { status = ORC_ERR_EXPERT; continue; }
+            cnt64[e] += 1;
+            mask[e / L] = 1;
+        }
+        for (int r = 0; r < R; ++r) num_tokens_per_rank[r] += mask[r];
+    }
+
+    int64_t run = 0;
+    for (int e = 0; e < E; ++e) {
+        expert_offsets[e] = (int32_t)run;
+        num_tokens_per_expert[e] = (int32_t)cnt64[e];
+        next[e] = run;
+        run += cnt64[e];
+    }
+    if (run > INT32_MAX) { free(cnt64); free(next); return ORC_ERR_ARG; }
+    expert_offsets[E] = (int32_t)run;
+
+    for (int64_t t = 0; t < T; ++t) {
+        for (int k = 0; k < K; ++k) {
+            int64_t e = topk_idx[t * K + k];
+            if (e < 0 || e >= E) { row_of_slot[t * K + k] = -1; continue; }
+            row_of_slot[t * K + k] = (int32_t)next[e]++;
+        }
+    }
+    free(cnt64);
+    free(next);
+    return status;
+}
+
+/* ---------------------------------------------------------------- dispatch */
+
+/* bf16 permute: recv_x[row_of_slot[t, k]] = x[t] for every used slot.
+ * Optional outputs (NULL = skip): recv_src_token[row] = t and
+ * recv_weights[row] = topk_weights[t, k]. */
+void orc_dispatch_bf16(const uint16_t* x, int64_t T, int H, const int32_t* row_of_slot,
+                       int K, const float* topk_weights, uint16_t* recv_x,
+                       int32_t* recv_src_token, float* recv_weights) {
+    for (int64_t t = 0; t < T; ++t) {
+        for (int k = 0; k < K; ++k) {
+            int32_t row = row_of_slot[t * K + k];
+            if (row < 0) continue;
+            memcpy(recv_x + (int64_t)row * H, x + t * H, (size_t)H * sizeof(uint16_t));
+            if (recv_src_token) recv_src_token[row] = (int32_t)t;
+            if (recv_weights && topk_weights) recv_weights[row] = topk_weights[t * K + k];
+        }
+    }
+}
+
+/* Quantise one token row to e4m3 with one fp32 scale per 128 channels:
+ *   amax  = max |x| over the block (exact, in fp32)
+ *   scale = amax / 448            (fp32 division, nearest-even)
+ *   q     = e4m3(x / scale)       (fp32 division, then nearest-even, satfinite)
+ * An all-zero block gives scale 0 and all-zero bytes. */
+void orc_quant_row_e4m3(const uint16_t* xrow, int H, uint8_t* qrow, float* srow) {
+    for (int b = 0; b < H / 128; ++b) {
+        float amax = 0.0f;
+        for (int i = 0; i < 128; ++i) {
+            float v = fabsf(orc_bf16_to_f32(xrow[b * 128 + i]));
+            if (v > amax) amax = v;
+        }
+        if (amax == 0.0f) {
+            srow[b] = 0.0f;
+            for (int i = 0; i < 128; ++i) qrow[b * 128 + i] = 0x00;
+            continue;
+        }
+        float scale = amax / 448.0f;
+        srow[b] = scale;
+        for (int i = 0; i < 128; ++i) {
+            float v = orc_bf16_to_f32(xrow[b * 128 + i]) / scale;
+            qrow[b * 128 + i] = orc_f32_to_e4m3(v);
+        }
+    }
+}
+
+/* fp8 permute: each used slot's row receives its token's e4m3 bytes [H] and
+ * scales [H/128]. */
+void orc_dispatch_e4m3(const uint16_t* x, int64_t T, int H, const int32_t* row_of_slot,
+                       int K, const float* topk_weights, uint8_t* recv_q, float* recv_scales,
+                       int32_t* recv_src_token, float* recv_weights) {
+    int nb = H / 128;
+    uint8_t* q = (uint8_t*)malloc((size_t)(H > 0 ? H : 1));
+    float* s = (float*)malloc((size_t)(nb > 0 ? nb : 1) * sizeof(float));
+    if (!q || !s) { free(q); free(s); return; }
+    for (int64_t t = 0; t < T; ++t) {
+        int any = 0;
+        for (int k = 0; k < K; ++k) any |= row_of_slot[t * K + k] >= 0;
+        if (!any) continue;
+        orc_quant_row_e4m3(x + t * H, H, q, s);
+        for (int k = 0; k < K; ++k) {
+            int32_t row = row_of_slot[t * K + k];
+            if (row < 0) continue;
+            memcpy(recv_q + (int64_t)row * H, q, (size_t)H);
+            memcpy(recv_scales + (int64_t)row * nb, s, (size_t)nb * sizeof(float));
+            if (recv_src_token) recv_src_token[row] = (int32_t)t;
+            if (recv_weights && topk_weights) recv_weights[row] = topk_weights[t * K + k];
+        }
+    }
+    free(q);
+    free(s);
+}
+
+/* ---------------------------------------------------------------- combine */
+
+/* One output row: out[h] = bf16( sum over k ascending with row >= 0 of
+ * w[k] * y[row_k, h] ), accumulated in fp32 with fmaf from +0.
+ * w == NULL means every weight is 1. */
+void orc_combine_row(const uint16_t* y, int H, const int32_t* rows, const float* w, int K,
+                     uint16_t* out_row) {
+    for (int h = 0; h < H; ++h) {
+        float acc = 0.0f;
+        for (int k = 0; k < K; ++k) {
+            int32_t row = rows[k];
+            if (row < 0) continue;
+            float wk = w ? w[k] : 1.0f;
+            acc = fmaf(wk, orc_bf16_to_f32(y[(int64_t)row * H + h]), acc);
+        }
+        out_row[h] = orc_f32_to_bf16(acc);
+    }
+}
+
+void orc_combine(const uint16_t* y, int H, const int32_t* row_of_slot, int64_t T, int K,
+                 const float* topk_weights, uint16_t* out) {
+    for (int64_t t = 0; t < T; ++t)
+        orc_combine_row(y, H, row_of_slot + t * K, topk_weights ? topk_weights + t * K : 0, K,
+                        out + t * H);
+}
+
+/* ---------------------------------------------------------------- arrays */
+
+/* Element-wise encoders over arrays, for exhaustive format sweeps. */
+void orc_f32_to_bf16_array(const float* in, int64_t n, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_bf16(in[i]);
+}
+
+void orc_f32_to_e4m3_array(const float* in, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_e4m3(in[i]);
+}
+
+/* Sweep fp32 bit patterns [lo, hi) through the e4m3 encoder (no input array). */
+void orc_e4m3_sweep(uint32_t lo, uint32_t hi, uint8_t* out) {
+    for (uint64_t u = lo; u < hi; ++u) {
+        uint32_t b = (uint32_t)u;
+        float f;
+        memcpy(&f, &b, sizeof f);
+        out[u - lo] = orc_f32_to_e4m3(f);
+    }
+}

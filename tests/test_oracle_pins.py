@@ -1,0 +1,307 @@
+"""Pins for the CPU oracle: each check comes from something other than the
+oracle itself -- hand-worked fixtures, an independent NumPy formulation, torch's
+own format casts, closed forms and invariants of the method."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import brute
+from gen import inputs as gi
+
+
+def _ints(v):
+    return np.array([int(x, 0) for x in v], dtype=np.int64)
+
+
+# ------------------------------------------------------------------ layout
+
+@pytest.mark.parametrize("name", ["layout_hand.txt", "layout_hand_dup.txt"])
+def test_layout_golden(golden, name):
+    g = golden(name)
+    T, K, E, R = (int(g[k][0]) for k in "TKER")
+    idx = _ints(g["topk_idx"]).reshape(T, K)
+    L = oracle.layout(idx, E, R)
+    assert L["status"] == oracle.OK
+    np.testing.assert_array_equal(L["num_tokens_per_expert"], _ints(g["num_tokens_per_expert"]))
+    np.testing.assert_array_equal(L["expert_offsets"], _ints(g["expert_offsets"]))
+    np.testing.assert_array_equal(L["row_of_slot"].ravel(), _ints(g["row_of_slot"]))
+    np.testing.assert_array_equal(L["is_token_in_rank"].ravel(), _ints(g["is_token_in_rank"]))
+    np.testing.assert_array_equal(L["num_tokens_per_rank"], _ints(g["num_tokens_per_rank"]))
+
+
+def _random_routing(rng, T, K, E, drop_p=0.0, distinct=True, bad_p=0.0):
+    if distinct and K <= E:
+        idx = np.argsort(rng.random((T, E)), axis=1)[:, :K]
+    else:
+        idx = rng.integers(0, E, size=(T, K))
+    idx = idx.astype(np.int64)
+    idx[rng.random((T, K)) < drop_p] = -1
+    if bad_p > 0:
+        bad = rng.random((T, K)) < bad_p
+        idx[bad] = rng.choice([E, E + 5, -2, -100], size=bad.sum())
+    return idx
+
+
+CORNERS = [
+    # (T, K, E, R, drop_p, distinct, bad_p)
+    (1, 1, 1, 1, 0.0, True, 0.0),
+    (1, 4, 8, 2, 0.0, True, 0.0),
+    (7, 3, 5, 5, 0.2, True, 0.0),    # E == R
+    (33, 2, 6, 1, 0.1, False, 0.0),  # R == 1, duplicates allowed
+    (50, 8, 8, 4, 0.0, True, 0.0),   # K == E: every token hits every expert
+    (64, 4, 16, 4, 1.0, True, 0.0),  # everything dropped
+    (129, 6, 64, 4, 0.05, True, 0.0),
+    (300, 2, 32, 8, 0.3, False, 0.0),
+    (40, 3, 12, 3, 0.0, True, 0.1),  # invalid ids
+]
+
+
+@pytest.mark.parametrize("case", CORNERS)
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_layout_vs_brute(case, seed):
+    T, K, E, R, drop_p, distinct, bad_p = case
+    rng = np.random.default_rng(seed)
+    idx = _random_routing(rng, T, K, E, drop_p, distinct, bad_p)
+    a = oracle.layout(idx, E, R)
+    b = brute.layout(idx, E, R)
+    for key in ["num_tokens_per_expert", "num_tokens_per_rank", "is_token_in_rank",
+                "expert_offsets", "row_of_slot", "status"]:
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+
+
+def test_layout_one_expert_takes_all():
+    idx = np.full((100, 1), 3, np.int64)
+    L = oracle.layout(idx, 8, 2)
+    assert L["num_tokens_per_expert"].tolist() == [0, 0, 0, 100, 0, 0, 0, 0]
+    assert L["row_of_slot"].ravel().tolist() == list(range(100))
+    assert L["num_tokens_per_rank"].tolist() == [100, 0]
+
+
+def test_layout_k1_is_stable_argsort():
+    rng = np.random.default_rng(5)
+    e = rng.integers(0, 16, size=500)
+    L = oracle.layout(e[:, None], 16, 4)
+    order = np.argsort(e, kind="stable")
+    rows = np.empty(500, np.int64)
+    rows[order] = np.arange(500)
+    np.testing.assert_array_equal(L["row_of_slot"].ravel(), rows)
+
+
+def test_layout_bad_args():
+    idx = np.zeros((4, 2), np.int64)
+    assert oracle.layout(idx, 6, 4)["status"] == oracle.ERR_ARG  # E % R != 0
+
+
+def _check_invariants(idx, E, R, L):
+    T, K = idx.shape
+    valid = idx >= 0
+    N = int(valid.sum())
+    cnt, off, rows = L["num_tokens_per_expert"], L["expert_offsets"], L["row_of_slot"]
+    assert cnt.sum() == N and off[0] == 0 and off[E] == N
+    assert (np.diff(off) == cnt).all()
+    r = rows[valid]
+    assert np.array_equal(np.sort(r), np.arange(N))            # bijection onto [0, N)
+    assert (rows[~valid] == -1).all()
+    # rows of expert e lie in its range, in strictly increasing (t, k) order
+    e_of_row = np.empty(N, np.int64)
+    slot_of_row = np.empty(N, np.int64)
+    e_of_row[r] = idx[valid]
+    slot_of_row[r] = np.flatnonzero(valid.ravel())
+    for e in range(E):
+        seg = slice(off[e], off[e + 1])
+        assert (e_of_row[seg] == e).all()
+        assert (np.diff(slot_of_row[seg]) > 0).all()
+    Lr = E // R
+    slab = np.array([off[(q + 1) * Lr] - off[q * Lr] for q in range(R)])
+    assert slab.sum() == N
+    ntr = L["num_tokens_per_rank"]
+    assert (ntr <= np.minimum(T, slab)).all()
+    assert (L["is_token_in_rank"].sum(axis=0) == ntr).all()
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "skewed"])
+def test_layout_invariants_on_workloads(name):
+    w = gi.WORKLOADS[name]
+    inp = gi.make(name, 0, with_y=False)
+    L = oracle.layout(inp.topk_idx, w.E, w.R)
+    assert L["status"] == oracle.OK
+    _check_invariants(inp.topk_idx, w.E, w.R, L)
+
+
+# ------------------------------------------------------------------ formats
+
+def _torch_bf16_bits(f32):
+    t = torch.from_numpy(np.ascontiguousarray(f32, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _torch_e4m3_bits(f32):
+    t = torch.from_numpy(np.ascontiguousarray(f32, np.float32)).clamp(-448.0, 448.0)
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _structured_f32_patterns():
+    """All sign/exponent/top-mantissa combinations with low bits near the
+    rounding midpoints of bf16 (bit 15) and e4m3 (bits 19 and below)."""
+    hi = np.arange(1 << 13, dtype=np.uint32) << np.uint32(19)   # sign, exp, top 4 mantissa bits
+    lows = np.array([0, 1, 0x7FFF, 0x8000, 0x8001, 0xFFFF, 0x3FFFF, 0x40000, 0x40001, 0x7FFFF,
+                     0x10000, 0x18000], np.uint32)
+    u = (hi[:, None] | lows[None, :]).ravel()
+    f = u.view(np.float32)
+    return f[np.isfinite(f)]
+
+
+def test_bf16_encoder_vs_torch():
+    rng = np.random.default_rng(0)
+    f = np.concatenate([_structured_f32_patterns(),
+                        rng.integers(0, 2**32, 2_000_000, dtype=np.uint64).astype(np.uint32).view(np.float32)])
+    f = f[np.isfinite(f)]
+    np.testing.assert_array_equal(oracle.f32_to_bf16(f), _torch_bf16_bits(f))
+
+
+def test_e4m3_encoder_vs_torch():
+    rng = np.random.default_rng(1)
+    f = np.concatenate([_structured_f32_patterns(),
+                        rng.integers(0, 2**32, 2_000_000, dtype=np.uint64).astype(np.uint32).view(np.float32),
+                        (rng.standard_normal(500_000) * 100).astype(np.float32),
+                        (rng.standard_normal(500_000) * 0.01).astype(np.float32)])
+    f = f[np.isfinite(f)]
+    np.testing.assert_array_equal(oracle.f32_to_e4m3(f), _torch_e4m3_bits(f))
+
+
+def test_e4m3_encoder_vs_brute_search():
+    rng = np.random.default_rng(2)
+    codes, vals = brute.e4m3_values()
+    mids = (np.sort(vals)[1:] + np.sort(vals)[:-1]) / 2
+    f = np.concatenate([vals, mids, mids * (1 + 2**-20), mids * (1 - 2**-20), [500.0, -1e30, 464.0, -0.0],
+                        rng.standard_normal(3000) * 50]).astype(np.float32)
+    np.testing.assert_array_equal(oracle.f32_to_e4m3(f), brute.e4m3_encode(f))
+
+
+def test_e4m3_decode_roundtrip():
+    codes, vals = brute.e4m3_values()
+    dec = oracle.e4m3_to_f32(codes)
+    np.testing.assert_array_equal(dec.astype(np.float64), vals)
+    np.testing.assert_array_equal(oracle.f32_to_e4m3(vals.astype(np.float32)), codes)
+
+
+# ------------------------------------------------------------------ fp8 quantiser
+
+def test_fp8_block_golden(golden):
+    g = golden("fp8_block_hand.txt")
+    x = np.zeros(128, np.float32)
+    for kv in g["x"]:
+        i, v = kv.split(":")
+        x[int(i)] = float(v)
+    xb = gi.f32_to_bf16_bits(x)
+    assert (gi.bf16_bits_to_f32(xb) == x).all(), "fixture values must be bf16-exact"
+    q, s = oracle.quant_row_e4m3(xb)
+    assert s[0] == np.float32(float(g["scale"][0]))
+    want = np.zeros(128, np.uint8)
+    for kv in g["q"]:
+        i, v = kv.split(":")
+        want[int(i)] = int(v, 16)
+    np.testing.assert_array_equal(q, want)
+
+
+def test_fp8_closed_forms():
+    rng = np.random.default_rng(3)
+    H = 1024
+    x = (rng.standard_normal((64, H)) * 2).astype(np.float32)
+    x[0, :128] = 0.0          # an all-zero block
+    x[1, 128:256] = -0.0      # all negative zeros
+    x[2, 256:384] = 1e-38     # tiny normal values
+    xb = gi.f32_to_bf16_bits(x)
+    xf = gi.bf16_bits_to_f32(xb).reshape(64, H // 128, 128)
+    for t in range(64):
+        q, s = oracle.quant_row_e4m3(xb[t])
+        qb = q.reshape(-1, 128)
+        deq = oracle.e4m3_to_f32(q).reshape(-1, 128).astype(np.float64)
+        for b in range(H // 128):
+            blk = xf[t, b]
+            amax = np.abs(blk).max()
+            if amax == 0:
+                assert s[b] == 0 and (qb[b] == 0).all()
+                continue
+            assert s[b] == np.float32(amax) / np.float32(448.0)
+            # the block-max element always lands on +-448
+            i = int(np.argmax(np.abs(blk)))
+            assert qb[b, i] in (0x7E, 0xFE)
+            # dequantisation error: half a step of e4m3 at each magnitude
+            err = np.abs(deq[b] * s[b] - blk.astype(np.float64))
+            bound = np.maximum(np.abs(blk) * 2.0**-4, 2.0**-10 * s[b]) * (1 + 1e-6)
+            assert (err <= bound).all()
+
+
+# ------------------------------------------------------------------ dispatch / combine
+
+def test_dispatch_bf16_moves_rows():
+    inp = gi.make("tiny", 0)
+    w = inp.w
+    L = oracle.layout(inp.topk_idx, w.E, w.R)
+    N = int(L["expert_offsets"][-1])
+    recv, src, rw = oracle.dispatch_bf16(inp.x, L["row_of_slot"], N, inp.topk_weights)
+    for t in range(w.T):
+        for k in range(w.K):
+            r = L["row_of_slot"][t, k]
+            assert (recv[r] == inp.x[t]).all() and src[r] == t and rw[r] == inp.topk_weights[t, k]
+
+
+def test_combine_golden(golden):
+    g = golden("combine_hand.txt")
+    H = int(g["H"][0])
+    y = gi.f32_to_bf16_bits(np.array([float(v) for v in g["y"]], np.float32)).reshape(-1, H)
+    rows = _ints(g["row_of_slot"]).reshape(-1, 2).astype(np.int32)
+    w = np.array([float(v) for v in g["topk_weights"]], np.float32).reshape(-1, 2)
+    out = oracle.combine(y, rows, w)
+    want = np.array([float(v) for v in g["out"]], np.float32).reshape(-1, H)
+    np.testing.assert_array_equal(gi.bf16_bits_to_f32(out), want)
+
+
+def test_combine_one_hot_recovers_rows():
+    inp = gi.make("tiny", 1)
+    w = inp.w
+    L = oracle.layout(inp.topk_idx, w.E, w.R)
+    N = int(L["expert_offsets"][-1])
+    rng = np.random.default_rng(0)
+    y = gi.f32_to_bf16_bits(rng.standard_normal((N, w.H)).astype(np.float32))
+    onehot = np.zeros((w.T, w.K), np.float32)
+    pick = rng.integers(0, w.K, w.T)
+    onehot[np.arange(w.T), pick] = 1.0
+    out = oracle.combine(y, L["row_of_slot"], onehot)
+    np.testing.assert_array_equal(out, y[L["row_of_slot"][np.arange(w.T), pick]])
+
+
+def test_combine_identity_expert_recovers_x():
+    inp = gi.make("tiny", 0)
+    w = inp.w
+    L = oracle.layout(inp.topk_idx, w.E, w.R)
+    N = int(L["expert_offsets"][-1])
+    recv, _, _ = oracle.dispatch_bf16(inp.x, L["row_of_slot"], N)
+    out = gi.bf16_bits_to_f32(oracle.combine(recv, L["row_of_slot"], inp.topk_weights))
+    x = gi.bf16_bits_to_f32(inp.x)
+    # weights sum to 1 within a few fp32 ulps, then one bf16 round
+    np.testing.assert_allclose(out, x, rtol=2.0**-7, atol=0)
+
+
+@pytest.mark.parametrize("name,null_w", [("skewed", False), ("decode", False), ("tiny", True)])
+def test_combine_vs_f64(name, null_w):
+    inp = gi.make(name, 2, T=96)
+    w = inp.w
+    L = oracle.layout(inp.topk_idx, w.E, w.R)
+    N = int(L["expert_offsets"][-1])
+    y = inp.y if inp.y is not None else gi.normal_bf16(np.random.SeedSequence(9), N, w.H)
+    wt = None if null_w else inp.topk_weights
+    out = gi.bf16_bits_to_f32(oracle.combine(y, L["row_of_slot"], wt)).astype(np.float64)
+    yf = gi.bf16_bits_to_f32(y)
+    ref = brute.combine_f64(yf, L["row_of_slot"], wt)
+    absw = np.ones((w.T, w.K)) if wt is None else np.abs(wt.astype(np.float64))
+    mag = brute.combine_f64(np.abs(yf), L["row_of_slot"], absw)
+    # fp32 accumulation error (K roundings of at most 2^-24 relative to the
+    # running magnitude) plus half a bf16 ulp of the result
+    bound = w.K * 2.0**-24 * mag + 2.0**-8 * np.abs(ref) + 1e-30
+    assert (np.abs(out - ref) <= bound).all()
+    # and dropped-only tokens give +0
+    dead = (L["row_of_slot"] < 0).all(axis=1)
+    assert (out[dead] == 0).all()
