@@ -1,0 +1,491 @@
+"""Benchmark: MoE routing layout + bf16 dispatch + weighted combine on one GB300.
+
+Workload (prefill shape): T=8192 tokens, H=7168, E=256 experts, top-8,
+R=8 logical rank slabs; x bf16 ~N(0,1), K distinct uniform experts per token,
+fp32 weights U(0,1) normalised, expert outputs y bf16 ~N(0,1) [N, H].
+One step = ep_layout + ep_dispatch(bf16) + ep_combine through the C ABI.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line on rank 0. Under torchrun every rank runs its own
+replica of the workload on its own GPU (no data exchange); the step time is
+the max over ranks and `value` counts the bytes of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gen import inputs as gi  # noqa: E402
+
+METRIC = "dispatch & combine HBM GB/s + tokens/s, T=8192 H=7168 E=256 top-8 bf16"
+WORKLOAD = "prefill"
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ---------------------------------------------------------------- bytes
+
+def bytes_layout(T, K, E, R):
+    # topk_idx read, counts/offsets/masks written, slot -> row map written
+    return 8 * T * K + 4 * E + 4 * R + T * R + 4 * (E + 1) + 4 * T * K
+
+
+def bytes_dispatch_bf16(T, K, H, N):
+    return 2 * T * H + 2 * N * H + 4 * T * K
+
+
+def bytes_dispatch_fp8(T, K, H, N):
+    return 2 * T * H + N * H + 4 * N * (H // 128) + 4 * T * K
+
+
+def bytes_combine(T, K, H, N):
+    return 2 * N * H + 4 * T * K + 4 * T * K + 2 * T * H
+
+
+# ---------------------------------------------------------------- environment
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.samples = []   # (t, sm, max, reasons set)
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms={self.period}"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            reasons = {n for n, v in zip(names, parts[5:9]) if v.lower() == "active"}
+            self.samples.append((time.perf_counter(), sm, mx, reasons))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
+        note = "timed region"
+        if not win and self.samples:
+            # the timed region was shorter than one sampling period: use the
+            # samples closest to it (warm-up and timed work run back to back)
+            win = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            note = "nearest samples (timed region shorter than the sampling period)"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        reasons = sorted(set().union(*[s[3] for s in win]))
+        return {"sm_mhz": statistics.median(s[1] for s in win), "sm_max_mhz": max(s[2] for s in win),
+                "reasons": reasons, "samples": len(win), "note": note}
+
+
+def smi_id(local: int) -> str:
+    """nvidia-smi's id of CUDA device `local` (honours CUDA_VISIBLE_DEVICES)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").strip()
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local < len(ids):
+            return ids[local]
+    return str(local)
+
+
+def read_traffic(kernel: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if
+    the kernel source has not changed since the capture (else None)."""
+    import hashlib
+    import re
+
+    path = os.path.join(ROOT, "profiles", "ncu_summary.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(rf"<!-- traffic kernel={kernel} bytes=(\d+) src_sha256=([0-9a-f]+) -->", txt)
+    if not m:
+        return None
+    src = {"dispatch_bf16": "ep_dispatch.cu", "combine": "ep_combine.cu"}.get(kernel)
+    if src is None:
+        return None
+    h = hashlib.sha256(open(os.path.join(ROOT, "combine_get_dispatch_layout_gb300", "csrc", src), "rb").read())
+    return int(m.group(1)) if h.hexdigest()[:16] == m.group(2) else None
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def gpu_arm(args, rank, world, local):
+    import torch
+
+    import combine_get_dispatch_layout_gb300 as ep
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    ep.lib()   # raises if the library is missing: there is no other path
+
+    inp = gi.make(WORKLOAD, seed=args.seed + rank)
+    w = inp.w
+    T, H, E, K, R, N = w.T, w.H, w.E, w.K, w.R, inp.num_valid
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        idx = torch.from_numpy(inp.topk_idx).to(dev)
+        x = torch.from_numpy(inp.x.view(np.int16)).to(dev).view(torch.bfloat16)
+        wt = torch.from_numpy(inp.topk_weights).to(dev)
+        y = torch.from_numpy(inp.y.view(np.int16)).to(dev).view(torch.bfloat16)
+        cnt = torch.empty(E, dtype=torch.int32, device=dev)
+        ntr = torch.empty(R, dtype=torch.int32, device=dev)
+        itr = torch.empty(T, R, dtype=torch.uint8, device=dev)
+        off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        recv = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    stream.synchronize()
+    handle = ep.ep_layout(idx, E, R, cnt, ntr, itr, off, stream=stream)   # creates the handle once
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        ep.ep_layout(idx, E, R, cnt, ntr, itr, off, handle=handle, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        ep.ep_dispatch(handle, x, ep.EP_DTYPE_BF16, recv, N, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        ep.ep_combine(handle, y, out, topk_weights=wt, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    sampler = ClockSampler(smi_id(local))
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        step(events[i])
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.perf_counter()
+    if world > 1:
+        torch.distributed.barrier()
+    time.sleep(0.15)
+    sampler.stop()
+
+    per = np.array([[events[i][j].elapsed_time(events[i][j + 1]) for j in range(3)] for i in range(args.steps)])
+    total_ms = float(events[0][0].elapsed_time(events[-1][3]))
+    ms_layout, ms_dispatch, ms_combine = (float(per[:, j].mean()) for j in range(3))
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+
+    b_lay = bytes_layout(T, K, E, R)
+    b_dis = bytes_dispatch_bf16(T, K, H, N)
+    b_com = bytes_combine(T, K, H, N)
+    b_step = b_lay + b_dis + b_com
+    peak, peak_src = load_peaks()
+
+    # fp8 quantise-permute on the fp8 workload (same shapes and routing recipe)
+    fp8 = gi.make("fp8", seed=args.seed + rank, with_y=False)
+    with torch.cuda.stream(stream):
+        x8 = torch.from_numpy(fp8.x.view(np.int16)).to(dev).view(torch.bfloat16)
+        idx8 = torch.from_numpy(fp8.topk_idx).to(dev)
+        q = torch.empty(fp8.num_valid, H, dtype=torch.uint8, device=dev)
+        sc = torch.empty(fp8.num_valid, H // 128, dtype=torch.float32, device=dev)
+    h8 = ep.ep_layout(idx8, E, R, cnt, ntr, itr, off, stream=stream)
+    reps8 = max(3, min(args.steps, 200))
+    ev8 = [torch.cuda.Event(enable_timing=True) for _ in range(reps8 + 1)]
+    for _ in range(3):
+        ep.ep_dispatch(h8, x8, ep.EP_DTYPE_FP8_E4M3, q, fp8.num_valid, recv_scales=sc, stream=stream)
+    for i in range(reps8):
+        ev8[i].record(stream)
+        ep.ep_dispatch(h8, x8, ep.EP_DTYPE_FP8_E4M3, q, fp8.num_valid, recv_scales=sc, stream=stream)
+    ev8[reps8].record(stream)
+    stream.synchronize()
+    ms_fp8 = float(np.mean([ev8[i].elapsed_time(ev8[i + 1]) for i in range(reps8)]))
+    b_fp8 = bytes_dispatch_fp8(T, K, H, fp8.num_valid)
+
+    # end to end through the public API with pinned host buffers
+    e2e = e2e_measure(torch, ep, dev, inp, args, stream)
+    if world > 1:
+        t = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e["ms_per_step"] = float(t.item())
+    handle.destroy()
+    h8.destroy()
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    dominant = "dispatch_bf16" if ms_dispatch >= ms_combine else "combine"
+    dom_ms = ms_dispatch if dominant == "dispatch_bf16" else ms_combine
+    dom_bytes = b_dis if dominant == "dispatch_bf16" else b_com
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    clocks = sampler.summary(t_wall0 - 0.3, t_wall1)
+    line = {
+        "metric": METRIC,
+        "value": round(world * b_step / (ms_step * 1e-3) / 1e9, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded numpy PCG64; recipe in gen/inputs.py)",
+        "config": {"workload": "prefill dispatch+combine: T=8192 H=7168 E=256 K=8 R=8, bf16 rows, "
+                               "uniform distinct routing, fp32 weights U(0,1) normalised",
+                   "T": T, "H": H, "E": E, "K": K, "R": R, "N": N,
+                   "step": "ep_layout + ep_dispatch(bf16) + ep_combine",
+                   "l2": "no flush: every step moves >1 GB (> 129 MB L2) through each of dispatch and combine",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": round(world * T / (ms_step * 1e-3), 1),
+        "kernels": {
+            "layout": {"us": round(ms_layout * 1e3, 2), "bytes": b_lay},
+            "dispatch_bf16": {"us": round(ms_dispatch * 1e3, 2), "bytes": b_dis,
+                              "gbs": round(b_dis / (ms_dispatch * 1e-3) / 1e9, 1),
+                              "frac_of_measured": round(b_dis / (ms_dispatch * 1e-3) / 1e9 / peak, 4),
+                              "frac_of_8tbs": round(b_dis / (ms_dispatch * 1e-3) / 8e12, 4)},
+            "combine": {"us": round(ms_combine * 1e3, 2), "bytes": b_com,
+                        "gbs": round(b_com / (ms_combine * 1e-3) / 1e9, 1),
+                        "frac_of_measured": round(b_com / (ms_combine * 1e-3) / 1e9 / peak, 4),
+                        "frac_of_8tbs": round(b_com / (ms_combine * 1e-3) / 8e12, 4)},
+            "dispatch_fp8": {"workload": "fp8: x ~N(0,2^2) + 7 outlier channels x50, same shapes",
+                             "us": round(ms_fp8 * 1e3, 2), "bytes": b_fp8,
+                             "gbs": round(b_fp8 / (ms_fp8 * 1e-3) / 1e9, 1),
+                             "frac_of_measured": round(b_fp8 / (ms_fp8 * 1e-3) / 1e9 / peak, 4),
+                             "frac_of_8tbs": round(b_fp8 / (ms_fp8 * 1e-3) / 8e12, 4)},
+        },
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": read_traffic(dominant)},
+        "e2e": {"value": round(world * b_step / (e2e["ms_per_step"] * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "ms_per_step": round(e2e["ms_per_step"], 4), "steps": e2e["steps"]},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def e2e_measure(torch, ep, dev, inp, args, stream):
+    """Same step through the public API with host buffers: H2D of topk_idx,
+    weights, x and y from pinned memory, layout + dispatch + combine, D2H of
+    the combined output."""
+    w = inp.w
+    T, H, E, K, R, N = w.T, w.H, w.E, w.K, w.R, inp.num_valid
+    h_idx = torch.from_numpy(inp.topk_idx).pin_memory()
+    h_w = torch.from_numpy(inp.topk_weights).pin_memory()
+    h_x = torch.from_numpy(inp.x.view(np.int16)).pin_memory()
+    h_y = torch.from_numpy(inp.y.view(np.int16)).pin_memory()
+    h_out = torch.empty((T, H), dtype=torch.int16).pin_memory()
+    with torch.cuda.stream(stream):
+        d_idx = torch.empty_like(h_idx, device=dev)
+        d_w = torch.empty_like(h_w, device=dev)
+        d_x = torch.empty_like(h_x, device=dev)
+        d_y = torch.empty_like(h_y, device=dev)
+        d_out = torch.empty((T, H), dtype=torch.int16, device=dev)
+        cnt = torch.empty(E, dtype=torch.int32, device=dev)
+        ntr = torch.empty(R, dtype=torch.int32, device=dev)
+        itr = torch.empty(T, R, dtype=torch.uint8, device=dev)
+        off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        recv = torch.empty(N, H, dtype=torch.int16, device=dev)
+    stream.synchronize()
+    handle = ep.ep_layout(d_idx, E, R, cnt, ntr, itr, off, stream=stream)
+
+    def one():
+        with torch.cuda.stream(stream):
+            d_idx.copy_(h_idx, non_blocking=True)
+            d_w.copy_(h_w, non_blocking=True)
+            d_x.copy_(h_x, non_blocking=True)
+            d_y.copy_(h_y, non_blocking=True)
+            ep.ep_layout(d_idx, E, R, cnt, ntr, itr, off, handle=handle, stream=stream)
+            ep.ep_dispatch(handle, d_x, ep.EP_DTYPE_BF16, recv, N, stream=stream)
+            ep.ep_combine(handle, d_y, d_out, topk_weights=d_w, stream=stream)
+            h_out.copy_(d_out, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    stream.synchronize()
+    steps = max(3, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    stream.synchronize()
+    handle.destroy()
+    h2d = h_idx.numel() * 8 + h_w.numel() * 4 + h_x.numel() * 2 + h_y.numel() * 2
+    return {"ms_per_step": e0.elapsed_time(e1) / steps, "h2d": h2d, "d2h": h_out.numel() * 2, "steps": steps}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def _oracle_step(oracle, inp):
+    w = inp.w
+    L = oracle.layout(inp.topk_idx, w.E, w.R)
+    N = int(L["expert_offsets"][-1])
+    oracle.dispatch_bf16(inp.x, L["row_of_slot"], N)
+    oracle.combine(inp.y, L["row_of_slot"], inp.topk_weights)
+    w = inp.w
+    return (bytes_layout(w.T, w.K, w.E, w.R) + bytes_dispatch_bf16(w.T, w.K, w.H, N)
+            + bytes_combine(w.T, w.K, w.H, N))
+
+
+def cpu_baseline(budget_s: float = 15.0):
+    """The oracle as it stands (single-threaded C) on a token sample of the
+    prefill workload; GB/s of the same algorithmic bytes."""
+    import oracle
+
+    oracle.build()
+    probe = gi.make(WORKLOAD, seed=0, T=256)
+    t0 = time.perf_counter()
+    _oracle_step(oracle, probe)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    T_s = int(min(gi.WORKLOADS[WORKLOAD].T, max(256, 256 * budget_s / dt)))
+    T_s -= T_s % 64
+    sample = gi.make(WORKLOAD, seed=0, T=T_s)
+    t0 = time.perf_counter()
+    nbytes = _oracle_step(oracle, sample)
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "host_cores": host_cores(),
+            "sample": f"first-seed prefill recipe with T={T_s} tokens (of 8192): layout + bf16 dispatch + "
+                      f"combine, {dt:.1f} s single-threaded"}
+
+
+def reference_arm(args, rank, world):
+    """The oracle timed on the host cores, one bounded token sample per step."""
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    per_step_budget = max(0.05, args.ref_budget / max(1, args.steps + args.warmup))
+    probe = gi.make(WORKLOAD, seed=0, T=128)
+    t0 = time.perf_counter()
+    _oracle_step(oracle, probe)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    T_s = int(min(gi.WORKLOADS[WORKLOAD].T, max(16, 128 * per_step_budget / dt)))
+    sample = gi.make(WORKLOAD, seed=0, T=T_s)
+    for _ in range(args.warmup):
+        _oracle_step(oracle, sample)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        nbytes += _oracle_step(oracle, sample)
+    dt = time.perf_counter() - t0
+    val = nbytes / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded numpy PCG64; recipe in gen/inputs.py)",
+        "config": {"workload": "prefill dispatch+combine: T=8192 H=7168 E=256 K=8 R=8 (token sample per step)",
+                   "T_sample": T_s},
+        "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "host_cores": host_cores(),
+                         "sample": f"T={T_s} tokens of the prefill recipe per step, single-threaded C oracle"},
+        "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-budget", type=float, default=90.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+    else:
+        gpu_arm(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

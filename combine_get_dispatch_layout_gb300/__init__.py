@@ -1,0 +1,159 @@
+"""GB300 MoE token dispatch / combine: thin Python binding over libep.so.
+
+Each function has the name of the C entry point it wraps (include/ep.h) and
+only marshals arguments: torch tensors become device pointers, the current
+torch CUDA stream becomes the stream argument, and a non-OK status raises
+EPError. All computation runs in the library's CUDA kernels; there is no CPU
+path. If libep.so is missing the first call raises, it never falls back.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB as _LIB_PATH, build
+
+EP_OK, EP_ERR_INVALID_ARG, EP_ERR_INVALID_EXPERT, EP_ERR_CAPACITY, EP_ERR_CUDA, EP_ERR_ALLOC = range(6)
+EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3 = 0, 1
+
+# Exported symbols declared in include/ep.h.
+EXPORTS = ("ep_layout", "ep_dispatch", "ep_combine", "ep_handle_query",
+           "ep_handle_copy_row_of_slot", "ep_handle_destroy", "ep_status_string")
+
+_lib = None
+
+
+class EPError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        super().__init__(f"{call} -> {status_string(status)} ({status})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libep.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libep.so is not built ({_LIB_PATH}); run "
+                               "combine_get_dispatch_layout_gb300.build.build()")
+        L = ctypes.CDLL(_LIB_PATH)
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        L.ep_layout.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, ctypes.POINTER(P), P]
+        L.ep_dispatch.argtypes = [P, P, i32, i32, P, P, P, P, P, i64, P]
+        L.ep_combine.argtypes = [P, P, i64, i32, P, P, P]
+        L.ep_handle_query.argtypes = [P, ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_int32)]
+        L.ep_handle_copy_row_of_slot.argtypes = [P, P, P]
+        L.ep_handle_destroy.argtypes = [P]
+        L.ep_status_string.argtypes = [i32]
+        L.ep_status_string.restype = ctypes.c_char_p
+        for name in EXPORTS[:-1]:
+            getattr(L, name).restype = i32
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().ep_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _fnptr(f):
+    """A ctypes CFUNCTYPE callback (or None) as a plain function pointer."""
+    return None if f is None else ctypes.cast(f, ctypes.c_void_p).value
+
+
+def _check(st: int, call: str) -> None:
+    if st != EP_OK:
+        raise EPError(st, call)
+
+
+class Handle:
+    """Owner of an ep_handle_t; destroyed explicitly or when garbage-collected."""
+
+    def __init__(self):
+        self.ptr = ctypes.c_void_p(None)
+
+    def __bool__(self):
+        return bool(self.ptr.value)
+
+    def destroy(self):
+        if self.ptr.value:
+            _check(lib().ep_handle_destroy(self.ptr), "ep_handle_destroy")
+            self.ptr = ctypes.c_void_p(None)
+
+    def __del__(self):
+        try:
+            if self.ptr.value and _lib is not None:
+                _lib.ep_handle_destroy(self.ptr)
+        except Exception:
+            pass
+
+
+def ep_layout(topk_idx, num_experts: int, num_ranks: int, num_tokens_per_expert,
+              num_tokens_per_rank, is_token_in_rank, expert_offsets, handle: Handle | None = None,
+              stream=None, alloc_fn=None, free_fn=None) -> Handle:
+    """Routing layout of topk_idx [T, K] int64 into the given int32/uint8 outputs.
+
+    Reuses `handle` if given (no allocation), else creates one. Returns the handle.
+    """
+    T, K = topk_idx.shape
+    h = handle if handle is not None else Handle()
+    st = lib().ep_layout(_ptr(topk_idx), T, K, num_experts, num_ranks, _ptr(num_tokens_per_expert),
+                         _ptr(num_tokens_per_rank), _ptr(is_token_in_rank), _ptr(expert_offsets),
+                         _fnptr(alloc_fn), _fnptr(free_fn), ctypes.byref(h.ptr), _stream(stream))
+    _check(st, "ep_layout")
+    return h
+
+
+def ep_dispatch(handle: Handle, x, out_dtype: int, recv_x, recv_capacity: int, recv_scales=None,
+                recv_src_token=None, recv_weights=None, topk_weights=None, stream=None) -> None:
+    """Permute x [T, H] bf16 into recv_x (bf16 [cap, H] or uint8 [cap, H] for fp8)."""
+    H = x.shape[-1]
+    st = lib().ep_dispatch(handle.ptr, _ptr(x), H, out_dtype, _ptr(topk_weights), _ptr(recv_x),
+                           _ptr(recv_scales), _ptr(recv_src_token), _ptr(recv_weights),
+                           int(recv_capacity), _stream(stream))
+    _check(st, "ep_dispatch")
+
+
+def ep_combine(handle: Handle, y, out, topk_weights=None, y_rows: int | None = None, stream=None) -> None:
+    """out [T, H] bf16 = weighted sum over each token's slots of y [rows, H] bf16."""
+    H = y.shape[-1] if y is not None else out.shape[-1]
+    rows = int(y.shape[0]) if y_rows is None else int(y_rows)
+    st = lib().ep_combine(handle.ptr, _ptr(y), rows, H, _ptr(topk_weights), _ptr(out), _stream(stream))
+    _check(st, "ep_combine")
+
+
+def ep_handle_query(handle: Handle) -> tuple[int, int]:
+    """(N, device error word) after the last ep_layout; synchronises its stream."""
+    n = ctypes.c_int64(0)
+    err = ctypes.c_int32(0)
+    st = lib().ep_handle_query(handle.ptr, ctypes.byref(n), ctypes.byref(err))
+    if st not in (EP_OK, EP_ERR_INVALID_EXPERT):
+        _check(st, "ep_handle_query")
+    return n.value, err.value
+
+
+def ep_handle_copy_row_of_slot(handle: Handle, dst, stream=None) -> None:
+    _check(lib().ep_handle_copy_row_of_slot(handle.ptr, _ptr(dst), _stream(stream)),
+           "ep_handle_copy_row_of_slot")
+
+
+def ep_handle_destroy(handle: Handle) -> None:
+    handle.destroy()

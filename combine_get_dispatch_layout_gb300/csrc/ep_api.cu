@@ -1,0 +1,310 @@
+// C ABI of libep.so: argument checks, handle lifecycle and kernel launches.
+//
+// The call set mirrors nccl_ep.cc (ncclEpCreateHandle -> ep_layout,
+// ncclEpDispatch -> ep_dispatch, ncclEpCombine -> ep_combine,
+// ncclEpHandleDestroy -> ep_handle_destroy, ncclEpHandleGetNumRecvTokens ->
+// ep_handle_query). Where that file asserts on a bad argument, these calls
+// return EP_ERR_INVALID_ARG before enqueuing anything. The handle owns one
+// device block (slot -> row map, layout scratch, a few state words) allocated
+// through the caller's hooks, and a pinned host mirror of the state words.
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "ep_internal.cuh"
+
+struct ep_handle {
+    int device = -1;
+    ep_alloc_fn alloc_fn = nullptr;
+    ep_free_fn free_fn = nullptr;
+    // routing of the last ep_layout
+    int T = 0, K = 0, E = 0, R = 0;
+    ep::LayoutPlan plan{};
+    cudaStream_t layout_stream = nullptr;
+    bool error_latched = false;
+    // capacities of the device block
+    int64_t cap_slots = 0, cap_chunk_cells = 0, cap_rank_cells = 0;
+    void* dev_block = nullptr;
+    int32_t* meta = nullptr;        // [ep::kMetaWords]
+    int32_t* row_of_slot = nullptr; // [cap_slots]
+    int32_t* chunk_cnt = nullptr;   // [cap_chunk_cells]
+    int32_t* block_rank = nullptr;  // [cap_rank_cells]
+    int32_t* host_meta = nullptr;   // pinned [ep::kMetaWords]
+};
+
+namespace {
+
+int default_alloc(void** p, size_t bytes) { return cudaMalloc(p, bytes) == cudaSuccess ? 0 : 1; }
+int default_free(void* p) { return cudaFree(p) == cudaSuccess ? 0 : 1; }
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+ep_status_t current_device_is(const ep_handle* h) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return EP_ERR_CUDA;
+    return dev == h->device ? EP_OK : EP_ERR_INVALID_ARG;
+}
+
+void release_block(ep_handle* h) {
+    if (h->dev_block) h->free_fn(h->dev_block);
+    h->dev_block = nullptr;
+    h->meta = h->row_of_slot = h->chunk_cnt = h->block_rank = nullptr;
+    h->cap_slots = h->cap_chunk_cells = h->cap_rank_cells = 0;
+}
+
+// (Re)allocate the device block for at least the given sizes; zeroes the state words.
+ep_status_t ensure_block(ep_handle* h, int64_t slots, int64_t chunk_cells, int64_t rank_cells,
+                         cudaStream_t stream) {
+    if (h->dev_block && slots <= h->cap_slots && chunk_cells <= h->cap_chunk_cells &&
+        rank_cells <= h->cap_rank_cells)
+        return EP_OK;
+    if (h->dev_block) {
+        // work already enqueued may still read the old block
+        if (cudaDeviceSynchronize() != cudaSuccess) return EP_ERR_CUDA;
+        release_block(h);
+    }
+    const size_t a = 256;
+    const size_t meta_b = round_up(sizeof(int32_t) * ep::kMetaWords, a);
+    const size_t rows_b = round_up(sizeof(int32_t) * static_cast<size_t>(slots > 0 ? slots : 1), a);
+    const size_t cnt_b = round_up(sizeof(int32_t) * static_cast<size_t>(chunk_cells > 0 ? chunk_cells : 1), a);
+    const size_t rank_b = round_up(sizeof(int32_t) * static_cast<size_t>(rank_cells > 0 ? rank_cells : 1), a);
+    void* block = nullptr;
+    if (h->alloc_fn(&block, meta_b + rows_b + cnt_b + rank_b) != 0 || block == nullptr) return EP_ERR_ALLOC;
+    char* base = static_cast<char*>(block);
+    h->dev_block = block;
+    h->meta = reinterpret_cast<int32_t*>(base);
+    h->row_of_slot = reinterpret_cast<int32_t*>(base + meta_b);
+    h->chunk_cnt = reinterpret_cast<int32_t*>(base + meta_b + rows_b);
+    h->block_rank = reinterpret_cast<int32_t*>(base + meta_b + rows_b + cnt_b);
+    h->cap_slots = slots;
+    h->cap_chunk_cells = chunk_cells;
+    h->cap_rank_cells = rank_cells;
+    // stream-ordered so the first layout on `stream` sees zeroed state words
+    if (cudaMemsetAsync(h->meta, 0, meta_b, stream) != cudaSuccess) return EP_ERR_CUDA;
+    return EP_OK;
+}
+
+// Read the state words written by the last layout (synchronises its stream).
+ep_status_t read_meta(ep_handle* h, int64_t* rows, int32_t* err) {
+    if (cudaMemcpyAsync(h->host_meta, h->meta, sizeof(int32_t) * ep::kMetaWords, cudaMemcpyDeviceToHost,
+                        h->layout_stream) != cudaSuccess)
+        return EP_ERR_CUDA;
+    if (cudaStreamSynchronize(h->layout_stream) != cudaSuccess) return EP_ERR_CUDA;
+    if (rows) *rows = h->host_meta[ep::kMetaRows];
+    if (err) *err = h->host_meta[ep::kMetaError];
+    if (h->host_meta[ep::kMetaError] != 0) h->error_latched = true;
+    return EP_OK;
+}
+
+// Rows that a consumer buffer must hold: skip the device read when the
+// buffer holds T*K rows, the most a routing can produce.
+ep_status_t check_rows(ep_handle* h, int64_t capacity) {
+    if (h->error_latched) return EP_ERR_INVALID_EXPERT;
+    const int64_t max_rows = static_cast<int64_t>(h->T) * h->K;
+    if (capacity >= max_rows) return EP_OK;
+    int64_t n = 0;
+    int32_t err = 0;
+    ep_status_t st = read_meta(h, &n, &err);
+    if (st != EP_OK) return st;
+    if (err != 0) return EP_ERR_INVALID_EXPERT;
+    return n > capacity ? EP_ERR_CAPACITY : EP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ep_status_t ep_layout(const int64_t* topk_idx, int T, int K, int E, int R,
+                      int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                      uint8_t* is_token_in_rank, int32_t* expert_offsets,
+                      ep_alloc_fn alloc_fn, ep_free_fn free_fn,
+                      ep_handle_t* handle, void* stream) {
+    if (!handle || !num_tokens_per_expert || !num_tokens_per_rank || !expert_offsets)
+        return EP_ERR_INVALID_ARG;
+    if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS || R < 1 || R > EP_MAX_RANKS ||
+        E % R != 0)
+        return EP_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(T) * K >= (int64_t{1} << 31)) return EP_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !is_token_in_rank)) return EP_ERR_INVALID_ARG;
+    if ((alloc_fn == nullptr) != (free_fn == nullptr)) return EP_ERR_INVALID_ARG;
+    if (!aligned(topk_idx, 8) || !aligned(num_tokens_per_expert, 4) || !aligned(num_tokens_per_rank, 4) ||
+        !aligned(expert_offsets, 4))
+        return EP_ERR_INVALID_ARG;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ep_handle* h = *handle;
+    bool created = false;
+    if (h == nullptr) {
+        h = new (std::nothrow) ep_handle();
+        if (!h) return EP_ERR_ALLOC;
+        created = true;
+        if (cudaGetDevice(&h->device) != cudaSuccess) { delete h; return EP_ERR_CUDA; }
+        h->alloc_fn = alloc_fn ? alloc_fn : default_alloc;
+        h->free_fn = free_fn ? free_fn : default_free;
+        if (cudaMallocHost(reinterpret_cast<void**>(&h->host_meta), sizeof(int32_t) * ep::kMetaWords) !=
+            cudaSuccess) {
+            delete h;
+            return EP_ERR_ALLOC;
+        }
+    } else {
+        ep_status_t st = current_device_is(h);
+        if (st != EP_OK) return st;
+    }
+
+    const ep::LayoutPlan plan = ep::make_layout_plan(T, K, E, R);
+    ep_status_t st = ensure_block(h, static_cast<int64_t>(T) * K,
+                                  static_cast<int64_t>(E) * plan.num_chunks,
+                                  static_cast<int64_t>(R) * plan.num_blocks, s);
+    if (st != EP_OK) {
+        if (created) {
+            cudaFreeHost(h->host_meta);
+            release_block(h);
+            delete h;
+        } else {
+            h->T = 0;   // the old block is gone: later calls on this handle move nothing
+        }
+        return st;
+    }
+    h->T = T; h->K = K; h->E = E; h->R = R;
+    h->plan = plan;
+    h->layout_stream = s;
+    h->error_latched = false;
+
+    cudaError_t err;
+    if (T == 0) {
+        err = cudaMemsetAsync(num_tokens_per_expert, 0, sizeof(int32_t) * E, s);
+        if (err == cudaSuccess) err = cudaMemsetAsync(num_tokens_per_rank, 0, sizeof(int32_t) * R, s);
+        if (err == cudaSuccess) err = cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E + 1), s);
+        if (err == cudaSuccess) err = cudaMemsetAsync(h->meta, 0, sizeof(int32_t) * ep::kMetaWords, s);
+    } else {
+        ep::LayoutArgs a{};
+        a.topk_idx = topk_idx;
+        a.num_tokens_per_expert = num_tokens_per_expert;
+        a.num_tokens_per_rank = num_tokens_per_rank;
+        a.is_token_in_rank = is_token_in_rank;
+        a.expert_offsets = expert_offsets;
+        a.row_of_slot = h->row_of_slot;
+        a.chunk_cnt = h->chunk_cnt;
+        a.block_rank = h->block_rank;
+        a.meta = h->meta;
+        err = ep::launch_layout(plan, a, s);
+    }
+    *handle = h;
+    return err == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+ep_status_t ep_dispatch(ep_handle_t handle, const void* x, int H, ep_dtype_t out_dtype,
+                        const float* topk_weights,
+                        void* recv_x, float* recv_scales, int32_t* recv_src_token,
+                        float* recv_weights, int64_t recv_capacity, void* stream) {
+    if (!handle) return EP_ERR_INVALID_ARG;
+    if (H < 8 || H % 8 != 0 || recv_capacity < 0) return EP_ERR_INVALID_ARG;
+    if (out_dtype != EP_DTYPE_BF16 && out_dtype != EP_DTYPE_FP8_E4M3) return EP_ERR_INVALID_ARG;
+    const bool fp8 = out_dtype == EP_DTYPE_FP8_E4M3;
+    if (fp8 && (H % 128 != 0 || !recv_scales || !aligned(recv_scales, 4))) return EP_ERR_INVALID_ARG;
+    if (recv_weights && !topk_weights) return EP_ERR_INVALID_ARG;
+    if (handle->T > 0 && (!x || !recv_x)) return EP_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(recv_x, 16) || !aligned(topk_weights, 4) || !aligned(recv_src_token, 4) ||
+        !aligned(recv_weights, 4))
+        return EP_ERR_INVALID_ARG;
+    ep_status_t st = current_device_is(handle);
+    if (st != EP_OK) return st;
+    st = check_rows(handle, recv_capacity);
+    if (st != EP_OK) return st;
+
+    ep::DispatchArgs a{};
+    a.x = x;
+    a.row_of_slot = handle->row_of_slot;
+    a.topk_weights = topk_weights;
+    a.recv_x = recv_x;
+    a.recv_scales = recv_scales;
+    a.recv_src_token = recv_src_token;
+    a.recv_weights = recv_weights;
+    a.recv_capacity = recv_capacity;
+    a.T = handle->T;
+    a.K = handle->K;
+    a.H = H;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t err = fp8 ? ep::launch_dispatch_fp8(a, s) : ep::launch_dispatch_bf16(a, s);
+    return err == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+ep_status_t ep_combine(ep_handle_t handle, const void* y, int64_t y_rows, int H,
+                       const float* topk_weights, void* out, void* stream) {
+    if (!handle) return EP_ERR_INVALID_ARG;
+    if (H < 8 || H % 8 != 0 || y_rows < 0) return EP_ERR_INVALID_ARG;
+    if (handle->T > 0 && !out) return EP_ERR_INVALID_ARG;
+    if (y_rows > 0 && !y) return EP_ERR_INVALID_ARG;
+    if (!aligned(y, 16) || !aligned(out, 16) || !aligned(topk_weights, 4)) return EP_ERR_INVALID_ARG;
+    ep_status_t st = current_device_is(handle);
+    if (st != EP_OK) return st;
+    st = check_rows(handle, y_rows);
+    if (st != EP_OK) return st;
+
+    ep::CombineArgs a{};
+    a.y = y;
+    a.row_of_slot = handle->row_of_slot;
+    a.topk_weights = topk_weights;
+    a.out = out;
+    a.y_rows = y_rows;
+    a.T = handle->T;
+    a.K = handle->K;
+    a.H = H;
+    cudaError_t err = ep::launch_combine(a, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+ep_status_t ep_handle_query(ep_handle_t handle, int64_t* num_recv_rows, int32_t* device_error) {
+    if (!handle) return EP_ERR_INVALID_ARG;
+    ep_status_t st = current_device_is(handle);
+    if (st != EP_OK) return st;
+    int64_t n = 0;
+    int32_t err = 0;
+    st = read_meta(handle, &n, &err);
+    if (st != EP_OK) return st;
+    if (num_recv_rows) *num_recv_rows = n;
+    if (device_error) *device_error = err;
+    return err != 0 ? EP_ERR_INVALID_EXPERT : EP_OK;
+}
+
+ep_status_t ep_handle_copy_row_of_slot(ep_handle_t handle, int32_t* dst, void* stream) {
+    if (!handle) return EP_ERR_INVALID_ARG;
+    const size_t bytes = sizeof(int32_t) * static_cast<size_t>(handle->T) * handle->K;
+    if (bytes == 0) return EP_OK;
+    if (!dst || !aligned(dst, 4)) return EP_ERR_INVALID_ARG;
+    ep_status_t st = current_device_is(handle);
+    if (st != EP_OK) return st;
+    return cudaMemcpyAsync(dst, handle->row_of_slot, bytes, cudaMemcpyDeviceToDevice,
+                           static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? EP_OK
+               : EP_ERR_CUDA;
+}
+
+ep_status_t ep_handle_destroy(ep_handle_t handle) {
+    if (!handle) return EP_OK;
+    int prev = -1;
+    cudaGetDevice(&prev);
+    const bool switch_dev = prev != handle->device;
+    if (switch_dev && cudaSetDevice(handle->device) != cudaSuccess) return EP_ERR_CUDA;
+    ep_status_t st = cudaDeviceSynchronize() == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+    release_block(handle);
+    if (handle->host_meta) cudaFreeHost(handle->host_meta);
+    delete handle;
+    if (switch_dev) cudaSetDevice(prev);
+    return st;
+}
+
+const char* ep_status_string(ep_status_t status) {
+    switch (status) {
+        case EP_OK: return "EP_OK";
+        case EP_ERR_INVALID_ARG: return "EP_ERR_INVALID_ARG";
+        case EP_ERR_INVALID_EXPERT: return "EP_ERR_INVALID_EXPERT";
+        case EP_ERR_CAPACITY: return "EP_ERR_CAPACITY";
+        case EP_ERR_CUDA: return "EP_ERR_CUDA";
+        case EP_ERR_ALLOC: return "EP_ERR_ALLOC";
+    }
+    return "EP_ERR_UNKNOWN";
+}
+
+}  // extern "C"

@@ -1,0 +1,136 @@
+// Combine: weighted top-k gather-reduce of expert outputs back to token order,
+//   out[t, :] = bf16( sum_k w[t,k] * y[row_of_slot[t,k], :] ).
+//
+// What is computed follows nccl_ep.cc, ncclEpCombine (low-latency branch:
+// expert outputs are combined with the fp32 topk_weights [T, K] into
+// out [T, hidden] of the input dtype) and NeMo fused_a2a,
+// HybridEPCombine.forward (rows come back in the original token order).
+// Reading where the pages are silent: fp32 fused multiply-adds in ascending k
+// starting from +0, skipping unused slots, then one round to nearest-even.
+//
+// GPU design: the work item is (token, column segment), one warp per item.
+// The warp compacts the token's used slots (ballot + popc) into shared memory
+// in ascending k, then for each of its 16-byte column vectors issues the loads
+// of up to 8 slots at once (16 loads in flight per lane) before accumulating
+// them in k order, so the gather keeps enough bytes in flight for HBM.
+#include <cuda_bf16.h>
+
+#include "ep_internal.cuh"
+
+namespace ep {
+
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+constexpr int kUnroll = 2;      // 16-byte column vectors per lane per item
+constexpr int kGroup = 8;       // slots whose loads are issued together
+
+__device__ __forceinline__ int4 ld_stream(const int4* p) {
+    int4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void fma8(float* acc, float w, const int4& v) {
+    const unsigned u[4] = {static_cast<unsigned>(v.x), static_cast<unsigned>(v.y),
+                           static_cast<unsigned>(v.z), static_cast<unsigned>(v.w)};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = __fmaf_rn(w, __uint_as_float(u[i] << 16), acc[2 * i]);
+        acc[2 * i + 1] = __fmaf_rn(w, __uint_as_float(u[i] & 0xffff0000u), acc[2 * i + 1]);
+    }
+}
+
+__device__ __forceinline__ unsigned pack_bf16x2(float lo, float hi) {
+    const unsigned short l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+    const unsigned short h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+    return static_cast<unsigned>(l) | (static_cast<unsigned>(h) << 16);
+}
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+combine_kernel(CombineArgs a, int64_t num_items, int num_segments) {
+    __shared__ int s_row[kWarpsPerBlock][32];
+    __shared__ float s_w[kWarpsPerBlock][32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t item = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp;
+    if (item >= num_items) return;
+    const int t = static_cast<int>(item / num_segments);
+    const int seg = static_cast<int>(item - static_cast<int64_t>(t) * num_segments);
+    const int H16 = a.H / 8;
+
+    int row = -1;
+    float w = 1.0f;
+    if (lane < a.K) {
+        row = __ldg(a.row_of_slot + static_cast<int64_t>(t) * a.K + lane);
+        if (a.topk_weights) w = __ldg(a.topk_weights + static_cast<int64_t>(t) * a.K + lane);
+    }
+    const unsigned used = __ballot_sync(kFullMask, row >= 0);
+    const int n_used = __popc(used);
+    if (row >= 0) {
+        const int pos = __popc(used & ((1u << lane) - 1u));   // ascending k order
+        s_row[warp][pos] = row;
+        s_w[warp][pos] = w;
+    }
+    __syncwarp();
+
+    const int4* y = reinterpret_cast<const int4*>(a.y);
+    int4* out = reinterpret_cast<int4*>(a.out) + static_cast<int64_t>(t) * H16;
+    const int j0 = seg * (32 * kUnroll) + lane;
+
+    float acc[kUnroll][8];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
+
+    for (int g = 0; g < n_used; g += kGroup) {
+        int4 v[kUnroll][kGroup];
+#pragma unroll
+        for (int i = 0; i < kGroup; ++i) {
+            if (g + i < n_used) {
+                const int4* yr = y + static_cast<int64_t>(s_row[warp][g + i]) * H16;
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int j = j0 + u * 32;
+                    if (j < H16) v[u][i] = ld_stream(yr + j);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kGroup; ++i) {
+            if (g + i < n_used) {
+                const float wk = s_w[warp][g + i];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) fma8(acc[u], wk, v[u][i]);
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const int j = j0 + u * 32;
+        if (j < H16) {
+            int4 o;
+            o.x = static_cast<int>(pack_bf16x2(acc[u][0], acc[u][1]));
+            o.y = static_cast<int>(pack_bf16x2(acc[u][2], acc[u][3]));
+            o.z = static_cast<int>(pack_bf16x2(acc[u][4], acc[u][5]));
+            o.w = static_cast<int>(pack_bf16x2(acc[u][6], acc[u][7]));
+            out[j] = o;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
+    const int H16 = a.H / 8;
+    const int per_item = 32 * kUnroll;
+    const int segs = (H16 + per_item - 1) / per_item;
+    const int64_t items = static_cast<int64_t>(a.T) * segs;
+    if (items == 0) return cudaSuccess;
+    const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    combine_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a, items, segs);
+    return cudaGetLastError();
+}
+
+}  // namespace ep

@@ -1,0 +1,174 @@
+// Dispatch: stable expert-major permute of token rows into the receive buffer,
+// optionally quantised to e4m3 with one fp32 scale per 128 channels.
+//
+// What is computed follows nccl_ep.cc, ncclEpDispatch (tokens are bf16 rows;
+// the fp8 path writes fp32 scales shaped [rows, hidden/128]) and the DeepEP
+// API docs, "dispatch()" (do_expand: every (token, expert) pair gets its own
+// received row). Readings where the pages are silent: scale = amax / 448 with
+// IEEE division, q = e4m3(x / scale) rounded to nearest-even and saturated to
+// +-448, and an all-zero block gives scale 0 and zero bytes.
+//
+// GPU design: the work item is (token, column segment), one warp per item.
+// The warp reads its slice of the token row once with 16-byte loads and
+// writes it to each of the token's K receive rows with 16-byte (bf16) or
+// 8-byte (fp8) streaming stores, so x is read once although it is written K
+// times. For fp8, a lane holds 8 channels, 16 lanes one 128-channel block; the
+// block amax is a 4-step xor-shuffle max, and the scale and codes are computed
+// once per token and reused for all K copies.
+#include "ep_internal.cuh"
+
+namespace ep {
+
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+constexpr int kBf16Unroll = 4;     // 16-byte vectors per lane per item
+constexpr int kFp8Unroll = 4;      // 256-channel groups per item
+
+__device__ __forceinline__ int4 ld_stream(const int4* p) {
+    int4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+// Row of each slot of token t, lane k holds slot k (K <= 32); -1 if unused.
+__device__ __forceinline__ int slot_row(const int32_t* row_of_slot, int t, int K, int lane) {
+    return lane < K ? __ldg(row_of_slot + static_cast<int64_t>(t) * K + lane) : -1;
+}
+
+__device__ __forceinline__ void write_side_outputs(const DispatchArgs& a, int t, int lane, int row) {
+    if (lane < a.K && row >= 0) {
+        if (a.recv_src_token) a.recv_src_token[row] = t;
+        if (a.recv_weights) a.recv_weights[row] = __ldg(a.topk_weights + static_cast<int64_t>(t) * a.K + lane);
+    }
+}
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+dispatch_bf16_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
+    const int lane = threadIdx.x & 31;
+    const int64_t item = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (item >= num_items) return;
+    const int t = static_cast<int>(item / num_segments);
+    const int seg = static_cast<int>(item - static_cast<int64_t>(t) * num_segments);
+    const int H16 = a.H / 8;                          // 16-byte vectors per row
+    const int row = slot_row(a.row_of_slot, t, a.K, lane);
+    if (seg == 0) write_side_outputs(a, t, lane, row);
+
+    const int4* src = reinterpret_cast<const int4*>(a.x) + static_cast<int64_t>(t) * H16;
+    int4* dst = reinterpret_cast<int4*>(a.recv_x);
+    const int j0 = seg * (32 * kBf16Unroll) + lane;
+    int4 v[kBf16Unroll];
+#pragma unroll
+    for (int u = 0; u < kBf16Unroll; ++u) {
+        const int j = j0 + u * 32;
+        if (j < H16) v[u] = ld_stream(src + j);
+    }
+    for (int k = 0; k < a.K; ++k) {
+        const int r = __shfl_sync(kFullMask, row, k);
+        if (r < 0) continue;
+        int4* d = dst + static_cast<int64_t>(r) * H16;
+#pragma unroll
+        for (int u = 0; u < kBf16Unroll; ++u) {
+            const int j = j0 + u * 32;
+            if (j < H16) __stcs(d + j, v[u]);
+        }
+    }
+}
+
+// Two fp32 values -> two e4m3 codes (RNE, satfinite); `lo` goes to the low byte.
+__device__ __forceinline__ unsigned short e4m3x2(float lo, float hi) {
+    unsigned short d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+__device__ __forceinline__ float bf16_lo(unsigned u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(unsigned u) { return __uint_as_float(u & 0xffff0000u); }
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+dispatch_fp8_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
+    const int lane = threadIdx.x & 31;
+    const int64_t item = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (item >= num_items) return;
+    const int t = static_cast<int>(item / num_segments);
+    const int seg = static_cast<int>(item - static_cast<int64_t>(t) * num_segments);
+    const int H16 = a.H / 8;                          // 8-channel groups per row
+    const int nb = a.H / 128;                         // scale blocks per row
+    const int row = slot_row(a.row_of_slot, t, a.K, lane);
+    if (seg == 0) write_side_outputs(a, t, lane, row);
+
+    const int4* src = reinterpret_cast<const int4*>(a.x) + static_cast<int64_t>(t) * H16;
+    uint2 q[kFp8Unroll];
+    float scale[kFp8Unroll];
+    const int g0 = seg * (32 * kFp8Unroll) + lane;    // 8-channel group index
+#pragma unroll
+    for (int u = 0; u < kFp8Unroll; ++u) {
+        const int g = g0 + u * 32;
+        int4 v = make_int4(0, 0, 0, 0);
+        if (g < H16) v = ld_stream(src + g);
+        float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                      bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+#pragma unroll
+        for (int d = 8; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, d));
+        // m is now the amax of this lane's 128-channel block (16 lanes)
+        if (m == 0.0f) {
+            scale[u] = 0.0f;
+            q[u] = make_uint2(0u, 0u);
+        } else {
+            const float s = __fdiv_rn(m, 448.0f);
+            scale[u] = s;
+            unsigned w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const unsigned short p = e4m3x2(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
+                w[i] = p;
+            }
+            q[u] = make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+        }
+    }
+    uint2* dst = reinterpret_cast<uint2*>(a.recv_x);   // 8 codes per lane
+    for (int k = 0; k < a.K; ++k) {
+        const int r = __shfl_sync(kFullMask, row, k);
+        if (r < 0) continue;
+        uint2* d = dst + static_cast<int64_t>(r) * H16;
+        float* srow = a.recv_scales + static_cast<int64_t>(r) * nb;
+#pragma unroll
+        for (int u = 0; u < kFp8Unroll; ++u) {
+            const int g = g0 + u * 32;
+            if (g < H16) {
+                __stcs(d + g, q[u]);
+                if ((lane & 15) == 0) __stcs(srow + g / 16, scale[u]);
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch_bf16(const DispatchArgs& a, cudaStream_t stream) {
+    const int H16 = a.H / 8;
+    const int per_item = 32 * kBf16Unroll;
+    const int segs = (H16 + per_item - 1) / per_item;
+    const int64_t items = static_cast<int64_t>(a.T) * segs;
+    if (items == 0) return cudaSuccess;
+    const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    dispatch_bf16_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a, items, segs);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_fp8(const DispatchArgs& a, cudaStream_t stream) {
+    const int H16 = a.H / 8;
+    const int per_item = 32 * kFp8Unroll;
+    const int segs = (H16 + per_item - 1) / per_item;
+    const int64_t items = static_cast<int64_t>(a.T) * segs;
+    if (items == 0) return cudaSuccess;
+    const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    dispatch_fp8_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a, items, segs);
+    return cudaGetLastError();
+}
+
+}  // namespace ep

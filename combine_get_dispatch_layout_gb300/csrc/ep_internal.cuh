@@ -1,0 +1,79 @@
+// Internal declarations shared by the translation units of libep.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ep.h"
+
+namespace ep {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// Layout of the handle's small device word block.
+enum MetaWord : int {
+    kMetaDone = 0,   // blocks of the count kernel that have finished (reset by the last)
+    kMetaRows = 1,   // N = number of valid slots
+    kMetaError = 2,  // EP_ERR_INVALID_EXPERT once an id outside [-1, E) was seen
+    kMetaErrorAccum = 3,  // set by any block that sees a bad id; folded into kMetaError
+    kMetaWords = 4,
+};
+
+// Chunking of the routing table for the two layout kernels: each warp owns a
+// chunk of `chunk_tokens` consecutive tokens; `warps_per_block` warps form a block.
+struct LayoutPlan {
+    int T, K, E, R, L;
+    int chunk_tokens;
+    int num_chunks;
+    int warps_per_block;
+    int num_blocks;
+    int mask_words;          // 32-bit words per token in the block's rank bitmask
+    size_t smem_count;       // dynamic shared memory of the count kernel
+    size_t smem_assign;      // dynamic shared memory of the assign kernel
+};
+
+LayoutPlan make_layout_plan(int T, int K, int E, int R);
+
+struct LayoutArgs {
+    const int64_t* topk_idx;
+    int32_t* num_tokens_per_expert;
+    int32_t* num_tokens_per_rank;
+    uint8_t* is_token_in_rank;
+    int32_t* expert_offsets;
+    int32_t* row_of_slot;      // [T*K]
+    int32_t* chunk_cnt;        // [E][num_chunks]: counts, then exclusive bases
+    int32_t* block_rank;       // [R][num_blocks]: per-block tokens per rank
+    int32_t* meta;             // [kMetaWords]
+};
+
+cudaError_t launch_layout(const LayoutPlan& p, const LayoutArgs& a, cudaStream_t stream);
+
+struct DispatchArgs {
+    const void* x;             // bf16 [T, H]
+    const int32_t* row_of_slot;
+    const float* topk_weights; // [T, K] or null
+    void* recv_x;
+    float* recv_scales;
+    int32_t* recv_src_token;
+    float* recv_weights;
+    int64_t recv_capacity;
+    int T, K, H;
+};
+
+cudaError_t launch_dispatch_bf16(const DispatchArgs& a, cudaStream_t stream);
+cudaError_t launch_dispatch_fp8(const DispatchArgs& a, cudaStream_t stream);
+
+struct CombineArgs {
+    const void* y;             // bf16 [y_rows, H]
+    const int32_t* row_of_slot;
+    const float* topk_weights; // [T, K] or null (all ones)
+    void* out;                 // bf16 [T, H]
+    int64_t y_rows;
+    int T, K, H;
+};
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace ep

@@ -1,0 +1,192 @@
+/*
+ * ep.h -- C ABI of the GB300 MoE token dispatch / combine library (libep.so).
+ *
+ * One GPU, one process. The R "ranks" of expert parallelism are logical
+ * slabs of one receive buffer in this GPU's memory: expert e belongs to
+ * rank e / (E / R), and rank r's slab is receive rows
+ * [expert_offsets[r*E/R], expert_offsets[(r+1)*E/R]).
+ *
+ * Calls and the passages they follow (page title, then section):
+ *   ep_layout          nccl_ep.cc, ncclEpCreateHandle (handle built from
+ *                      topk_idx) and struct ncclEpHandle (is_token_in_rank,
+ *                      num_tokens_for_experts, sparse_to_dense_map);
+ *                      DeepEP API docs, "Prefix Sum Interpretation for Expert
+ *                      Token Counts" and "Computing with Handle Metadata".
+ *   ep_dispatch        nccl_ep.cc, ncclEpDispatch; DeepEP API docs,
+ *                      "dispatch()" with do_expand (one row per (token,
+ *                      expert) pair).
+ *   ep_combine         nccl_ep.cc, ncclEpCombine (low-latency branch:
+ *                      weighted by topk_weights); NeMo fused_a2a,
+ *                      HybridEPCombine.forward (rows back in token order).
+ *   ep_handle_destroy  nccl_ep.cc, ncclEpHandleDestroy.
+ *   ep_handle_query    nccl_ep.cc, ncclEpHandleGetNumRecvTokens.
+ *
+ * Conventions for every call:
+ *  - Pointers named as device pointers must be device memory (or managed
+ *    memory) of the GPU that is current on the calling thread. The caller
+ *    owns them; the library never frees caller memory.
+ *  - All device work is enqueued on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream) and is asynchronous, except where a call says it
+ *    synchronises.
+ *  - Arguments are checked on the host first. A failed check returns
+ *    EP_ERR_INVALID_ARG and enqueues nothing.
+ *  - Row buffers (x, recv_x, y, out) must be 16-byte aligned.
+ *  - A handle may be used from one host thread at a time.
+ */
+#ifndef EP_GB300_EP_H
+#define EP_GB300_EP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define EP_API __attribute__((visibility("default")))
+#else
+#define EP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    EP_OK = 0,
+    EP_ERR_INVALID_ARG = 1,    /* bad pointer, size, alignment or dtype       */
+    EP_ERR_INVALID_EXPERT = 2, /* a topk_idx entry outside [-1, E) was seen   */
+    EP_ERR_CAPACITY = 3,       /* receive buffer smaller than the valid rows  */
+    EP_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed        */
+    EP_ERR_ALLOC = 5           /* the allocation hook (or cudaMalloc) failed  */
+} ep_status_t;
+
+typedef enum {
+    EP_DTYPE_BF16 = 0,         /* receive rows are the bf16 token rows        */
+    EP_DTYPE_FP8_E4M3 = 1      /* receive rows are e4m3 bytes + fp32 scales   */
+} ep_dtype_t;
+
+/* Opaque routing handle: owns the slot -> row map [T*K] int32, the layout
+ * scratch and a small pinned host mirror. Keeps no pointer to topk_idx. */
+typedef struct ep_handle* ep_handle_t;
+
+/* Device-memory hooks (return 0 on success). NULL = cudaMalloc / cudaFree. */
+typedef int (*ep_alloc_fn)(void** ptr, size_t bytes);
+typedef int (*ep_free_fn)(void* ptr);
+
+/* Limits checked on the host. */
+#define EP_MAX_EXPERTS 4096
+#define EP_MAX_RANKS 1024
+#define EP_MAX_TOPK 32
+
+/*
+ * ep_layout -- routing layout of topk_idx (the "get dispatch layout" step).
+ *
+ *  topk_idx               device, int64 [T, K] row-major. Entry e in [0, E)
+ *                         routes the slot to expert e; -1 marks an unused
+ *                         (dropped) slot. Any other value is an invalid
+ *                         expert: that slot is treated as unused and the
+ *                         handle latches EP_ERR_INVALID_EXPERT (see
+ *                         ep_handle_query).
+ *  T, K, E, R             tokens, top-k, experts, logical ranks.
+ *                         1 <= K <= EP_MAX_TOPK, 1 <= E <= EP_MAX_EXPERTS,
+ *                         1 <= R <= EP_MAX_RANKS, E % R == 0, T >= 0,
+ *                         T*K < 2^31.
+ *  num_tokens_per_expert  device, int32 [E]: slots routed to each expert.
+ *  num_tokens_per_rank    device, int32 [R]: tokens with at least one slot
+ *                         on the rank (a token counts once per rank).
+ *  is_token_in_rank       device, uint8 [T, R]: 1 if token t has a slot on
+ *                         rank r, else 0.
+ *  expert_offsets         device, int32 [E + 1]: exclusive prefix sum of
+ *                         num_tokens_per_expert; expert_offsets[E] = N, the
+ *                         number of valid slots. Expert e owns receive rows
+ *                         [expert_offsets[e], expert_offsets[e+1]), filled in
+ *                         ascending (token, k) order.
+ *  alloc_fn, free_fn      device-memory hooks for a new handle (may be NULL).
+ *  handle                 in/out. If *handle is NULL a new handle is created
+ *                         (allocates device memory, pinned host memory and
+ *                         synchronises the device once). If *handle is an
+ *                         existing handle it is reused; it grows (after a
+ *                         stream synchronise) only if T*K or the chunking
+ *                         outgrows it. Reuse is stream-ordered: earlier work
+ *                         that reads the handle must be on `stream` or
+ *                         finished.
+ * Writes every element of the four outputs; needs no zeroed memory.
+ * Two kernel launches, no host synchronisation (except on creation/growth).
+ */
+EP_API ep_status_t ep_layout(const int64_t* topk_idx, int T, int K, int E, int R,
+                      int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                      uint8_t* is_token_in_rank, int32_t* expert_offsets,
+                      ep_alloc_fn alloc_fn, ep_free_fn free_fn,
+                      ep_handle_t* handle, void* stream);
+
+/*
+ * ep_dispatch -- stable expert-major permute of the token rows.
+ *
+ * For every valid slot (t, k) with receive row n = row_of_slot[t, k]:
+ *   EP_DTYPE_BF16:     recv_x[n, :] = x[t, :]                 (bf16 [cap, H])
+ *   EP_DTYPE_FP8_E4M3: per 128-channel block b of token t,
+ *                      amax = max |x[t, 128b : 128b+128]|,
+ *                      scale = amax / 448 (fp32, IEEE division),
+ *                      recv_x[n, c] = e4m3 satfinite RNE of x[t, c] / scale
+ *                      (uint8 [cap, H]), recv_scales[n, b] = scale
+ *                      (fp32 [cap, H/128] row-major). An all-zero block has
+ *                      scale 0 and zero bytes.
+ *   recv_src_token[n] = t          (optional, int32 [cap], NULL = skip)
+ *   recv_weights[n] = topk_weights[t, k]  (optional, fp32 [cap]; needs
+ *                                  topk_weights; NULL = skip)
+ * x is bf16 [T, H] (device); H % 8 == 0, and H % 128 == 0 for fp8.
+ * Rows >= N of the receive buffers are not written.
+ * recv_capacity is the number of rows the receive buffers hold. If it is
+ * below T*K the call reads N from the device (one stream synchronise) and
+ * returns EP_ERR_CAPACITY, enqueuing nothing, when N > recv_capacity.
+ * Returns EP_ERR_INVALID_EXPERT if the handle is known to have seen an
+ * invalid expert id.
+ */
+EP_API ep_status_t ep_dispatch(ep_handle_t handle, const void* x, int H, ep_dtype_t out_dtype,
+                        const float* topk_weights,
+                        void* recv_x, float* recv_scales, int32_t* recv_src_token,
+                        float* recv_weights, int64_t recv_capacity, void* stream);
+
+/*
+ * ep_combine -- weighted top-k gather-reduce back to token order.
+ *
+ *   out[t, h] = bf16_rne( sum over k = 0..K-1 with row_of_slot[t,k] >= 0 of
+ *                         w[t,k] * y[row_of_slot[t,k], h] )
+ * accumulated in fp32 with fused multiply-adds in ascending k from +0, and
+ * rounded once. topk_weights is fp32 [T, K] (device) or NULL for all-ones.
+ * y is bf16 [y_rows, H] (device), out is bf16 [T, H] (device), H % 8 == 0.
+ * A token with no valid slot gets +0. If y_rows < T*K the call reads N
+ * (one stream synchronise) and returns EP_ERR_CAPACITY when N > y_rows.
+ */
+EP_API ep_status_t ep_combine(ep_handle_t handle, const void* y, int64_t y_rows, int H,
+                       const float* topk_weights, void* out, void* stream);
+
+/*
+ * ep_handle_query -- synchronous read of the handle's device state after the
+ * last ep_layout: N (number of valid slots = receive rows) and the device
+ * error word (0, or EP_ERR_INVALID_EXPERT). Synchronises the layout stream.
+ * Returns EP_ERR_INVALID_EXPERT if the error word is set (outputs still
+ * filled). Either output pointer may be NULL.
+ */
+EP_API ep_status_t ep_handle_query(ep_handle_t handle, int64_t* num_recv_rows, int32_t* device_error);
+
+/*
+ * ep_handle_copy_row_of_slot -- copy the handle's slot -> row map
+ * (int32 [T, K], -1 for unused slots) into dst (device, caller-owned),
+ * enqueued on stream.
+ */
+EP_API ep_status_t ep_handle_copy_row_of_slot(ep_handle_t handle, int32_t* dst, void* stream);
+
+/*
+ * ep_handle_destroy -- free the handle's device and pinned memory (with its
+ * own free hook). Synchronises the device first so no enqueued work still
+ * reads it. NULL is a no-op.
+ */
+EP_API ep_status_t ep_handle_destroy(ep_handle_t handle);
+
+/* Human-readable name of a status code (static storage). */
+EP_API const char* ep_status_string(ep_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_GB300_EP_H */

@@ -1,0 +1,94 @@
+"""CPU-only checks of the C ABI library: it builds, loads, exports every
+symbol include/ep.h declares, rejects bad arguments on the host before any
+CUDA call, and the binding fails loudly when the library is missing."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from combine_get_dispatch_layout_gb300.build import build
+    import combine_get_dispatch_layout_gb300 as ep
+
+    build()
+    return ep.lib()
+
+
+def declared_symbols():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            names += re.findall(r"EP_API\s+[\w\s\*]+?\b(ep_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_symbols()
+    assert len(names) >= 7
+    for n in names:
+        assert hasattr(L, n), n
+    import combine_get_dispatch_layout_gb300 as ep
+    assert sorted(ep.EXPORTS) == names
+
+
+def test_status_strings(L):
+    import combine_get_dispatch_layout_gb300 as ep
+    assert ep.status_string(0) == "EP_OK"
+    assert ep.status_string(3) == "EP_ERR_CAPACITY"
+    assert ep.status_string(99) == "EP_ERR_UNKNOWN"
+
+
+def _layout(L, T=4, K=2, E=8, R=2, null_handle=False, idx=16, outs=(32, 32, 32, 32)):
+    h = ctypes.c_void_p(None)
+    return L.ep_layout(idx, T, K, E, R, *outs, None, None, None if null_handle else ctypes.byref(h), None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(null_handle=True),
+    dict(E=6, R=4),          # E % R != 0
+    dict(K=0), dict(K=33),   # top-k range
+    dict(E=0), dict(E=5000), dict(R=2000, E=2000),
+    dict(T=-1),
+    dict(T=1 << 28, K=8),    # T*K >= 2^31
+    dict(idx=None),          # T > 0 needs topk_idx
+    dict(idx=12),            # topk_idx not 8-byte aligned
+    dict(outs=(None, 32, 32, 32)),
+    dict(outs=(32, 32, 32, 34)),
+])
+def test_layout_rejects_bad_args(L, kw):
+    assert _layout(L, **kw) == 1
+
+
+def test_other_calls_reject_null_handle(L):
+    assert L.ep_dispatch(None, 16, 128, 0, None, 16, None, None, None, 10, None) == 1
+    assert L.ep_combine(None, 16, 10, 128, None, 16, None) == 1
+    assert L.ep_handle_query(None, None, None) == 1
+    assert L.ep_handle_copy_row_of_slot(None, 16, None) == 1
+    assert L.ep_handle_destroy(None) == 0
+
+
+def test_binding_fails_loudly_without_library(monkeypatch):
+    import combine_get_dispatch_layout_gb300 as ep
+    monkeypatch.setattr(ep, "_lib", None)
+    monkeypatch.setattr(ep, "_LIB_PATH", os.path.join(ROOT, "does-not-exist.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        ep.lib()
+
+
+def test_product_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "combine_get_dispatch_layout_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"\boracle\b", src), f"{f} mentions the oracle"
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".py", ".c", ".h")):
+            src = open(os.path.join(ROOT, "oracle", f)).read()
+            assert "combine_get_dispatch_layout_gb300" not in src and "libep" not in src

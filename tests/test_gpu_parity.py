@@ -1,0 +1,451 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle
+on the same seeded inputs.
+
+Bars: layout arrays, slot -> row map, permuted bf16 rows, fp8 bytes and
+scales, receive-side token ids and weights are bit-exact; combine is within
+1 bf16 ulp per element (the stated tolerance; both sides use the same fp32
+fused multiply-add order, so the test also reports exact matches).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gen import inputs as gi
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 8          # extra rows / bytes after every output, checked untouched
+SENT16 = 0x7BAD    # sentinel bf16 bits in guard rows
+SENT8 = 0xA5
+
+
+@pytest.fixture(scope="module")
+def ep():
+    import combine_get_dispatch_layout_gb300 as m
+    from combine_get_dispatch_layout_gb300.build import build
+
+    build()
+    m.lib()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.set_device(0)
+    return m
+
+
+def _dev(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.cuda() if dtype is None else t.cuda().view(dtype)
+
+
+def _u16(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def bf16_ulp_dist(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """Distance in bf16 units in the last place (sign-magnitude made monotonic)."""
+    def mono(u):
+        u = u.astype(np.int32)
+        return np.where(u & 0x8000, 0x8000 - u, u)
+    return np.abs(mono(a) - mono(b))
+
+
+class Run:
+    """One layout (+ optional dispatch / combine) on the GPU with guard bands."""
+
+    def __init__(self, ep, idx: np.ndarray, E: int, R: int, handle=None):
+        self.ep = ep
+        self.T, self.K = idx.shape
+        self.E, self.R = E, R
+        T, K = self.T, self.K
+        self.idx = _dev(idx)
+        self.cnt = torch.full((E + GUARD,), -7, dtype=torch.int32, device="cuda")
+        self.ntr = torch.full((R + GUARD,), -7, dtype=torch.int32, device="cuda")
+        self.itr = torch.full((T * R + GUARD,), SENT8, dtype=torch.uint8, device="cuda")
+        self.off = torch.full((E + 1 + GUARD,), -7, dtype=torch.int32, device="cuda")
+        self.h = ep.ep_layout(self.idx, E, R, self.cnt, self.ntr, self.itr, self.off, handle=handle)
+        self.rows = torch.full((T * K + GUARD,), -9, dtype=torch.int32, device="cuda")
+        ep.ep_handle_copy_row_of_slot(self.h, self.rows)
+        torch.cuda.synchronize()
+
+    def layout(self):
+        E, R, T, K = self.E, self.R, self.T, self.K
+        c, n, i, o, r = (self.cnt.cpu().numpy(), self.ntr.cpu().numpy(), self.itr.cpu().numpy(),
+                         self.off.cpu().numpy(), self.rows.cpu().numpy())
+        assert (c[E:] == -7).all() and (n[R:] == -7).all() and (i[T * R:] == SENT8).all()
+        assert (o[E + 1:] == -7).all() and (r[T * K:] == -9).all(), "guard band overwritten"
+        return dict(num_tokens_per_expert=c[:E], num_tokens_per_rank=n[:R],
+                    is_token_in_rank=i[:T * R].reshape(T, R), expert_offsets=o[:E + 1],
+                    row_of_slot=r[:T * K].reshape(T, K))
+
+
+def check_layout(run: Run, ref: dict):
+    got = run.layout()
+    for k in ["num_tokens_per_expert", "num_tokens_per_rank", "is_token_in_rank", "expert_offsets",
+              "row_of_slot"]:
+        np.testing.assert_array_equal(got[k], ref[k], err_msg=k)
+
+
+def dispatch_bf16(ep, run, x, N, weights=None):
+    T, H = x.shape
+    recv = torch.full((N + GUARD, H), SENT16, dtype=torch.int16, device="cuda")
+    src = torch.full((N + GUARD,), -5, dtype=torch.int32, device="cuda")
+    rw = torch.full((N + GUARD,), -3.0, dtype=torch.float32, device="cuda") if weights is not None else None
+    wt = _dev(weights) if weights is not None else None
+    ep.ep_dispatch(run.h, _dev(x.view(np.int16)), ep.EP_DTYPE_BF16, recv, N + GUARD,
+                   recv_src_token=src, recv_weights=rw, topk_weights=wt)
+    torch.cuda.synchronize()
+    r = recv.cpu().numpy().view(np.uint16)
+    s = src.cpu().numpy()
+    assert (r[N:] == SENT16).all() and (s[N:] == -5).all(), "rows >= N written"
+    w = None
+    if rw is not None:
+        w = rw.cpu().numpy()
+        assert (w[N:] == -3.0).all()
+        w = w[:N]
+    return r[:N], s[:N], w
+
+
+def dispatch_fp8(ep, run, x, N):
+    T, H = x.shape
+    q = torch.full((N + GUARD, H), SENT8, dtype=torch.uint8, device="cuda")
+    sc = torch.full((N + GUARD, H // 128), -1.0, dtype=torch.float32, device="cuda")
+    src = torch.full((N + GUARD,), -5, dtype=torch.int32, device="cuda")
+    ep.ep_dispatch(run.h, _dev(x.view(np.int16)), ep.EP_DTYPE_FP8_E4M3, q, N + GUARD, recv_scales=sc,
+                   recv_src_token=src)
+    torch.cuda.synchronize()
+    qn, sn = q.cpu().numpy(), sc.cpu().numpy()
+    assert (qn[N:] == SENT8).all() and (sn[N:] == -1.0).all(), "rows >= N written"
+    return qn[:N], sn[:N], src.cpu().numpy()[:N]
+
+
+def combine(ep, run, y, weights, H):
+    T = run.T
+    out = torch.full((T + 1, H), SENT16, dtype=torch.int16, device="cuda")
+    yd = _dev(y.view(np.int16)) if y is not None and y.shape[0] > 0 else None
+    wt = _dev(weights) if weights is not None else None
+    rows = 0 if y is None else y.shape[0]
+    if yd is None:
+        yd = torch.empty((1, H), dtype=torch.int16, device="cuda")
+    ep.ep_combine(run.h, yd, out, topk_weights=wt, y_rows=rows)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy().view(np.uint16)
+    assert (o[T:] == SENT16).all(), "combine wrote past T rows"
+    return o[:T]
+
+
+def assert_combine(got, want):
+    d = bf16_ulp_dist(got, want)
+    assert d.max() <= 1, f"combine off by {d.max()} ulp at {np.argwhere(d > 1)[:5]}"
+    # same fp32 fma order on both sides: expect exact equality
+    assert (d == 0).all(), f"{int((d > 0).sum())} of {d.size} elements differ by 1 ulp"
+
+
+def full_path(ep, inp, fp8=False, weights=True):
+    w = inp.w
+    ref = oracle.layout(inp.topk_idx, w.E, w.R)
+    assert ref["status"] == oracle.OK
+    run = Run(ep, inp.topk_idx, w.E, w.R)
+    check_layout(run, ref)
+    n, err = ep.ep_handle_query(run.h)
+    N = int(ref["expert_offsets"][-1])
+    assert (n, err) == (N, 0)
+    wt = inp.topk_weights if weights else None
+    r_x, r_src, r_w = oracle.dispatch_bf16(inp.x, ref["row_of_slot"], N, wt)
+    g_x, g_src, g_w = dispatch_bf16(ep, run, inp.x, N, wt)
+    np.testing.assert_array_equal(g_x, r_x)
+    np.testing.assert_array_equal(g_src, r_src)
+    if wt is not None:
+        np.testing.assert_array_equal(g_w.view(np.uint32), r_w.view(np.uint32))
+    if fp8:
+        r_q, r_s, r_src8, _ = oracle.dispatch_e4m3(inp.x, ref["row_of_slot"], N)
+        g_q, g_s, g_src8 = dispatch_fp8(ep, run, inp.x, N)
+        np.testing.assert_array_equal(g_s.view(np.uint32), r_s.view(np.uint32))
+        np.testing.assert_array_equal(g_q, r_q)
+        np.testing.assert_array_equal(g_src8, r_src8)
+    y = inp.y if inp.y is not None else r_x          # identity expert
+    got = combine(ep, run, y, wt, w.H)
+    want = oracle.combine(y, ref["row_of_slot"], wt)
+    assert_combine(got, want)
+    run.h.destroy()
+
+
+# ------------------------------------------------------------------ workloads
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny(ep, seed):
+    full_path(ep, gi.make("tiny", seed), fp8=True)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_decode(ep, seed):
+    full_path(ep, gi.make("decode", seed), fp8=True)
+
+
+def test_prefill_bf16(ep):
+    full_path(ep, gi.make("prefill", 0))
+
+
+def test_prefill_fp8(ep):
+    full_path(ep, gi.make("fp8", 0), fp8=True)
+
+
+def test_skewed(ep):
+    full_path(ep, gi.make("skewed", 0), fp8=True)
+
+
+@pytest.mark.parametrize("name,T", [("prefill", 777), ("skewed", 1001), ("fp8", 333)])
+def test_ragged_token_counts(ep, name, T):
+    full_path(ep, gi.make(name, 3, T=T), fp8=True)
+
+
+# ------------------------------------------------------------------ edge cases
+
+def _workload(T, H, E, K, R, **kw):
+    return gi.Workload("edge", T=T, H=H, E=E, K=K, R=R, **kw)
+
+
+@pytest.mark.parametrize("w", [
+    _workload(1, 128, 1, 1, 1),                          # T=1, K=1, E=R=1
+    _workload(37, 264, 5, 3, 5, drop_p=0.3),             # E == R, ragged H (not a multiple of 256)
+    _workload(100, 384, 16, 4, 1, drop_p=0.1),           # R == 1, odd number of fp8 blocks
+    _workload(513, 640, 64, 6, 4, routing="zipf", drop_p=0.05),
+    _workload(300, 8, 8, 8, 2),                          # H = 8 (one vector), K == E
+    _workload(64, 1152, 32, 32, 8),                      # K = 32 (maximum top-k)
+    _workload(200, 136, 4096, 8, 1024),                  # maximum E and R
+])
+def test_edge_shapes(ep, w):
+    inp = gi.make(w, 11)
+    full_path(ep, inp, fp8=(w.H % 128 == 0))
+
+
+def test_all_dropped(ep):
+    w = _workload(50, 256, 8, 2, 2, drop_p=1.0)
+    inp = gi.make(w, 0)
+    assert inp.num_valid == 0
+    full_path(ep, inp, fp8=True)
+
+
+def test_empty_tokens(ep):
+    idx = np.zeros((0, 4), np.int64)
+    run = Run(ep, idx, 8, 2)
+    got = run.layout()
+    assert (got["num_tokens_per_expert"] == 0).all() and (got["expert_offsets"] == 0).all()
+    assert (got["num_tokens_per_rank"] == 0).all()
+    assert ep.ep_handle_query(run.h) == (0, 0)
+
+
+def test_one_expert_takes_all(ep):
+    idx = np.full((4000, 1), 5, np.int64)
+    x = gi.normal_bf16(np.random.SeedSequence(4), 4000, 256)
+    inp = gi.Inputs(w=_workload(4000, 256, 8, 1, 4), seed=0, x=x, topk_idx=idx,
+                    topk_weights=np.ones((4000, 1), np.float32),
+                    y=gi.normal_bf16(np.random.SeedSequence(5), 4000, 256), num_valid=4000)
+    full_path(ep, inp, fp8=True)
+
+
+def test_duplicate_experts_in_token(ep):
+    rng = np.random.default_rng(0)
+    idx = rng.integers(0, 6, size=(500, 4)).astype(np.int64)
+    idx[rng.random((500, 4)) < 0.1] = -1
+    x = gi.normal_bf16(np.random.SeedSequence(6), 500, 128)
+    N = int((idx >= 0).sum())
+    inp = gi.Inputs(w=_workload(500, 128, 6, 4, 3), seed=0, x=x, topk_idx=idx,
+                    topk_weights=rng.random((500, 4)).astype(np.float32),
+                    y=gi.normal_bf16(np.random.SeedSequence(7), N, 128), num_valid=N)
+    full_path(ep, inp, fp8=True)
+
+
+def test_combine_signed_zeros_and_null_weights(ep):
+    rng = np.random.default_rng(1)
+    T, K, E, R, H = 64, 4, 8, 2, 256
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :K].astype(np.int64)
+    N = T * K
+    y = gi.normal_bf16(np.random.SeedSequence(8), N, H)
+    y[::3, ::5] = 0x8000        # -0
+    y[1::3, ::7] = 0x0000       # +0
+    inp = gi.Inputs(w=_workload(T, H, E, K, R), seed=0, x=gi.normal_bf16(np.random.SeedSequence(9), T, H),
+                    topk_idx=idx, topk_weights=np.zeros((T, K), np.float32), y=y, num_valid=N)
+    full_path(ep, inp)                     # all-zero weights: every output is +0
+    full_path(ep, inp, weights=False)      # NULL weights: plain sums
+
+
+def test_fp8_special_blocks(ep):
+    rng = np.random.default_rng(2)
+    T, H = 48, 1024
+    xf = (rng.standard_normal((T, H)) * 2).astype(np.float32)
+    xf[0, :128] = 0.0
+    xf[1, 128:256] = -0.0
+    xf[2, 256:384] = 1e-38
+    xf[3, 384:512] = 3e38
+    xf[4, :] = np.float32(2.0 ** -133)    # bf16 subnormal amax
+    xf[5, ::2] *= 1e4
+    x = gi.f32_to_bf16_bits(xf)
+    idx = np.argsort(rng.random((T, 16)), axis=1)[:, :3].astype(np.int64)
+    inp = gi.Inputs(w=_workload(T, H, 16, 3, 4), seed=0, x=x, topk_idx=idx,
+                    topk_weights=np.full((T, 3), 1 / 3, np.float32), y=None, num_valid=3 * T)
+    full_path(ep, inp, fp8=True)
+
+
+def test_fp8_encoder_sweep_all_bf16(ep):
+    """Every finite bf16 pattern through the quantiser under several block scales."""
+    pats = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    f = gi.bf16_bits_to_f32(pats)
+    pats = pats[np.isfinite(f)]
+    rows = []
+    for amax in [448.0, 1.0, 3.0, 1e-3, 7.5e7, 2.0 ** -120]:
+        vals = gi.bf16_bits_to_f32(pats)
+        vals = vals[np.abs(vals) <= amax]
+        per = 127
+        nblk = (len(vals) + per - 1) // per
+        blk = np.zeros((nblk, 128), np.float32)
+        flat = np.zeros(nblk * per, np.float32)
+        flat[:len(vals)] = vals
+        blk[:, :per] = flat.reshape(nblk, per)
+        blk[:, per] = amax
+        rows.append(blk)
+    allb = np.concatenate(rows)
+    H = 1024
+    nb = (len(allb) + 7) // 8
+    pad = np.zeros((nb * 8 - len(allb), 128), np.float32)
+    x = gi.f32_to_bf16_bits(np.concatenate([allb, pad]).reshape(nb, H))
+    idx = np.zeros((nb, 1), np.int64)
+    inp = gi.Inputs(w=_workload(nb, H, 1, 1, 1), seed=0, x=x, topk_idx=idx,
+                    topk_weights=np.ones((nb, 1), np.float32), y=None, num_valid=nb)
+    full_path(ep, inp, fp8=True)
+
+
+def test_invalid_expert_ids(ep):
+    rng = np.random.default_rng(3)
+    T, K, E, R = 200, 4, 16, 4
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :K].astype(np.int64)
+    idx[5, 1] = E
+    idx[17, 0] = -3
+    idx[100, 3] = 1 << 40
+    ref = oracle.layout(idx, E, R)
+    assert ref["status"] == oracle.ERR_EXPERT
+    run = Run(ep, idx, E, R)
+    check_layout(run, ref)                       # bad slots are treated as dropped
+    n, err = ep.ep_handle_query(run.h)
+    assert err == ep.EP_ERR_INVALID_EXPERT and n == int(ref["expert_offsets"][-1])
+    x = torch.zeros((T, 128), dtype=torch.bfloat16, device="cuda")
+    recv = torch.zeros((T * K, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ep.EPError) as e:
+        ep.ep_dispatch(run.h, x, ep.EP_DTYPE_BF16, recv, T * K)
+    assert e.value.status == ep.EP_ERR_INVALID_EXPERT
+    # a fresh layout with valid ids clears the latch on the same handle
+    idx2 = np.argsort(rng.random((T, E)), axis=1)[:, :K].astype(np.int64)
+    run2 = Run(ep, idx2, E, R, handle=run.h)
+    check_layout(run2, oracle.layout(idx2, E, R))
+    assert ep.ep_handle_query(run2.h)[1] == 0
+    ep.ep_dispatch(run2.h, x, ep.EP_DTYPE_BF16, recv, T * K)
+    run.h.destroy()
+
+
+def test_capacity_errors(ep):
+    rng = np.random.default_rng(4)
+    T, K, E, R, H = 100, 4, 8, 2, 64
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :K].astype(np.int64)
+    idx[rng.random((T, K)) < 0.5] = -1
+    N = int((idx >= 0).sum())
+    run = Run(ep, idx, E, R)
+    x = torch.zeros((T, H), dtype=torch.bfloat16, device="cuda")
+    small = torch.zeros((N - 1, H), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ep.EPError) as e:
+        ep.ep_dispatch(run.h, x, ep.EP_DTYPE_BF16, small, N - 1)
+    assert e.value.status == ep.EP_ERR_CAPACITY
+    exact = torch.zeros((N, H), dtype=torch.bfloat16, device="cuda")
+    ep.ep_dispatch(run.h, x, ep.EP_DTYPE_BF16, exact, N)     # exactly N rows is enough
+    out = torch.zeros((T, H), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ep.EPError) as e:
+        ep.ep_combine(run.h, small, out)
+    assert e.value.status == ep.EP_ERR_CAPACITY
+    ep.ep_combine(run.h, exact, out)
+    run.h.destroy()
+
+
+def test_handle_reuse_grow_and_shrink(ep):
+    h = None
+    for (T, K, E, R, seed) in [(64, 2, 8, 2, 0), (5000, 8, 256, 8, 1), (10, 3, 6, 3, 2), (20000, 6, 64, 4, 3)]:
+        rng = np.random.default_rng(seed)
+        idx = np.argsort(rng.random((T, E)), axis=1)[:, :K].astype(np.int64)
+        run = Run(ep, idx, E, R, handle=h)
+        h = run.h
+        check_layout(run, oracle.layout(idx, E, R))
+    h.destroy()
+
+
+def test_layout_repeatable_on_same_handle(ep):
+    """Back-to-back layouts on one handle (the done-counter reset path)."""
+    inp = gi.make("skewed", 5, with_y=False)
+    w = inp.w
+    ref = oracle.layout(inp.topk_idx, w.E, w.R)
+    h = None
+    for _ in range(5):
+        run = Run(ep, inp.topk_idx, w.E, w.R, handle=h)
+        h = run.h
+        check_layout(run, ref)
+    h.destroy()
+
+
+def test_side_stream(ep):
+    """Calls honour the stream they are given."""
+    inp = gi.make("decode", 4)
+    w = inp.w
+    ref = oracle.layout(inp.topk_idx, w.E, w.R)
+    N = int(ref["expert_offsets"][-1])
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        idx = _dev(inp.topk_idx)
+        x = _dev(inp.x.view(np.int16), torch.bfloat16)
+        cnt = torch.empty(w.E, dtype=torch.int32, device="cuda")
+        ntr = torch.empty(w.R, dtype=torch.int32, device="cuda")
+        itr = torch.empty(w.T, w.R, dtype=torch.uint8, device="cuda")
+        off = torch.empty(w.E + 1, dtype=torch.int32, device="cuda")
+        h = ep.ep_layout(idx, w.E, w.R, cnt, ntr, itr, off, stream=s)
+        recv = torch.empty(N, w.H, dtype=torch.bfloat16, device="cuda")
+        ep.ep_dispatch(h, x, ep.EP_DTYPE_BF16, recv, N, stream=s)
+    s.synchronize()
+    r_x, _, _ = oracle.dispatch_bf16(inp.x, ref["row_of_slot"], N)
+    np.testing.assert_array_equal(_u16(recv), r_x)
+    h.destroy()
+
+
+def test_alloc_hooks(ep):
+    """A caller-supplied allocator is used, and its failure is reported."""
+    import ctypes
+
+    calls = {"alloc": 0, "free": 0}
+    keep = {}
+
+    ALLOC = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t)
+    FREE = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_void_p)
+
+    @ALLOC
+    def alloc(pp, nbytes):
+        calls["alloc"] += 1
+        t = torch.empty(int(nbytes), dtype=torch.uint8, device="cuda")
+        keep[t.data_ptr()] = t
+        pp[0] = t.data_ptr()
+        return 0
+
+    @FREE
+    def free(p):
+        calls["free"] += 1
+        keep.pop(p, None)
+        return 0
+
+    @ALLOC
+    def failing(pp, nbytes):
+        return 1
+
+    idx = _dev(np.zeros((10, 2), np.int64))
+    outs = [torch.empty(4, dtype=torch.int32, device="cuda"), torch.empty(2, dtype=torch.int32, device="cuda"),
+            torch.empty(20, dtype=torch.uint8, device="cuda"), torch.empty(5, dtype=torch.int32, device="cuda")]
+    h = ep.ep_layout(idx, 4, 2, *outs, alloc_fn=alloc, free_fn=free)
+    torch.cuda.synchronize()
+    assert outs[3].cpu().tolist() == [0, 20, 20, 20, 20]
+    h.destroy()
+    assert calls == {"alloc": 1, "free": 1}
+    with pytest.raises(ep.EPError) as e:
+        ep.ep_layout(idx, 4, 2, *outs, alloc_fn=failing, free_fn=free)
+    assert e.value.status == ep.EP_ERR_ALLOC
