@@ -12,14 +12,13 @@ constexpr unsigned kFullMask = 0xffffffffu;
 
 // Layout of the handle's small device word block.
 enum MetaWord : int {
-    kMetaDone = 0,   // blocks of the count kernel that have finished (reset by the last)
-    kMetaRows = 1,   // N = number of valid slots
-    kMetaError = 2,  // EP_ERR_INVALID_EXPERT once an id outside [-1, E) was seen
-    kMetaErrorAccum = 3,  // set by any block that sees a bad id; folded into kMetaError
+    kMetaRows = 0,        // N = number of valid slots
+    kMetaError = 1,       // EP_ERR_INVALID_EXPERT once an id outside [-1, E) was seen
+    kMetaErrorAccum = 2,  // set by any block that sees a bad id; folded into kMetaError
     kMetaWords = 4,
 };
 
-// Chunking of the routing table for the two layout kernels: each warp owns a
+// Chunking of the routing table for the layout kernels: each warp owns a
 // chunk of `chunk_tokens` consecutive tokens; `warps_per_block` warps form a block.
 struct LayoutPlan {
     int T, K, E, R, L;
@@ -27,7 +26,6 @@ struct LayoutPlan {
     int num_chunks;
     int warps_per_block;
     int num_blocks;
-    int mask_words;          // 32-bit words per token in the block's rank bitmask
     size_t smem_count;       // dynamic shared memory of the count kernel
     size_t smem_assign;      // dynamic shared memory of the assign kernel
 };

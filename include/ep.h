@@ -109,7 +109,7 @@ typedef int (*ep_free_fn)(void* ptr);
  *                         that reads the handle must be on `stream` or
  *                         finished.
  * Writes every element of the four outputs; needs no zeroed memory.
- * Two kernel launches, no host synchronisation (except on creation/growth).
+ * Three kernel launches, no host synchronisation (except on creation/growth).
  */
 EP_API ep_status_t ep_layout(const int64_t* topk_idx, int T, int K, int E, int R,
                       int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
