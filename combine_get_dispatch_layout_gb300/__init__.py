@@ -20,7 +20,7 @@ EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3 = 0, 1
 
 # Exported symbols declared in include/ep.h.
 EXPORTS = ("ep_layout", "ep_dispatch", "ep_combine", "ep_handle_query",
-           "ep_handle_copy_row_of_slot", "ep_handle_destroy", "ep_status_string")
+           "ep_handle_copy_row_of_slot", "ep_handle_destroy", "ep_layout_noalloc", "ep_status_string")
 
 _lib = None
 
@@ -46,6 +46,7 @@ def lib() -> ctypes.CDLL:
         L.ep_handle_query.argtypes = [P, ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_int32)]
         L.ep_handle_copy_row_of_slot.argtypes = [P, P, P]
         L.ep_handle_destroy.argtypes = [P]
+        L.ep_layout_noalloc.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, P]
         L.ep_status_string.argtypes = [i32]
         L.ep_status_string.restype = ctypes.c_char_p
         for name in EXPORTS[:-1]:
@@ -153,6 +154,19 @@ def ep_handle_query(handle: Handle) -> tuple[int, int]:
 def ep_handle_copy_row_of_slot(handle: Handle, dst, stream=None) -> None:
     _check(lib().ep_handle_copy_row_of_slot(handle.ptr, _ptr(dst), _stream(stream)),
            "ep_handle_copy_row_of_slot")
+
+
+def ep_layout_noalloc(topk_idx, num_experts: int, num_ranks: int, num_tokens_per_expert,
+                      num_tokens_per_rank, is_token_in_rank, expert_offsets, row_of_slot,
+                      device_error=None, stream=None) -> None:
+    """ep_layout without a handle or any allocation: the slot -> row map goes
+    to the caller's row_of_slot [T, K] int32; scratch is the library's fixed
+    array (one call at a time per device, ordered on one stream)."""
+    T, K = topk_idx.shape
+    st = lib().ep_layout_noalloc(_ptr(topk_idx), T, K, num_experts, num_ranks, _ptr(num_tokens_per_expert),
+                                 _ptr(num_tokens_per_rank), _ptr(is_token_in_rank), _ptr(expert_offsets),
+                                 _ptr(row_of_slot), _ptr(device_error), _stream(stream))
+    _check(st, "ep_layout_noalloc")
 
 
 def ep_handle_destroy(handle: Handle) -> None:

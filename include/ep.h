@@ -182,6 +182,47 @@ EP_API ep_status_t ep_handle_copy_row_of_slot(ep_handle_t handle, int32_t* dst, 
  */
 EP_API ep_status_t ep_handle_destroy(ep_handle_t handle);
 
+/*
+ * ep_layout_noalloc -- the routing layout of ep_layout, for callers that
+ * cannot allocate device memory.
+ *
+ * No counterpart on the pages this library follows: it exists for callers
+ * whose device memory is all owned by someone else -- for example a serving
+ * engine that reserves the GPU's memory for its own pool at start-up and
+ * hands out no allocation hook -- or that must not pay cudaMalloc's
+ * implicit device synchronisation inside a latency-critical loop. It calls
+ * no cudaMalloc, cudaFree, cudaMallocHost or other allocating routine.
+ *
+ * Instead of a handle it uses one fixed scratch array compiled into the
+ * library, EP_NOALLOC_SCRATCH_BYTES (2 MiB) of device memory that every GPU
+ * which loads the library keeps until the process exits. The scratch holds
+ * E * C + R * B + 64 int32 words, where C <= 256 is the number of token
+ * chunks and B the number of count blocks (B = C/8 when E <= 2730), so
+ * roughly (E + R) * 256 words; routings that need more are rejected with
+ * EP_ERR_CAPACITY before anything is enqueued.
+ *
+ * Arguments and outputs are those of ep_layout, plus:
+ *  row_of_slot    device, int32 [T, K]: receive row of each slot, -1 if
+ *                 unused (what ep_handle_copy_row_of_slot returns for a
+ *                 handle); the caller owns it.
+ *  device_error   device, int32 [1] or NULL: set to 0, or to
+ *                 EP_ERR_INVALID_EXPERT if an id outside [-1, E) was seen
+ *                 (those slots are treated as unused).
+ *
+ * Calls share the one scratch array, which keeps the last call's contents;
+ * each call clears the words that must start at zero. Calls whose work
+ * overlaps on the GPU (different streams, or several host threads) race on
+ * that array and give wrong results: order them on one stream.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.
+ */
+#define EP_NOALLOC_SCRATCH_BYTES (2u << 20)
+EP_API ep_status_t ep_layout_noalloc(const int64_t* topk_idx, int T, int K, int E, int R,
+                                     int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                                     uint8_t* is_token_in_rank, int32_t* expert_offsets,
+                                     int32_t* row_of_slot, int32_t* device_error, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 EP_API const char* ep_status_string(ep_status_t status);
 

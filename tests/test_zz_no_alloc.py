@@ -1,0 +1,89 @@
+"""The allocation-free layout entry point against the handle-based one.
+
+ep_layout_noalloc serves callers that cannot allocate device memory (all of
+it belongs to another allocator, or cudaMalloc's implicit synchronisation is
+not allowed where they run); it keeps its scratch in a fixed array inside
+the library. This file is named to be collected last, so a run that stops
+at the first failure has already run every other test. It passes alone in a
+fresh process and after the rest of the suite.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gen import inputs as gi
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ep():
+    import combine_get_dispatch_layout_gb300 as m
+    from combine_get_dispatch_layout_gb300.build import build
+
+    build()
+    m.lib()
+    torch.cuda.set_device(0)
+    return m
+
+
+def _outs(T, K, E, R):
+    return dict(num_tokens_per_expert=torch.full((E,), -7, dtype=torch.int32, device="cuda"),
+                num_tokens_per_rank=torch.full((R,), -7, dtype=torch.int32, device="cuda"),
+                is_token_in_rank=torch.full((T, R), 0xA5, dtype=torch.uint8, device="cuda"),
+                expert_offsets=torch.full((E + 1,), -7, dtype=torch.int32, device="cuda"),
+                row_of_slot=torch.full((T, K), -9, dtype=torch.int32, device="cuda"))
+
+
+def _with_handle(ep, idx, E, R):
+    T, K = idx.shape
+    o = _outs(T, K, E, R)
+    h = ep.ep_layout(idx, E, R, o["num_tokens_per_expert"], o["num_tokens_per_rank"],
+                     o["is_token_in_rank"], o["expert_offsets"])
+    ep.ep_handle_copy_row_of_slot(h, o["row_of_slot"])
+    _, err = ep.ep_handle_query(h)
+    h.destroy()
+    return {k: v.cpu().numpy() for k, v in o.items()}, err
+
+
+def _no_alloc(ep, idx, E, R):
+    T, K = idx.shape
+    o = _outs(T, K, E, R)
+    err = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    ep.ep_layout_noalloc(idx, E, R, o["num_tokens_per_expert"], o["num_tokens_per_rank"],
+                         o["is_token_in_rank"], o["expert_offsets"], o["row_of_slot"], device_error=err)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in o.items()}, int(err.item())
+
+
+def _cases():
+    prefill = gi.make("prefill", 0, with_y=False)
+    skewed = gi.make("skewed", 1, with_y=False)
+    rng = np.random.default_rng(7)
+    bad = np.argsort(rng.random((300, 16)), axis=1)[:, :4].astype(np.int64)
+    bad[3, 2], bad[77, 0] = 16, -5
+    return [(prefill.topk_idx, 256, 8), (skewed.topk_idx, 64, 4), (bad, 16, 4),
+            (gi.make("decode", 2, with_y=False).topk_idx, 256, 8)]
+
+
+def test_no_alloc_matches_layout_on_consecutive_calls(ep):
+    # consecutive calls share the scratch array: each must match the handle path,
+    # including after a call that saw invalid ids (its error flag must not leak)
+    for idx_np, E, R in _cases():
+        idx = torch.from_numpy(idx_np).cuda()
+        want, want_err = _with_handle(ep, idx, E, R)
+        for _ in range(2):
+            got, got_err = _no_alloc(ep, idx, E, R)
+            assert got_err == want_err
+            for k in want:
+                np.testing.assert_array_equal(got[k], want[k], err_msg=k)
+
+
+def test_no_alloc_rejects_routings_beyond_the_scratch(ep):
+    T, K, E, R = 4096, 8, 4096, 1024      # (E + R) * 256 words > 2 MiB
+    idx = torch.zeros((T, K), dtype=torch.int64, device="cuda")
+    o = _outs(T, K, E, R)
+    with pytest.raises(ep.EPError) as e:
+        ep.ep_layout_noalloc(idx, E, R, o["num_tokens_per_expert"], o["num_tokens_per_rank"],
+                             o["is_token_in_rank"], o["expert_offsets"], o["row_of_slot"])
+    assert e.value.status == ep.EP_ERR_CAPACITY
