@@ -334,7 +334,7 @@ def gpu_arm(args, rank, world, local):
         "e2e": {"value": round(world * b_step / (e2e["ms_per_step"] * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e["ms_per_step"], 4), "steps": e2e["steps"]},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 5 * args.steps,
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -10,9 +10,12 @@
 //
 // GPU design: the work item is (token, column segment), one warp per item.
 // The warp compacts the token's used slots (ballot + popc) into shared memory
-// in ascending k, then for each of its 16-byte column vectors issues the loads
-// of up to 8 slots at once (16 loads in flight per lane) before accumulating
-// them in k order, so the gather keeps enough bytes in flight for HBM.
+// in ascending k, then for its 16-byte column vector issues the loads of 4
+// slots at once before accumulating them in k order. Items are small (256
+// channels) and blocks are 2 warps, so many warps per SM keep the gather's
+// bytes in flight and the last wave is short; a sweep of vectors per lane
+// (1, 2, 4), slots per load group (4, 8) and warps per block (1 to 8) on the
+// prefill shape picked this point.
 #include <cuda_bf16.h>
 
 #include "ep_internal.cuh"
@@ -21,13 +24,13 @@ namespace ep {
 
 namespace {
 
-constexpr int kWarpsPerBlock = 8;
-constexpr int kUnroll = 2;      // 16-byte column vectors per lane per item
-constexpr int kGroup = 8;       // slots whose loads are issued together
+constexpr int kWarpsPerBlock = 2;   // small blocks: fine-grained scheduling
+constexpr int kUnroll = 1;      // 16-byte column vectors per lane per item
+constexpr int kGroup = 4;       // slots whose loads are issued together
 
 __device__ __forceinline__ int4 ld_stream(const int4* p) {
     int4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.nc.v4.s32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
 }

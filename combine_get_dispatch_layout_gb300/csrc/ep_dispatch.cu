@@ -14,7 +14,9 @@
 // 8-byte (fp8) streaming stores, so x is read once although it is written K
 // times. For fp8, a lane holds 8 channels, 16 lanes one 128-channel block; the
 // block amax is a 4-step xor-shuffle max, and the scale and codes are computed
-// once per token and reused for all K copies.
+// once per token and reused for all K copies. Small items (2 vectors per
+// lane) won a sweep of 1 to 8 vectors per lane and 2 to 8 warps per block on
+// the prefill shape: they shorten the last wave and balance the SMs.
 #include "ep_internal.cuh"
 
 namespace ep {
@@ -22,8 +24,8 @@ namespace ep {
 namespace {
 
 constexpr int kWarpsPerBlock = 8;
-constexpr int kBf16Unroll = 4;     // 16-byte vectors per lane per item
-constexpr int kFp8Unroll = 4;      // 256-channel groups per item
+constexpr int kBf16Unroll = 2;     // 16-byte vectors per lane per item
+constexpr int kFp8Unroll = 2;      // 256-channel groups per item
 
 __device__ __forceinline__ int4 ld_stream(const int4* p) {
     int4 v;
