@@ -22,12 +22,21 @@ enum MetaWord : int {
 // chunk of `chunk_tokens` consecutive tokens; `warps_per_block` warps form a block.
 struct LayoutPlan {
     int T, K, E, R, L;
+    int key_bits;            // bits of (expert id + 1)
     int chunk_tokens;
     int num_chunks;
     int warps_per_block;
     int num_blocks;
     size_t smem_count;       // dynamic shared memory of the count kernel
     size_t smem_assign;      // dynamic shared memory of the assign kernel
+    // single-kernel path: one thread-block cluster of cl_ctas CTAs x cl_warps
+    // warps; chosen at launch when the routing is small enough
+    int cl_ctas;
+    int cl_warps;
+    int cl_chunk_tokens;
+    unsigned l_magic;        // ceil(2^32 / L): rank = umulhi(expert, l_magic)
+    int itr_words;           // is_token_in_rank rows can be written as 32-bit words
+    size_t smem_cluster;
 };
 
 LayoutPlan make_layout_plan(int T, int K, int E, int R);

@@ -218,6 +218,12 @@ def test_edge_shapes(ep, w):
     full_path(ep, inp, fp8=(w.H % 128 == 0))
 
 
+def test_large_routing_multiblock_path(ep):
+    """Routings above 2^18 slots take the multi-block layout path."""
+    w = _workload(40000, 128, 64, 8, 4, routing="zipf", drop_p=0.05)
+    full_path(ep, gi.make(w, 12), fp8=True)
+
+
 def test_all_dropped(ep):
     w = _workload(50, 256, 8, 2, 2, drop_p=1.0)
     inp = gi.make(w, 0)

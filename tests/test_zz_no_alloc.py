@@ -62,8 +62,10 @@ def _cases():
     rng = np.random.default_rng(7)
     bad = np.argsort(rng.random((300, 16)), axis=1)[:, :4].astype(np.int64)
     bad[3, 2], bad[77, 0] = 16, -5
+    large = gi.make(gi.Workload("large", T=40000, H=128, E=64, K=8, R=4, routing="zipf", drop_p=0.05),
+                    3, with_y=False)
     return [(prefill.topk_idx, 256, 8), (skewed.topk_idx, 64, 4), (bad, 16, 4),
-            (gi.make("decode", 2, with_y=False).topk_idx, 256, 8)]
+            (large.topk_idx, 64, 4), (gi.make("decode", 2, with_y=False).topk_idx, 256, 8)]
 
 
 def test_no_alloc_matches_layout_on_consecutive_calls(ep):
