@@ -30,6 +30,8 @@
 // through distributed shared memory, and separates the phases with hardware
 // cluster barriers. That needs no global scratch and replaces three
 // dependent launches with one.
+#include <algorithm>
+
 #include <cooperative_groups.h>
 
 #include "ep_internal.cuh"
@@ -315,30 +317,40 @@ __device__ __forceinline__ unsigned rank_of(unsigned e, const LayoutPlan& p) {
 // Single-launch layout by one cluster of p.cl_ctas CTAs, p.cl_warps warps each.
 // Warp g (CTA-major) owns tokens [g*ct, (g+1)*ct), at most kMaxRounds rounds
 // of 32 slots, whose keys and stable local ranks stay in registers.
+// Shared memory (ints, sized for 16 CTAs): hist[W][E] | all_tot[16][E] |
+// all_rank[16][R] | all_bad[16] | tail[max(W * ct_cap, 2E)], where the tail
+// holds the token rank masks (R <= 32) and later the offsets and CTA bases.
 __global__ void __launch_bounds__(1024, 1)
 layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
     extern __shared__ int smem[];
-    __shared__ int s_bad;
     cg::cluster_group cluster = cg::this_cluster();
     const int cta = static_cast<int>(cluster.block_rank());
-    const int W = p.cl_warps, E = p.E, R = p.R;
+    const int C = p.cl_ctas, W = p.cl_warps, E = p.E, R = p.R, ct = p.cl_chunk_tokens;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int* hist = smem;                       // [W][E]: counts, then the warp's base in the CTA
-    int* cta_tot = hist + W * E;            // [E] this CTA's expert totals (read by peers)
-    int* offs = cta_tot + E;                // [E] expert totals, then exclusive offsets
-    int* cta_base = offs + E;               // [E] rows of expert e in lower-ranked CTAs
-    int* rank_cnt = cta_base + E;           // [R] this CTA's tokens per rank (read by CTA 0)
+    int* hist = smem;                              // counts, then the warp's base in the CTA
+    int* all_tot = hist + W * E;                   // [C][E] every CTA's expert totals (pushed)
+    int* all_rank = all_tot + C * E;               // [C][R] every CTA's tokens per rank
+    int* all_bad = all_rank + C * R;               // [C] every CTA's invalid-id flag
+    int* tail = all_bad + kMaxClusterCtas;
+    unsigned* tokmask = reinterpret_cast<unsigned*>(tail);   // [W][ct] token rank bitmasks
     int* mine = hist + warp * E;
+    unsigned* my_mask = tokmask + warp * ct;
+    const bool small_r = R <= 32;
 
+    // Peers write into this CTA's shared memory later; that is only allowed
+    // once every CTA of the cluster runs, so arrive now and wait before the
+    // first remote store (by then every CTA has long started).
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     for (int e = lane; e < E; e += 32) mine[e] = 0;
-    for (int r = threadIdx.x; r < R; r += blockDim.x) rank_cnt[r] = 0;
-    if (threadIdx.x == 0) s_bad = 0;
+    if (small_r)
+        for (int i = lane; i < ct; i += 32) my_mask[i] = 0u;
+    if (threadIdx.x == 0) all_bad[cta] = 0;   // own entry only: peers write their own
     __syncthreads();
 
-    // ---- phase 1: stable local ranks and the warp's histogram, one pass
+    // ---- phase 1: stable local ranks, the warp's histogram, token rank masks
     const int g = cta * W + warp;
-    const int t0 = min(p.T, g * p.cl_chunk_tokens);
-    const int t1 = min(p.T, t0 + p.cl_chunk_tokens);
+    const int t0 = min(p.T, g * ct);
+    const int t1 = min(p.T, t0 + ct);
     const int64_t s0 = static_cast<int64_t>(t0) * p.K, s1 = static_cast<int64_t>(t1) * p.K;
     const int nr = static_cast<int>((s1 - s0 + 31) / 32);   // <= kMaxRounds (host check)
     const unsigned lt = lanemask_lt();
@@ -361,7 +373,13 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
             any_bad |= bad;
             const unsigned peers = peer_mask(key, p.key_bits);
             int loc = -1;
-            if (key >= 0) loc = mine[key] + __popc(peers & lt);
+            if (key >= 0) {
+                loc = mine[key] + __popc(peers & lt);
+                if (small_r) {
+                    const int tl = static_cast<int>((s0 + (j0 + j) * 32 + lane) / p.K) - t0;
+                    atomicOr(my_mask + tl, 1u << rank_of(static_cast<unsigned>(key), p));
+                }
+            }
             __syncwarp();
             if (key >= 0 && lane == __ffs(peers) - 1) mine[key] += __popc(peers);
             __syncwarp();
@@ -369,22 +387,16 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
             loc_r[j0 + j] = loc;
         }
     }
-    if (__any_sync(kFullMask, any_bad) && lane == 0) s_bad = 1;
+    const bool warp_bad = __any_sync(kFullMask, any_bad);
 
-    // is_token_in_rank and per-rank token counts
-    if (R <= 32) {
-        int my_rank_cnt = 0;                 // lane r counts rank r
-        for (int tb = t0; tb < t1; tb += 32) {
-            const int t = tb + lane;
-            unsigned mask = 0;
-            if (t < t1) {
-                const int64_t* row = a.topk_idx + static_cast<int64_t>(t) * p.K;
-#pragma unroll 8
-                for (int k = 0; k < p.K; ++k) {
-                    const int64_t e = __ldg(row + k);
-                    if (e >= 0 && e < E) mask |= 1u << rank_of(static_cast<unsigned>(e), p);
-                }
-                uint8_t* dst = a.is_token_in_rank + static_cast<int64_t>(t) * R;
+    // is_token_in_rank and this warp's tokens per rank (lane r counts rank r)
+    int my_rank_cnt = 0;
+    if (small_r) {
+        for (int tb = 0; tb < t1 - t0; tb += 32) {
+            const int tl = tb + lane;
+            const unsigned mask = tl < t1 - t0 ? my_mask[tl] : 0u;
+            if (tl < t1 - t0) {
+                uint8_t* dst = a.is_token_in_rank + static_cast<int64_t>(t0 + tl) * R;
                 if (p.itr_words) {
                     for (int w = 0; w < R / 4; ++w) {
                         const unsigned m4 = mask >> (4 * w);
@@ -400,7 +412,13 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
                 if (lane == r) my_rank_cnt += c;
             }
         }
-        if (lane < R && my_rank_cnt) atomicAdd(rank_cnt + lane, my_rank_cnt);
+    }
+    // reuse all_rank[cta] as this CTA's accumulator until the push
+    int* rank_acc = all_rank + cta * R;
+    for (int r = threadIdx.x; r < R; r += blockDim.x) rank_acc[r] = 0;
+    __syncthreads();
+    if (small_r) {
+        if (lane < R && my_rank_cnt) atomicAdd(rank_acc + lane, my_rank_cnt);
     } else {
         const int pairs = (t1 - t0) * R;
         for (int i = lane; i < pairs; i += 32) {
@@ -414,12 +432,15 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
                 hit |= (e >= e_lo && e < e_hi) ? 1 : 0;
             }
             a.is_token_in_rank[static_cast<int64_t>(t0) * R + i] = hit;
-            if (hit) atomicAdd(rank_cnt + r, 1);
+            if (hit) atomicAdd(rank_acc + r, 1);
         }
     }
+    if (warp_bad && lane == 0) all_bad[cta] = 1;   // only ever set: peers read after the barrier
     __syncthreads();
 
-    // ---- phase 2: per-warp bases inside the CTA and the CTA's expert totals
+    // ---- phase 2: per-warp bases inside the CTA; push this CTA's totals,
+    // rank counts and error flag into every CTA of the cluster
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // all CTAs have started
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int run = 0;
         for (int w0 = 0; w0 < W; w0 += 8) {   // W is a multiple of 8
@@ -432,45 +453,49 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
                 run += c[i];
             }
         }
-        cta_tot[e] = run;
+#pragma unroll
+        for (int c = 0; c < kMaxClusterCtas; ++c)
+            if (c < C) *cluster.map_shared_rank(all_tot + cta * E + e, c) = run;
     }
-    cluster.sync();   // every CTA's cta_tot, rank_cnt and s_bad are final
+    for (int i = threadIdx.x; i < R + 1; i += blockDim.x) {
+        const int v = i < R ? rank_acc[i] : all_bad[cta];
+#pragma unroll
+        for (int c = 0; c < kMaxClusterCtas; ++c)
+            if (c < C && c != cta)
+                *cluster.map_shared_rank(i < R ? all_rank + cta * R + i : all_bad + cta, c) = v;
+    }
+    // Every push lands before any CTA passes this barrier (release/acquire at
+    // cluster scope), and nothing touches another CTA's shared memory after
+    // it, so CTAs may finish independently.
+    cluster.sync();
 
-    // ---- phase 3: combine the CTAs' totals through distributed shared memory.
-    // Items: E experts, then (CTA 0 only) R rank totals and the error flag;
-    // each item issues its (up to 16) remote loads back to back.
-    const int C = p.cl_ctas;
-    const int items = E + (cta == 0 ? R + 1 : 0);
-    for (int i = threadIdx.x; i < items; i += blockDim.x) {
-        const int* src = i < E ? cta_tot + i : (i < E + R ? rank_cnt + (i - E) : &s_bad);
-        int v[kMaxClusterCtas];
+    // ---- phase 3 (local): expert totals and this CTA's base per expert
+    int* offs = tail;          // the token masks are consumed: reuse the tail
+    int* cta_base = tail + E;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int below = 0, total = 0;
 #pragma unroll
-        for (int c = 0; c < kMaxClusterCtas; ++c) v[c] = c < C ? *cluster.map_shared_rank(src, c) : 0;
-        if (i < E) {
-            int below = 0, total = 0;
-#pragma unroll
-            for (int c = 0; c < kMaxClusterCtas; ++c) {
-                below += c < cta ? v[c] : 0;
-                total += v[c];
-            }
-            cta_base[i] = below;
-            offs[i] = total;
-        } else if (i < E + R) {
+        for (int c = 0; c < kMaxClusterCtas; ++c) {
+            const int v = c < C ? all_tot[c * E + e] : 0;
+            below += c < cta ? v : 0;
+            total += v;
+        }
+        cta_base[e] = below;
+        offs[e] = total;
+        if (cta == 0) a.num_tokens_per_expert[e] = total;
+    }
+    if (cta == 0) {
+        for (int r = threadIdx.x; r < R; r += blockDim.x) {
             int total = 0;
-#pragma unroll
-            for (int c = 0; c < kMaxClusterCtas; ++c) total += v[c];
-            a.num_tokens_per_rank[i - E] = total;
-        } else {
+            for (int c = 0; c < C; ++c) total += all_rank[c * R + r];
+            a.num_tokens_per_rank[r] = total;
+        }
+        if (threadIdx.x == 0) {
             int bad = 0;
-#pragma unroll
-            for (int c = 0; c < kMaxClusterCtas; ++c) bad |= v[c];
+            for (int c = 0; c < C; ++c) bad |= all_bad[c];
             a.meta[kMetaError] = bad ? EP_ERR_INVALID_EXPERT : 0;
         }
     }
-    cluster.sync();   // no remote reads after this point: CTAs may finish freely
-
-    if (cta == 0)
-        for (int e = threadIdx.x; e < E; e += blockDim.x) a.num_tokens_per_expert[e] = offs[e];
     __syncthreads();
     if (warp == 0) {
         const int n_rows = warp_exclusive_scan(offs, E, lane);
@@ -517,15 +542,20 @@ LayoutPlan make_layout_plan(int T, int K, int E, int R) {
     // single-cluster geometry (CTA count fixed at launch): as many warps per
     // CTA as shared memory allows, up to 32
     // about four 32-slot rounds per warp on a 16-CTA cluster, 8 to 32 warps,
-    // fewer if shared memory (cw + 3 rows of E ints) does not fit
+    // fewer if shared memory does not fit; smem_cluster = 0 disables the path
     const int64_t slots = static_cast<int64_t>(T) * K;
     int cw = 8;
     while (cw < 32 && slots > static_cast<int64_t>(16) * cw * 32 * kRoundsInFlight) cw <<= 1;
-    while (cw > 8 && (static_cast<size_t>(cw) + 3) * E * sizeof(int) > kClusterSmemBudget) cw >>= 1;
+    auto cluster_smem = [&](int w) {
+        const size_t ct_cap = static_cast<size_t>(kMaxRounds * 32 / K);
+        const size_t tail = std::max(static_cast<size_t>(w) * ct_cap, static_cast<size_t>(2 * E));
+        return (static_cast<size_t>(w + kMaxClusterCtas) * E + kMaxClusterCtas * (R + 1) + tail) * sizeof(int);
+    };
+    while (cw > 8 && cluster_smem(cw) > kClusterSmemBudget) cw >>= 1;
     p.cl_warps = cw;
     p.cl_ctas = 0;
     p.cl_chunk_tokens = 0;
-    p.smem_cluster = ((static_cast<size_t>(cw) + 3) * E + R) * sizeof(int);
+    p.smem_cluster = cluster_smem(cw) <= kClusterSmemBudget ? cluster_smem(cw) : 0;
     p.l_magic = p.L > 1 ? static_cast<unsigned>(((uint64_t{1} << 32) + p.L - 1) / p.L) : 0u;
     p.itr_words = 0;
     return p;
@@ -589,13 +619,15 @@ cudaError_t launch_layout(const LayoutPlan& plan, const LayoutArgs& a, cudaStrea
     if (plan.num_blocks == 0) return cudaSuccess;
 
     const int64_t slots = static_cast<int64_t>(plan.T) * plan.K;
-    if (slots <= kClusterMaxSlots && plan.smem_cluster <= kClusterSmemBudget + 8 * 1024) {
+    if (slots <= kClusterMaxSlots && plan.smem_cluster > 0) {
         const int ctas = cluster_ctas_for(dev, plan.cl_warps, plan.smem_cluster);
-        if (ctas > 0 && slots <= static_cast<int64_t>(ctas) * plan.cl_warps * 32 * kMaxRounds) {
+        const int warps = ctas * plan.cl_warps;
+        const int ct = warps > 0 ? (plan.T + warps - 1) / warps : 0;
+        // each warp's chunk must fit kMaxRounds rounds (and the token-mask area)
+        if (ctas > 0 && static_cast<int64_t>(ct) * plan.K <= kMaxRounds * 32) {
             LayoutPlan p = plan;
             p.cl_ctas = ctas;
-            const int warps = ctas * p.cl_warps;
-            p.cl_chunk_tokens = (p.T + warps - 1) / warps;
+            p.cl_chunk_tokens = ct;
             p.itr_words = (p.R % 4 == 0 && reinterpret_cast<uintptr_t>(a.is_token_in_rank) % 4 == 0) ? 1 : 0;
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(ctas);

@@ -212,6 +212,10 @@ def _workload(T, H, E, K, R, **kw):
     _workload(300, 8, 8, 8, 2),                          # H = 8 (one vector), K == E
     _workload(64, 1152, 32, 32, 8),                      # K = 32 (maximum top-k)
     _workload(200, 136, 4096, 8, 1024),                  # maximum E and R
+    _workload(300, 128, 512, 8, 64),                     # R > 32 on the single-cluster path
+    _workload(500, 128, 256, 8, 32, drop_p=0.1),         # R = 32: every rank bit in use
+    _workload(21504, 64, 64, 6, 4, routing="zipf"),      # K = 6: largest single-cluster chunk
+    _workload(21505, 64, 64, 6, 4, routing="zipf"),      # one token more: multi-block path
 ])
 def test_edge_shapes(ep, w):
     inp = gi.make(w, 11)
