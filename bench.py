@@ -158,7 +158,7 @@ def read_traffic(kernel: str):
     import hashlib
     import re
 
-    path = os.path.join(ROOT, "profiles", "ncu_summary.md")
+    path = os.path.join(ROOT, "profiles", "dram_traffic_prefill_T8192.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
@@ -170,6 +170,22 @@ def read_traffic(kernel: str):
         return None
     h = hashlib.sha256(open(os.path.join(ROOT, "combine_get_dispatch_layout_gb300", "csrc", src), "rb").read())
     return int(m.group(1)) if h.hexdigest()[:16] == m.group(2) else None
+
+
+def aggregate_over_ranks(local_ms: float, local_bytes: int, device=None):
+    """Whole-job numbers for replicas on several ranks: the step time is the
+    slowest rank's, the bytes are every rank's. Returns (max_ms, total_bytes).
+    One scalar all-reduce each; nothing on the data path is exchanged."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return local_ms, local_bytes
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    b = torch.tensor([local_bytes], dtype=torch.float64, device=device)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(b.item())
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -233,6 +249,7 @@ def gpu_arm(args, rank, world, local):
         step(events[i])
     torch.cuda.synchronize(dev)
     t_wall1 = time.perf_counter()
+    layout_kernels = ep.ep_handle_layout_kernels(handle)
     if world > 1:
         torch.distributed.barrier()
     time.sleep(0.15)
@@ -241,16 +258,12 @@ def gpu_arm(args, rank, world, local):
     per = np.array([[events[i][j].elapsed_time(events[i][j + 1]) for j in range(3)] for i in range(args.steps)])
     total_ms = float(events[0][0].elapsed_time(events[-1][3]))
     ms_layout, ms_dispatch, ms_combine = (float(per[:, j].mean()) for j in range(3))
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_step = total_ms / args.steps
-
     b_lay = bytes_layout(T, K, E, R)
     b_dis = bytes_dispatch_bf16(T, K, H, N)
     b_com = bytes_combine(T, K, H, N)
     b_step = b_lay + b_dis + b_com
+    total_ms, job_bytes = aggregate_over_ranks(total_ms, b_step, device=dev)
+    ms_step = total_ms / args.steps
     peak, peak_src = load_peaks()
 
     # fp8 quantise-permute on the fp8 workload (same shapes and routing recipe)
@@ -275,10 +288,7 @@ def gpu_arm(args, rank, world, local):
 
     # end to end through the public API with pinned host buffers
     e2e = e2e_measure(torch, ep, dev, inp, args, stream)
-    if world > 1:
-        t = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e["ms_per_step"] = float(t.item())
+    e2e["ms_per_step"], _ = aggregate_over_ranks(e2e["ms_per_step"], 0, device=dev)
     handle.destroy()
     h8.destroy()
 
@@ -294,7 +304,7 @@ def gpu_arm(args, rank, world, local):
     clocks = sampler.summary(t_wall0 - 0.3, t_wall1)
     line = {
         "metric": METRIC,
-        "value": round(world * b_step / (ms_step * 1e-3) / 1e9, 2),
+        "value": round(job_bytes / (ms_step * 1e-3) / 1e9, 2),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -331,10 +341,10 @@ def gpu_arm(args, rank, world, local):
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": read_traffic(dominant)},
-        "e2e": {"value": round(world * b_step / (e2e["ms_per_step"] * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(job_bytes / (e2e["ms_per_step"] * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e["ms_per_step"], 4), "steps": e2e["steps"]},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": (layout_kernels + 2) * args.steps,
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:

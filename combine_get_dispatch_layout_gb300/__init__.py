@@ -20,7 +20,8 @@ EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3 = 0, 1
 
 # Exported symbols declared in include/ep.h.
 EXPORTS = ("ep_layout", "ep_dispatch", "ep_combine", "ep_handle_query",
-           "ep_handle_copy_row_of_slot", "ep_handle_destroy", "ep_layout_noalloc", "ep_status_string")
+           "ep_handle_copy_row_of_slot", "ep_handle_destroy", "ep_handle_layout_kernels",
+           "ep_layout_noalloc", "ep_status_string")
 
 _lib = None
 
@@ -46,11 +47,14 @@ def lib() -> ctypes.CDLL:
         L.ep_handle_query.argtypes = [P, ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_int32)]
         L.ep_handle_copy_row_of_slot.argtypes = [P, P, P]
         L.ep_handle_destroy.argtypes = [P]
+        L.ep_handle_layout_kernels.argtypes = [P]
+        L.ep_handle_layout_kernels.restype = i32
         L.ep_layout_noalloc.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, P]
         L.ep_status_string.argtypes = [i32]
         L.ep_status_string.restype = ctypes.c_char_p
-        for name in EXPORTS[:-1]:
-            getattr(L, name).restype = i32
+        for name in EXPORTS:
+            if name != "ep_status_string":
+                getattr(L, name).restype = i32
         _lib = L
     return _lib
 
@@ -167,6 +171,11 @@ def ep_layout_noalloc(topk_idx, num_experts: int, num_ranks: int, num_tokens_per
                                  _ptr(num_tokens_per_rank), _ptr(is_token_in_rank), _ptr(expert_offsets),
                                  _ptr(row_of_slot), _ptr(device_error), _stream(stream))
     _check(st, "ep_layout_noalloc")
+
+
+def ep_handle_layout_kernels(handle: Handle) -> int:
+    """Kernels the last ep_layout on `handle` enqueued (1 or 3; 0 for T = 0)."""
+    return int(lib().ep_handle_layout_kernels(handle.ptr))
 
 
 def ep_handle_destroy(handle: Handle) -> None:

@@ -22,6 +22,7 @@ struct ep_handle {
     ep::LayoutPlan plan{};
     cudaStream_t layout_stream = nullptr;
     bool error_latched = false;
+    int layout_kernels = 0;     // kernels the last ep_layout enqueued
     // capacities of the device block
     int64_t cap_slots = 0, cap_chunk_cells = 0, cap_rank_cells = 0;
     void* dev_block = nullptr;
@@ -188,8 +189,9 @@ ep_status_t ep_layout(const int64_t* topk_idx, int T, int K, int E, int R,
         a.chunk_cnt = h->chunk_cnt;
         a.block_rank = h->block_rank;
         a.meta = h->meta;
-        err = ep::launch_layout(plan, a, s);
+        err = ep::launch_layout(plan, a, s, &h->layout_kernels);
     }
+    if (T == 0) h->layout_kernels = 0;
     *handle = h;
     return err == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
@@ -294,6 +296,8 @@ ep_status_t ep_handle_destroy(ep_handle_t handle) {
     if (switch_dev) cudaSetDevice(prev);
     return st;
 }
+
+int ep_handle_layout_kernels(ep_handle_t handle) { return handle ? handle->layout_kernels : -1; }
 
 const char* ep_status_string(ep_status_t status) {
     switch (status) {

@@ -53,7 +53,9 @@ struct LayoutArgs {
     int32_t* meta;             // [kMetaWords]
 };
 
-cudaError_t launch_layout(const LayoutPlan& p, const LayoutArgs& a, cudaStream_t stream);
+// Launches the layout; *kernels (if not null) receives the number of kernels
+// enqueued (1 on the single-cluster path, 3 on the multi-block path).
+cudaError_t launch_layout(const LayoutPlan& p, const LayoutArgs& a, cudaStream_t stream, int* kernels = nullptr);
 
 struct DispatchArgs {
     const void* x;             // bf16 [T, H]

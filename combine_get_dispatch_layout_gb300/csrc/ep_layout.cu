@@ -602,7 +602,8 @@ int cluster_ctas_for(int dev, int warps, size_t smem) {
 
 }  // namespace
 
-cudaError_t launch_layout(const LayoutPlan& plan, const LayoutArgs& a, cudaStream_t stream) {
+cudaError_t launch_layout(const LayoutPlan& plan, const LayoutArgs& a, cudaStream_t stream, int* kernels) {
+    if (kernels) *kernels = 0;
     // the shared-memory opt-in is per device
     static bool attr_set[64] = {};
     int dev = 0;
@@ -641,11 +642,13 @@ cudaError_t launch_layout(const LayoutPlan& plan, const LayoutArgs& a, cudaStrea
             attr.val.clusterDim.z = 1;
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
+            if (kernels) *kernels = 1;
             return cudaLaunchKernelEx(&cfg, layout_cluster_kernel, p, a);
         }
     }
 
     const int threads = plan.warps_per_block * 32;
+    if (kernels) *kernels = 3;
     layout_count_kernel<<<plan.num_blocks, threads, plan.smem_count, stream>>>(plan, a);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;

@@ -459,3 +459,14 @@ def test_alloc_hooks(ep):
     with pytest.raises(ep.EPError) as e:
         ep.ep_layout(idx, 4, 2, *outs, alloc_fn=failing, free_fn=free)
     assert e.value.status == ep.EP_ERR_ALLOC
+
+
+def test_layout_path_selection(ep):
+    """Routings up to the single-cluster limit take one launch, larger ones three."""
+    small = gi.make("prefill", 0, with_y=False)
+    big = gi.make(_workload(40000, 128, 64, 8, 4), 0, with_y=False)
+    for inp, want in [(small, 1), (big, 3)]:
+        w = inp.w
+        run = Run(ep, inp.topk_idx, w.E, w.R)
+        assert ep.ep_handle_layout_kernels(run.h) == want
+        run.h.destroy()
