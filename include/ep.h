@@ -22,8 +22,11 @@
  *   ep_handle_query    nccl_ep.cc, ncclEpHandleGetNumRecvTokens.
  *
  * Conventions for every call:
- *  - Pointers named as device pointers must be device memory (or managed
- *    memory) of the GPU that is current on the calling thread. The caller
+ *  - Pointers named as device pointers must be memory the current GPU can
+ *    address: its device memory, managed memory, or pinned host memory
+ *    mapped into the unified address space (cudaHostAlloc / cudaHostRegister;
+ *    on GB300 the kernels then stream it over NVLink-C2C, which is how a
+ *    caller with host-resident tokens avoids a separate copy). The caller
  *    owns them; the library never frees caller memory.
  *  - All device work is enqueued on `stream` (a cudaStream_t; NULL = the
  *    legacy default stream) and is asynchronous, except where a call says it

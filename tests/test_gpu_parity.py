@@ -470,3 +470,32 @@ def test_layout_path_selection(ep):
         run = Run(ep, inp.topk_idx, w.E, w.R)
         assert ep.ep_handle_layout_kernels(run.h) == want
         run.h.destroy()
+
+
+def test_pinned_host_buffers(ep):
+    """Host-resident inputs and outputs (pinned, mapped into the unified
+    address space) give the same bytes as device buffers."""
+    inp = gi.make("decode", 6)
+    w = inp.w
+    ref = oracle.layout(inp.topk_idx, w.E, w.R)
+    N = int(ref["expert_offsets"][-1])
+    h_idx = torch.from_numpy(inp.topk_idx).pin_memory()
+    h_x = torch.from_numpy(inp.x.view(np.int16)).pin_memory()
+    h_y = torch.from_numpy(inp.y.view(np.int16)).pin_memory()
+    h_w = torch.from_numpy(inp.topk_weights).pin_memory()
+    h_out = torch.full((w.T, w.H), SENT16, dtype=torch.int16).pin_memory()
+    cnt = torch.empty(w.E, dtype=torch.int32, device="cuda")
+    ntr = torch.empty(w.R, dtype=torch.int32, device="cuda")
+    itr = torch.empty(w.T, w.R, dtype=torch.uint8, device="cuda")
+    off = torch.empty(w.E + 1, dtype=torch.int32, device="cuda")
+    h = ep.ep_layout(h_idx, w.E, w.R, cnt, ntr, itr, off)
+    recv = torch.empty(N, w.H, dtype=torch.int16, device="cuda")
+    ep.ep_dispatch(h, h_x, ep.EP_DTYPE_BF16, recv, N)
+    ep.ep_combine(h, h_y, h_out, topk_weights=h_w)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(off.cpu().numpy(), ref["expert_offsets"])
+    r_x, _, _ = oracle.dispatch_bf16(inp.x, ref["row_of_slot"], N)
+    np.testing.assert_array_equal(recv.cpu().numpy().view(np.uint16), r_x)
+    want = oracle.combine(inp.y, ref["row_of_slot"], inp.topk_weights)
+    assert_combine(h_out.numpy().view(np.uint16), want)
+    h.destroy()
