@@ -47,6 +47,10 @@ def _lib():
             i64, i32 = ctypes.c_int64, ctypes.c_int
             L.orc_layout.argtypes = [P, i64, i32, i32, i32, P, P, P, P, P]
             L.orc_layout.restype = i32
+            L.orc_layout_aligned.argtypes = [P, i64, i32, i32, i32, i32, P, P, P, P, P]
+            L.orc_layout_aligned.restype = i32
+            L.orc_fill_pad_rows.argtypes = [P, P, i32, i64, P, P, i32, P, P]
+            L.orc_fill_pad_rows.restype = None
             L.orc_dispatch_bf16.argtypes = [P, i64, i32, P, i32, P, P, P, P]
             L.orc_dispatch_bf16.restype = None
             L.orc_dispatch_e4m3.argtypes = [P, i64, i32, P, i32, P, P, P, P, P]
@@ -92,6 +96,35 @@ def layout(topk_idx: np.ndarray, E: int, R: int) -> dict:
                            _p(out["expert_offsets"]), _p(out["row_of_slot"]))
     out["status"] = int(st)
     return out
+
+
+def layout_aligned(topk_idx: np.ndarray, E: int, R: int, alignment: int) -> dict:
+    """Layout whose expert row ranges start on multiples of `alignment`."""
+    idx = _c(topk_idx, np.int64)
+    T, K = idx.shape
+    out = dict(
+        num_tokens_per_expert=np.zeros(E, np.int32),
+        num_tokens_per_rank=np.zeros(R, np.int32),
+        is_token_in_rank=np.zeros((T, R), np.uint8),
+        expert_offsets=np.zeros(E + 1, np.int32),
+        row_of_slot=np.zeros((T, K), np.int32),
+    )
+    st = _lib().orc_layout_aligned(_p(idx), T, K, E, R, alignment, _p(out["num_tokens_per_expert"]),
+                                   _p(out["num_tokens_per_rank"]), _p(out["is_token_in_rank"]),
+                                   _p(out["expert_offsets"]), _p(out["row_of_slot"]))
+    out["status"] = int(st)
+    return out
+
+
+def fill_pad_rows(layout: dict, recv: np.ndarray, scales=None, src=None, weights=None) -> None:
+    """Zero the pad rows of an aligned layout in place (scale 0, source -1, weight 0)."""
+    E = len(layout["num_tokens_per_expert"])
+    assert recv.flags.c_contiguous
+    row_bytes = recv.strides[0]
+    nb = 0 if scales is None else scales.shape[1]
+    _lib().orc_fill_pad_rows(_p(_c(layout["num_tokens_per_expert"], np.int32)),
+                             _p(_c(layout["expert_offsets"], np.int32)), E, row_bytes, _p(recv),
+                             _p(scales), nb, _p(src), _p(weights))
 
 
 def dispatch_bf16(x: np.ndarray, row_of_slot: np.ndarray, num_rows: int,

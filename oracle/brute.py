@@ -37,6 +37,24 @@ def layout(topk_idx: np.ndarray, E: int, R: int) -> dict:
     )
 
 
+def layout_aligned(topk_idx: np.ndarray, E: int, R: int, A: int) -> dict:
+    """Aligned layout from scratch: aligned starts by cumulative ceil, then
+    each valid slot's rank inside its expert by sorting (expert, token, k)."""
+    base = layout(topk_idx, E, R)
+    cnt = base["num_tokens_per_expert"].astype(np.int64)
+    padded = -(-cnt // A) * A
+    starts = np.concatenate([[0], np.cumsum(padded)])
+    idx = np.asarray(topk_idx, np.int64)
+    rows = base["row_of_slot"].astype(np.int64)
+    valid = rows >= 0
+    rank_in_expert = rows - base["expert_offsets"][np.where(valid, idx, 0)]
+    new_rows = np.where(valid, starts[np.where(valid, idx, 0)] + rank_in_expert, -1)
+    out = dict(base)
+    out["expert_offsets"] = starts.astype(np.int32)
+    out["row_of_slot"] = new_rows.astype(np.int32)
+    return out
+
+
 def e4m3_values() -> tuple[np.ndarray, np.ndarray]:
     """(codes, values) of the 254 finite OCP E4M3 codes, decoded from their bits."""
     codes, vals = [], []

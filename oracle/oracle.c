@@ -283,3 +283,59 @@ void orc_e4m3_sweep(uint32_t lo, uint32_t hi, uint8_t* out) {
         out[u - lo] = orc_f32_to_e4m3(f);
     }
 }
+
+/* ---------------------------------------------------------------- alignment */
+
+/* Routing layout with per-expert row alignment A >= 1 (DeepEP API docs,
+ * "dispatch()" expert_alignment and "Prefix Sum Interpretation for Expert
+ * Token Counts": in expand mode expert i's rows start at the previous
+ * expert's end rounded up to a multiple of the alignment).
+ *   expert_offsets[e] = sum over e' < e of roundup(count[e'], A)
+ *   expert_offsets[E] = padded row total
+ * Expert e's real rows are expert_offsets[e] .. + count[e] - 1 in (t, k)
+ * order; the rest of its range up to expert_offsets[e+1] are pad rows.
+ * Counts, masks and per-rank tokens are those of orc_layout. */
+int orc_layout_aligned(const int64_t* topk_idx, int64_t T, int K, int E, int R, int A,
+                       int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                       uint8_t* is_token_in_rank, int32_t* expert_offsets,
+                       int32_t* row_of_slot) {
+    if (A < 1) return ORC_ERR_ARG;
+    int32_t* plain_offsets = (int32_t*)malloc(sizeof(int32_t) * (size_t)(E + 1));
+    if (!plain_offsets) return ORC_ERR_ARG;
+    int status = orc_layout(topk_idx, T, K, E, R, num_tokens_per_expert, num_tokens_per_rank,
+                            is_token_in_rank, plain_offsets, row_of_slot);
+    if (status == ORC_ERR_ARG) { free(plain_offsets); return status; }
+    int64_t run = 0;
+    for (int e = 0; e < E; ++e) {
+        expert_offsets[e] = (int32_t)run;
+        int64_t c = num_tokens_per_expert[e];
+        run += (c + A - 1) / A * A;
+    }
+    if (run > INT32_MAX) { free(plain_offsets); return ORC_ERR_ARG; }
+    expert_offsets[E] = (int32_t)run;
+    /* move every real row from its packed position to the aligned range */
+    for (int64_t s = 0; s < T * (int64_t)K; ++s) {
+        int64_t e = topk_idx[s];
+        if (row_of_slot[s] < 0) continue;
+        row_of_slot[s] = row_of_slot[s] - plain_offsets[e] + expert_offsets[e];
+    }
+    free(plain_offsets);
+    return status;
+}
+
+/* Pad rows of an aligned layout: every receive row of expert e from
+ * expert_offsets[e] + count[e] up to expert_offsets[e+1] is zero (row_bytes
+ * zero bytes), has scale 0 in each of its nb scale slots (if scales), source
+ * token -1 (if src) and weight 0 (if weights). */
+void orc_fill_pad_rows(const int32_t* num_tokens_per_expert, const int32_t* expert_offsets, int E,
+                       int64_t row_bytes, uint8_t* recv, float* scales, int nb, int32_t* src,
+                       float* weights) {
+    for (int e = 0; e < E; ++e) {
+        for (int64_t r = (int64_t)expert_offsets[e] + num_tokens_per_expert[e]; r < expert_offsets[e + 1]; ++r) {
+            memset(recv + r * row_bytes, 0, (size_t)row_bytes);
+            if (scales) for (int b = 0; b < nb; ++b) scales[r * nb + b] = 0.0f;
+            if (src) src[r] = -1;
+            if (weights) weights[r] = 0.0f;
+        }
+    }
+}

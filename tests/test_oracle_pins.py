@@ -305,3 +305,48 @@ def test_combine_vs_f64(name, null_w):
     # and dropped-only tokens give +0
     dead = (L["row_of_slot"] < 0).all(axis=1)
     assert (out[dead] == 0).all()
+
+
+# ------------------------------------------------------------------ alignment
+
+def test_layout_aligned_golden(golden):
+    g = golden("layout_hand_aligned.txt")
+    T, K, E, R, A = (int(g[k][0]) for k in "TKERA")
+    idx = _ints(g["topk_idx"]).reshape(T, K)
+    L = oracle.layout_aligned(idx, E, R, A)
+    assert L["status"] == oracle.OK
+    np.testing.assert_array_equal(L["num_tokens_per_expert"], _ints(g["num_tokens_per_expert"]))
+    np.testing.assert_array_equal(L["expert_offsets"], _ints(g["expert_offsets"]))
+    np.testing.assert_array_equal(L["row_of_slot"].ravel(), _ints(g["row_of_slot"]))
+    n_pad = int(L["expert_offsets"][-1])
+    recv = np.full((n_pad, 8), 0x7777, np.uint16)
+    src = np.full(n_pad, 99, np.int32)
+    oracle.fill_pad_rows(L, recv, src=src)
+    pad = sorted(int(r) for r in np.flatnonzero(src == -1))
+    assert pad == [int(v) for v in g["pad_rows"]]
+    assert (recv[pad] == 0).all() and (recv[src != -1] == 0x7777).all()
+
+
+@pytest.mark.parametrize("A", [1, 2, 3, 8, 64, 128])
+@pytest.mark.parametrize("case", CORNERS[:8])
+def test_layout_aligned_vs_brute(case, A):
+    T, K, E, R, drop_p, distinct, bad_p = case
+    rng = np.random.default_rng(A)
+    idx = _random_routing(rng, T, K, E, drop_p, distinct, bad_p)
+    a = oracle.layout_aligned(idx, E, R, A)
+    b = brute.layout_aligned(idx, E, R, A)
+    for key in ["num_tokens_per_expert", "num_tokens_per_rank", "is_token_in_rank",
+                "expert_offsets", "row_of_slot"]:
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    off = a["expert_offsets"]
+    assert (off % A == 0).all()
+    pad = np.diff(off) - a["num_tokens_per_expert"]
+    assert ((pad >= 0) & (pad < A)).all()
+
+
+def test_layout_aligned_one_is_plain_layout():
+    inp = gi.make("skewed", 0, with_y=False)
+    w = inp.w
+    a, b = oracle.layout_aligned(inp.topk_idx, w.E, w.R, 1), oracle.layout(inp.topk_idx, w.E, w.R)
+    for key in ["expert_offsets", "row_of_slot", "num_tokens_per_expert"]:
+        np.testing.assert_array_equal(a[key], b[key])
