@@ -286,6 +286,32 @@ def gpu_arm(args, rank, world, local):
     ms_fp8 = float(np.mean([ev8[i].elapsed_time(ev8[i + 1]) for i in range(reps8)]))
     b_fp8 = bytes_dispatch_fp8(T, K, H, fp8.num_valid)
 
+    # aligned layout (expert rows start on multiples of 128) + bf16 dispatch
+    # including the pad rows' zero fill, on the prefill routing
+    A = 128
+    with torch.cuda.stream(stream):
+        off_a = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        recv_a = torch.empty(N + E * (A - 1), H, dtype=torch.bfloat16, device=dev)
+    h_a = ep.ep_layout_aligned(idx, E, R, A, cnt, ntr, itr, off_a, stream=stream)
+    n_pad, _ = ep.ep_handle_query(h_a)
+    reps_a = max(3, min(args.steps, 100))
+    ev_a = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps_a)]
+    for i in range(-3, reps_a):
+        if i >= 0:
+            ev_a[i][0].record(stream)
+        ep.ep_layout_aligned(idx, E, R, A, cnt, ntr, itr, off_a, handle=h_a, stream=stream)
+        if i >= 0:
+            ev_a[i][1].record(stream)
+        ep.ep_dispatch(h_a, x, ep.EP_DTYPE_BF16, recv_a, recv_a.shape[0], stream=stream)
+        if i >= 0:
+            ev_a[i][2].record(stream)
+    stream.synchronize()
+    ms_lay_a = float(np.mean([e[0].elapsed_time(e[1]) for e in ev_a]))
+    ms_dis_a = float(np.mean([e[1].elapsed_time(e[2]) for e in ev_a]))
+    b_dis_a = 2 * T * H + 2 * n_pad * H + 4 * T * K
+    h_a.destroy()
+    del recv_a
+
     # end to end through the public API with pinned host buffers
     e2e = e2e_measure(torch, ep, dev, inp, args, stream)
     e2e["ms_per_step"], _ = aggregate_over_ranks(e2e["ms_per_step"], 0, device=dev)
@@ -332,6 +358,11 @@ def gpu_arm(args, rank, world, local):
                         "gbs": round(b_com / (ms_combine * 1e-3) / 1e9, 1),
                         "frac_of_measured": round(b_com / (ms_combine * 1e-3) / 1e9 / peak, 4),
                         "frac_of_8tbs": round(b_com / (ms_combine * 1e-3) / 8e12, 4)},
+            "dispatch_bf16_aligned128": {"rows_padded": n_pad, "layout_us": round(ms_lay_a * 1e3, 2),
+                                         "us": round(ms_dis_a * 1e3, 2), "bytes": b_dis_a,
+                                         "gbs": round(b_dis_a / (ms_dis_a * 1e-3) / 1e9, 1),
+                                         "frac_of_measured": round(b_dis_a / (ms_dis_a * 1e-3) / 1e9 / peak, 4),
+                                         "frac_of_8tbs": round(b_dis_a / (ms_dis_a * 1e-3) / 8e12, 4)},
             "dispatch_fp8": {"workload": "fp8: x ~N(0,2^2) + 7 outlier channels x50, same shapes",
                              "us": round(ms_fp8 * 1e3, 2), "bytes": b_fp8,
                              "gbs": round(b_fp8 / (ms_fp8 * 1e-3) / 1e9, 1),

@@ -19,7 +19,7 @@ EP_OK, EP_ERR_INVALID_ARG, EP_ERR_INVALID_EXPERT, EP_ERR_CAPACITY, EP_ERR_CUDA, 
 EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3 = 0, 1
 
 # Exported symbols declared in include/ep.h.
-EXPORTS = ("ep_layout", "ep_dispatch", "ep_combine", "ep_handle_query",
+EXPORTS = ("ep_layout", "ep_layout_aligned", "ep_dispatch", "ep_combine", "ep_handle_query",
            "ep_handle_copy_row_of_slot", "ep_handle_destroy", "ep_handle_layout_kernels",
            "ep_layout_noalloc", "ep_status_string")
 
@@ -42,6 +42,7 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(_LIB_PATH)
         P, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
         L.ep_layout.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, ctypes.POINTER(P), P]
+        L.ep_layout_aligned.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, P, P, ctypes.POINTER(P), P]
         L.ep_dispatch.argtypes = [P, P, i32, i32, P, P, P, P, P, i64, P]
         L.ep_combine.argtypes = [P, P, i64, i32, P, P, P]
         L.ep_handle_query.argtypes = [P, ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_int32)]
@@ -124,6 +125,20 @@ def ep_layout(topk_idx, num_experts: int, num_ranks: int, num_tokens_per_expert,
                          _ptr(num_tokens_per_rank), _ptr(is_token_in_rank), _ptr(expert_offsets),
                          _fnptr(alloc_fn), _fnptr(free_fn), ctypes.byref(h.ptr), _stream(stream))
     _check(st, "ep_layout")
+    return h
+
+
+def ep_layout_aligned(topk_idx, num_experts: int, num_ranks: int, expert_alignment: int,
+                      num_tokens_per_expert, num_tokens_per_rank, is_token_in_rank, expert_offsets,
+                      handle: Handle | None = None, stream=None, alloc_fn=None, free_fn=None) -> Handle:
+    """ep_layout with each expert's rows starting on a multiple of expert_alignment."""
+    T, K = topk_idx.shape
+    h = handle if handle is not None else Handle()
+    st = lib().ep_layout_aligned(_ptr(topk_idx), T, K, num_experts, num_ranks, int(expert_alignment),
+                                 _ptr(num_tokens_per_expert), _ptr(num_tokens_per_rank), _ptr(is_token_in_rank),
+                                 _ptr(expert_offsets), _fnptr(alloc_fn), _fnptr(free_fn), ctypes.byref(h.ptr),
+                                 _stream(stream))
+    _check(st, "ep_layout_aligned")
     return h
 
 

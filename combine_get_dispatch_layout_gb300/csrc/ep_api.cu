@@ -19,17 +19,20 @@ struct ep_handle {
     ep_free_fn free_fn = nullptr;
     // routing of the last ep_layout
     int T = 0, K = 0, E = 0, R = 0;
+    int align = 1;              // expert row alignment of the last layout
     ep::LayoutPlan plan{};
     cudaStream_t layout_stream = nullptr;
     bool error_latched = false;
     int layout_kernels = 0;     // kernels the last ep_layout enqueued
     // capacities of the device block
-    int64_t cap_slots = 0, cap_chunk_cells = 0, cap_rank_cells = 0;
+    int64_t cap_slots = 0, cap_chunk_cells = 0, cap_rank_cells = 0, cap_experts = 0;
     void* dev_block = nullptr;
     int32_t* meta = nullptr;        // [ep::kMetaWords]
     int32_t* row_of_slot = nullptr; // [cap_slots]
     int32_t* chunk_cnt = nullptr;   // [cap_chunk_cells]
     int32_t* block_rank = nullptr;  // [cap_rank_cells]
+    int32_t* counts = nullptr;      // [cap_experts] copy of num_tokens_per_expert
+    int32_t* offsets = nullptr;     // [cap_experts + 1] copy of expert_offsets
     int32_t* host_meta = nullptr;   // pinned [ep::kMetaWords]
 };
 
@@ -50,15 +53,15 @@ ep_status_t current_device_is(const ep_handle* h) {
 void release_block(ep_handle* h) {
     if (h->dev_block) h->free_fn(h->dev_block);
     h->dev_block = nullptr;
-    h->meta = h->row_of_slot = h->chunk_cnt = h->block_rank = nullptr;
-    h->cap_slots = h->cap_chunk_cells = h->cap_rank_cells = 0;
+    h->meta = h->row_of_slot = h->chunk_cnt = h->block_rank = h->counts = h->offsets = nullptr;
+    h->cap_slots = h->cap_chunk_cells = h->cap_rank_cells = h->cap_experts = 0;
 }
 
 // (Re)allocate the device block for at least the given sizes; zeroes the state words.
 ep_status_t ensure_block(ep_handle* h, int64_t slots, int64_t chunk_cells, int64_t rank_cells,
-                         cudaStream_t stream) {
+                         int64_t experts, cudaStream_t stream) {
     if (h->dev_block && slots <= h->cap_slots && chunk_cells <= h->cap_chunk_cells &&
-        rank_cells <= h->cap_rank_cells)
+        rank_cells <= h->cap_rank_cells && experts <= h->cap_experts)
         return EP_OK;
     if (h->dev_block) {
         // work already enqueued may still read the old block
@@ -70,17 +73,22 @@ ep_status_t ensure_block(ep_handle* h, int64_t slots, int64_t chunk_cells, int64
     const size_t rows_b = round_up(sizeof(int32_t) * static_cast<size_t>(slots > 0 ? slots : 1), a);
     const size_t cnt_b = round_up(sizeof(int32_t) * static_cast<size_t>(chunk_cells > 0 ? chunk_cells : 1), a);
     const size_t rank_b = round_up(sizeof(int32_t) * static_cast<size_t>(rank_cells > 0 ? rank_cells : 1), a);
+    const size_t exp_b = round_up(sizeof(int32_t) * static_cast<size_t>(2 * experts + 1), a);
     void* block = nullptr;
-    if (h->alloc_fn(&block, meta_b + rows_b + cnt_b + rank_b) != 0 || block == nullptr) return EP_ERR_ALLOC;
+    if (h->alloc_fn(&block, meta_b + rows_b + cnt_b + rank_b + exp_b) != 0 || block == nullptr)
+        return EP_ERR_ALLOC;
     char* base = static_cast<char*>(block);
     h->dev_block = block;
     h->meta = reinterpret_cast<int32_t*>(base);
     h->row_of_slot = reinterpret_cast<int32_t*>(base + meta_b);
     h->chunk_cnt = reinterpret_cast<int32_t*>(base + meta_b + rows_b);
     h->block_rank = reinterpret_cast<int32_t*>(base + meta_b + rows_b + cnt_b);
+    h->counts = reinterpret_cast<int32_t*>(base + meta_b + rows_b + cnt_b + rank_b);
+    h->offsets = h->counts + experts;
     h->cap_slots = slots;
     h->cap_chunk_cells = chunk_cells;
     h->cap_rank_cells = rank_cells;
+    h->cap_experts = experts;
     // stream-ordered so the first layout on `stream` sees zeroed state words
     if (cudaMemsetAsync(h->meta, 0, meta_b, stream) != cudaSuccess) return EP_ERR_CUDA;
     return EP_OK;
@@ -98,11 +106,16 @@ ep_status_t read_meta(ep_handle* h, int64_t* rows, int32_t* err) {
     return EP_OK;
 }
 
+// Most receive rows a routing can need: every slot valid, every expert padded.
+int64_t max_rows_of(int T, int K, int E, int align) {
+    return static_cast<int64_t>(T) * K + static_cast<int64_t>(E) * (align - 1);
+}
+
 // Rows that a consumer buffer must hold: skip the device read when the
-// buffer holds T*K rows, the most a routing can produce.
+// buffer holds the most a routing can produce.
 ep_status_t check_rows(ep_handle* h, int64_t capacity) {
     if (h->error_latched) return EP_ERR_INVALID_EXPERT;
-    const int64_t max_rows = static_cast<int64_t>(h->T) * h->K;
+    const int64_t max_rows = max_rows_of(h->T, h->K, h->E, h->align);
     if (capacity >= max_rows) return EP_OK;
     int64_t n = 0;
     int32_t err = 0;
@@ -114,19 +127,20 @@ ep_status_t check_rows(ep_handle* h, int64_t capacity) {
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-ep_status_t ep_layout(const int64_t* topk_idx, int T, int K, int E, int R,
-                      int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
-                      uint8_t* is_token_in_rank, int32_t* expert_offsets,
-                      ep_alloc_fn alloc_fn, ep_free_fn free_fn,
-                      ep_handle_t* handle, void* stream) {
+ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int align,
+                        int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                        uint8_t* is_token_in_rank, int32_t* expert_offsets,
+                        ep_alloc_fn alloc_fn, ep_free_fn free_fn,
+                        ep_handle_t* handle, void* stream) {
     if (!handle || !num_tokens_per_expert || !num_tokens_per_rank || !expert_offsets)
         return EP_ERR_INVALID_ARG;
     if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS || R < 1 || R > EP_MAX_RANKS ||
         E % R != 0)
         return EP_ERR_INVALID_ARG;
-    if (static_cast<int64_t>(T) * K >= (int64_t{1} << 31)) return EP_ERR_INVALID_ARG;
+    if (align < 1 || align > EP_MAX_ALIGNMENT) return EP_ERR_INVALID_ARG;
+    if (max_rows_of(T, K, E, align) >= (int64_t{1} << 31)) return EP_ERR_INVALID_ARG;
     if (T > 0 && (!topk_idx || !is_token_in_rank)) return EP_ERR_INVALID_ARG;
     if ((alloc_fn == nullptr) != (free_fn == nullptr)) return EP_ERR_INVALID_ARG;
     if (!aligned(topk_idx, 8) || !aligned(num_tokens_per_expert, 4) || !aligned(num_tokens_per_rank, 4) ||
@@ -153,10 +167,11 @@ ep_status_t ep_layout(const int64_t* topk_idx, int T, int K, int E, int R,
         if (st != EP_OK) return st;
     }
 
-    const ep::LayoutPlan plan = ep::make_layout_plan(T, K, E, R);
+    ep::LayoutPlan plan = ep::make_layout_plan(T, K, E, R);
+    plan.align = align;
     ep_status_t st = ensure_block(h, static_cast<int64_t>(T) * K,
                                   static_cast<int64_t>(E) * plan.num_chunks,
-                                  static_cast<int64_t>(R) * plan.num_blocks, s);
+                                  static_cast<int64_t>(R) * plan.num_blocks, E, s);
     if (st != EP_OK) {
         if (created) {
             cudaFreeHost(h->host_meta);
@@ -168,6 +183,7 @@ ep_status_t ep_layout(const int64_t* topk_idx, int T, int K, int E, int R,
         return st;
     }
     h->T = T; h->K = K; h->E = E; h->R = R;
+    h->align = align;
     h->plan = plan;
     h->layout_stream = s;
     h->error_latched = false;
@@ -178,6 +194,7 @@ ep_status_t ep_layout(const int64_t* topk_idx, int T, int K, int E, int R,
         if (err == cudaSuccess) err = cudaMemsetAsync(num_tokens_per_rank, 0, sizeof(int32_t) * R, s);
         if (err == cudaSuccess) err = cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E + 1), s);
         if (err == cudaSuccess) err = cudaMemsetAsync(h->meta, 0, sizeof(int32_t) * ep::kMetaWords, s);
+        if (err == cudaSuccess) err = cudaMemsetAsync(h->counts, 0, sizeof(int32_t) * (2 * E + 1), s);
     } else {
         ep::LayoutArgs a{};
         a.topk_idx = topk_idx;
@@ -189,11 +206,35 @@ ep_status_t ep_layout(const int64_t* topk_idx, int T, int K, int E, int R,
         a.chunk_cnt = h->chunk_cnt;
         a.block_rank = h->block_rank;
         a.meta = h->meta;
+        a.h_counts = h->counts;
+        a.h_offsets = h->offsets;
         err = ep::launch_layout(plan, a, s, &h->layout_kernels);
     }
     if (T == 0) h->layout_kernels = 0;
     *handle = h;
     return err == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+ep_status_t ep_layout(const int64_t* topk_idx, int T, int K, int E, int R,
+                      int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                      uint8_t* is_token_in_rank, int32_t* expert_offsets,
+                      ep_alloc_fn alloc_fn, ep_free_fn free_fn,
+                      ep_handle_t* handle, void* stream) {
+    return layout_impl(topk_idx, T, K, E, R, 1, num_tokens_per_expert, num_tokens_per_rank, is_token_in_rank,
+                       expert_offsets, alloc_fn, free_fn, handle, stream);
+}
+
+ep_status_t ep_layout_aligned(const int64_t* topk_idx, int T, int K, int E, int R, int expert_alignment,
+                              int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                              uint8_t* is_token_in_rank, int32_t* expert_offsets,
+                              ep_alloc_fn alloc_fn, ep_free_fn free_fn,
+                              ep_handle_t* handle, void* stream) {
+    return layout_impl(topk_idx, T, K, E, R, expert_alignment, num_tokens_per_expert, num_tokens_per_rank,
+                       is_token_in_rank, expert_offsets, alloc_fn, free_fn, handle, stream);
 }
 
 ep_status_t ep_dispatch(ep_handle_t handle, const void* x, int H, ep_dtype_t out_dtype,
@@ -204,9 +245,12 @@ ep_status_t ep_dispatch(ep_handle_t handle, const void* x, int H, ep_dtype_t out
     if (H < 8 || H % 8 != 0 || recv_capacity < 0) return EP_ERR_INVALID_ARG;
     if (out_dtype != EP_DTYPE_BF16 && out_dtype != EP_DTYPE_FP8_E4M3) return EP_ERR_INVALID_ARG;
     const bool fp8 = out_dtype == EP_DTYPE_FP8_E4M3;
-    if (fp8 && (H % 128 != 0 || !recv_scales || !aligned(recv_scales, 4))) return EP_ERR_INVALID_ARG;
+    if (fp8 && (H % 128 != 0 || !aligned(recv_scales, 4))) return EP_ERR_INVALID_ARG;
     if (recv_weights && !topk_weights) return EP_ERR_INVALID_ARG;
-    if (handle->T > 0 && (!x || !recv_x)) return EP_ERR_INVALID_ARG;
+    if (handle->T > 0 && !x) return EP_ERR_INVALID_ARG;
+    // zero-row receive buffers may be NULL; the capacity check below then
+    // guarantees no row is written
+    if (recv_capacity > 0 && (!recv_x || (fp8 && !recv_scales))) return EP_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(recv_x, 16) || !aligned(topk_weights, 4) || !aligned(recv_src_token, 4) ||
         !aligned(recv_weights, 4))
         return EP_ERR_INVALID_ARG;
@@ -229,6 +273,11 @@ ep_status_t ep_dispatch(ep_handle_t handle, const void* x, int H, ep_dtype_t out
     a.H = H;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t err = fp8 ? ep::launch_dispatch_fp8(a, s) : ep::launch_dispatch_bf16(a, s);
+    if (err == cudaSuccess && handle->align > 1 && handle->T > 0)
+        err = ep::launch_fill_pad_rows(handle->counts, handle->offsets, handle->E,
+                                       fp8 ? static_cast<int64_t>(H) : static_cast<int64_t>(H) * 2, recv_x,
+                                       fp8 ? recv_scales : nullptr, H / 128, recv_src_token, recv_weights, s,
+                                       handle->align - 1);
     return err == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
 

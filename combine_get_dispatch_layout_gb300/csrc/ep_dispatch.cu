@@ -149,6 +149,27 @@ dispatch_fp8_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
     }
 }
 
+// One warp per (expert, pad row): zero a pad row of an aligned layout.
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+fill_pad_rows_kernel(const int32_t* counts, const int32_t* offsets, int E, int max_pad, int64_t row_bytes,
+                     char* recv, float* scales, int nb, int32_t* src, float* weights) {
+    const int lane = threadIdx.x & 31;
+    const int64_t item = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int e = static_cast<int>(item / max_pad);
+    const int i = static_cast<int>(item - static_cast<int64_t>(e) * max_pad);
+    if (e >= E) return;
+    const int64_t row = static_cast<int64_t>(offsets[e]) + counts[e] + i;
+    if (row >= offsets[e + 1]) return;
+    int4* d = reinterpret_cast<int4*>(recv + row * row_bytes);   // row_bytes % 16 == 0
+    for (int64_t j = lane; j < row_bytes / 16; j += 32) d[j] = make_int4(0, 0, 0, 0);
+    if (scales)
+        for (int b = lane; b < nb; b += 32) scales[row * nb + b] = 0.0f;
+    if (lane == 0) {
+        if (src) src[row] = -1;
+        if (weights) weights[row] = 0.0f;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch_bf16(const DispatchArgs& a, cudaStream_t stream) {
@@ -159,6 +180,17 @@ cudaError_t launch_dispatch_bf16(const DispatchArgs& a, cudaStream_t stream) {
     if (items == 0) return cudaSuccess;
     const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
     dispatch_bf16_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a, items, segs);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fill_pad_rows(const int32_t* counts, const int32_t* offsets, int E, int64_t row_bytes,
+                                 void* recv, float* scales, int nb, int32_t* src, float* weights,
+                                 cudaStream_t stream, int max_pad) {
+    if (E == 0 || max_pad <= 0) return cudaSuccess;
+    const int64_t items = static_cast<int64_t>(E) * max_pad;
+    const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    fill_pad_rows_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(
+        counts, offsets, E, max_pad, row_bytes, static_cast<char*>(recv), scales, nb, src, weights);
     return cudaGetLastError();
 }
 

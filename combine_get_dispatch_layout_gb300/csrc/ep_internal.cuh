@@ -23,6 +23,7 @@ enum MetaWord : int {
 struct LayoutPlan {
     int T, K, E, R, L;
     int key_bits;            // bits of (expert id + 1)
+    int align;               // expert row alignment (1 = packed)
     int chunk_tokens;
     int num_chunks;
     int warps_per_block;
@@ -51,6 +52,8 @@ struct LayoutArgs {
     int32_t* chunk_cnt;        // [E][num_chunks]: counts, then exclusive bases
     int32_t* block_rank;       // [R][num_blocks]: per-block tokens per rank
     int32_t* meta;             // [kMetaWords]
+    int32_t* h_counts;         // [E] handle copy of the counts (or null)
+    int32_t* h_offsets;        // [E+1] handle copy of the offsets (or null)
 };
 
 // Launches the layout; *kernels (if not null) receives the number of kernels
@@ -71,6 +74,14 @@ struct DispatchArgs {
 
 cudaError_t launch_dispatch_bf16(const DispatchArgs& a, cudaStream_t stream);
 cudaError_t launch_dispatch_fp8(const DispatchArgs& a, cudaStream_t stream);
+
+// Zero the pad rows of an aligned layout: for each expert e the rows from
+// offsets[e] + counts[e] up to offsets[e+1] (at most max_pad of them) get
+// zero bytes (row_bytes each, a multiple of 16), scale 0 (if scales), source
+// -1 (if src) and weight 0 (if weights).
+cudaError_t launch_fill_pad_rows(const int32_t* counts, const int32_t* offsets, int E, int64_t row_bytes,
+                                 void* recv, float* scales, int nb, int32_t* src, float* weights,
+                                 cudaStream_t stream, int max_pad);
 
 struct CombineArgs {
     const void* y;             // bf16 [y_rows, H]

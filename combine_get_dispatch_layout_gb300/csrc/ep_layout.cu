@@ -6,8 +6,10 @@
 // once per destination; -1 for "not routed") and the DeepEP API docs ("Prefix
 // Sum Interpretation for Expert Token Counts": expert i owns a contiguous row
 // range given by a prefix sum of counts; "dispatch()" with do_expand: one row
-// per (token, expert) pair). Rows inside an expert are in ascending (token, k)
-// order, which makes the permutation deterministic.
+// per (token, expert) pair; expert_alignment: each expert's rows start on a
+// multiple of the alignment, its real rows first and pad rows after). Rows
+// inside an expert are in ascending (token, k) order, which makes the
+// permutation deterministic.
 //
 // GPU design (three short launches, no host sync, no memset):
 //   count  : each warp owns a chunk of consecutive tokens and builds its
@@ -72,6 +74,8 @@ __device__ __forceinline__ unsigned peer_mask(int key, int nbits) {
     }
     return peers;
 }
+
+__device__ __forceinline__ int round_up_to(int v, int a) { return (v + a - 1) / a * a; }
 
 // Classify a slot: expert id in [0, E) -> id, -1 or out of range -> -1.
 __device__ __forceinline__ int slot_key(int64_t e, int E, bool& bad) {
@@ -241,13 +245,21 @@ layout_assign_kernel(LayoutPlan p, LayoutArgs a) {
     int* warp_tmp = smem + p.E;                        // [33]
     int* run = smem + p.E + 33 + warp * p.E;           // this warp's running rows
     // every block rebuilds the E offsets from the totals (E <= 4096 values)
-    for (int e = threadIdx.x; e < p.E; e += blockDim.x) offs[e] = a.num_tokens_per_expert[e];
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+        const int c = a.num_tokens_per_expert[e];
+        offs[e] = round_up_to(c, p.align);
+        if (blockIdx.x == 0 && a.h_counts) a.h_counts[e] = c;
+    }
     __syncthreads();
     const int n_rows = block_exclusive_scan(offs, p.E, warp_tmp);
     if (blockIdx.x == 0) {
-        for (int e = threadIdx.x; e < p.E; e += blockDim.x) a.expert_offsets[e] = offs[e];
+        for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+            a.expert_offsets[e] = offs[e];
+            if (a.h_offsets) a.h_offsets[e] = offs[e];
+        }
         if (threadIdx.x == 0) {
             a.expert_offsets[p.E] = n_rows;
+            if (a.h_offsets) a.h_offsets[p.E] = n_rows;
             a.meta[kMetaRows] = n_rows;
         }
     }
@@ -481,8 +493,11 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
             total += v;
         }
         cta_base[e] = below;
-        offs[e] = total;
-        if (cta == 0) a.num_tokens_per_expert[e] = total;
+        offs[e] = round_up_to(total, p.align);
+        if (cta == 0) {
+            a.num_tokens_per_expert[e] = total;
+            if (a.h_counts) a.h_counts[e] = total;
+        }
     }
     if (cta == 0) {
         for (int r = threadIdx.x; r < R; r += blockDim.x) {
@@ -501,12 +516,16 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
         const int n_rows = warp_exclusive_scan(offs, E, lane);
         if (cta == 0 && lane == 0) {
             a.expert_offsets[E] = n_rows;
+            if (a.h_offsets) a.h_offsets[E] = n_rows;
             a.meta[kMetaRows] = n_rows;
         }
     }
     __syncthreads();
     if (cta == 0)
-        for (int e = threadIdx.x; e < E; e += blockDim.x) a.expert_offsets[e] = offs[e];
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            a.expert_offsets[e] = offs[e];
+            if (a.h_offsets) a.h_offsets[e] = offs[e];
+        }
 
     // ---- phase 4: row = expert offset + rows in lower CTAs + rows in lower
     // warps of this CTA + the slot's local rank
@@ -525,6 +544,7 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
 LayoutPlan make_layout_plan(int T, int K, int E, int R) {
     LayoutPlan p{};
     p.T = T; p.K = K; p.E = E; p.R = R; p.L = E / R;
+    p.align = 1;
     p.key_bits = 1;
     while ((1 << p.key_bits) < E + 1) ++p.key_bits;   // keys -1..E-1 shift to 0..E
     // About 256 warp-chunks: enough parallelism for a latency-bound pass while

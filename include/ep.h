@@ -78,6 +78,7 @@ typedef int (*ep_free_fn)(void* ptr);
 #define EP_MAX_EXPERTS 4096
 #define EP_MAX_RANKS 1024
 #define EP_MAX_TOPK 32
+#define EP_MAX_ALIGNMENT 1024
 
 /*
  * ep_layout -- routing layout of topk_idx (the "get dispatch layout" step).
@@ -121,6 +122,34 @@ EP_API ep_status_t ep_layout(const int64_t* topk_idx, int T, int K, int E, int R
                       ep_handle_t* handle, void* stream);
 
 /*
+ * ep_layout_aligned -- ep_layout with every expert's receive rows starting on
+ * a multiple of expert_alignment (DeepEP API docs, "dispatch()"
+ * expert_alignment, and "Prefix Sum Interpretation for Expert Token Counts":
+ * in expand mode an expert's range starts at the previous expert's end
+ * rounded up to the alignment), for consumers such as grouped GEMMs that
+ * want tile-aligned expert blocks.
+ *
+ *  expert_alignment       1 <= A <= EP_MAX_ALIGNMENT; A = 1 is ep_layout.
+ *  num_tokens_per_expert  real slots per expert (unpadded).
+ *  expert_offsets         expert_offsets[e] = sum over e' < e of
+ *                         roundup(num_tokens_per_expert[e'], A);
+ *                         expert_offsets[E] = padded row total. Expert e's
+ *                         real rows are expert_offsets[e] + 0 .. count - 1
+ *                         in (token, k) order; the rest of its range, up to
+ *                         expert_offsets[e+1], are pad rows.
+ * Later ep_dispatch calls on the handle also zero the pad rows (zero bytes,
+ * scale 0, recv_src_token -1, recv_weights 0), and receive / combine-input
+ * buffers must hold the padded total (at most T*K + E*(A-1) rows).
+ * Other arguments, outputs and errors as ep_layout; T*K + E*(A-1) < 2^31.
+ */
+EP_API ep_status_t ep_layout_aligned(const int64_t* topk_idx, int T, int K, int E, int R,
+                                     int expert_alignment,
+                                     int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                                     uint8_t* is_token_in_rank, int32_t* expert_offsets,
+                                     ep_alloc_fn alloc_fn, ep_free_fn free_fn,
+                                     ep_handle_t* handle, void* stream);
+
+/*
  * ep_dispatch -- stable expert-major permute of the token rows.
  *
  * For every valid slot (t, k) with receive row n = row_of_slot[t, k]:
@@ -136,10 +165,14 @@ EP_API ep_status_t ep_layout(const int64_t* topk_idx, int T, int K, int E, int R
  *   recv_weights[n] = topk_weights[t, k]  (optional, fp32 [cap]; needs
  *                                  topk_weights; NULL = skip)
  * x is bf16 [T, H] (device); H % 8 == 0, and H % 128 == 0 for fp8.
- * Rows >= N of the receive buffers are not written.
+ * recv_x (and recv_scales for fp8) may be NULL only when recv_capacity is 0.
+ * After an aligned layout (ep_layout_aligned) the pad rows are written too:
+ * zero bytes, scale 0, recv_src_token -1, recv_weights 0.
+ * Rows >= N (the padded total after an aligned layout) are not written.
  * recv_capacity is the number of rows the receive buffers hold. If it is
- * below T*K the call reads N from the device (one stream synchronise) and
- * returns EP_ERR_CAPACITY, enqueuing nothing, when N > recv_capacity.
+ * below the most the routing can need (T*K, plus E*(A-1) when aligned) the
+ * call reads N from the device (one stream synchronise) and returns
+ * EP_ERR_CAPACITY, enqueuing nothing, when N > recv_capacity.
  * Returns EP_ERR_INVALID_EXPERT if the handle is known to have seen an
  * invalid expert id.
  */

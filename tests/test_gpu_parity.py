@@ -499,3 +499,91 @@ def test_pinned_host_buffers(ep):
     want = oracle.combine(inp.y, ref["row_of_slot"], inp.topk_weights)
     assert_combine(h_out.numpy().view(np.uint16), want)
     h.destroy()
+
+
+# ------------------------------------------------------------------ aligned layout
+
+def full_path_aligned(ep, inp, A, fp8=True):
+    w = inp.w
+    T, K, E, R, H = w.T, w.K, w.E, w.R, w.H
+    ref = oracle.layout_aligned(inp.topk_idx, E, R, A)
+    assert ref["status"] == oracle.OK
+    n_pad = int(ref["expert_offsets"][-1])
+    idx = _dev(inp.topk_idx)
+    cnt = torch.full((E,), -7, dtype=torch.int32, device="cuda")
+    ntr = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+    itr = torch.full((T, R), SENT8, dtype=torch.uint8, device="cuda")
+    off = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
+    h = ep.ep_layout_aligned(idx, E, R, A, cnt, ntr, itr, off)
+    rows = torch.full((T, K), -9, dtype=torch.int32, device="cuda")
+    ep.ep_handle_copy_row_of_slot(h, rows)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(cnt.cpu().numpy(), ref["num_tokens_per_expert"])
+    np.testing.assert_array_equal(ntr.cpu().numpy(), ref["num_tokens_per_rank"])
+    np.testing.assert_array_equal(itr.cpu().numpy(), ref["is_token_in_rank"])
+    np.testing.assert_array_equal(off.cpu().numpy(), ref["expert_offsets"])
+    np.testing.assert_array_equal(rows.cpu().numpy(), ref["row_of_slot"])
+    assert ep.ep_handle_query(h) == (n_pad, 0)
+    # bf16 dispatch: real rows and zeroed pad rows
+    r_x, r_src, r_w = oracle.dispatch_bf16(inp.x, ref["row_of_slot"], n_pad, inp.topk_weights)
+    oracle.fill_pad_rows(ref, r_x, src=r_src, weights=r_w)
+    recv = torch.full((n_pad + GUARD, H), SENT16, dtype=torch.int16, device="cuda")
+    src = torch.full((n_pad + GUARD,), -5, dtype=torch.int32, device="cuda")
+    rw = torch.full((n_pad + GUARD,), -3.0, dtype=torch.float32, device="cuda")
+    ep.ep_dispatch(h, _dev(inp.x.view(np.int16)), ep.EP_DTYPE_BF16, recv, n_pad + GUARD,
+                   recv_src_token=src, recv_weights=rw, topk_weights=_dev(inp.topk_weights))
+    torch.cuda.synchronize()
+    g = recv.cpu().numpy().view(np.uint16)
+    np.testing.assert_array_equal(g[:n_pad], r_x)
+    assert (g[n_pad:] == SENT16).all()
+    np.testing.assert_array_equal(src.cpu().numpy()[:n_pad], r_src)
+    np.testing.assert_array_equal(rw.cpu().numpy()[:n_pad].view(np.uint32), r_w.view(np.uint32))
+    if fp8 and H % 128 == 0:
+        r_q, r_s, _, _ = oracle.dispatch_e4m3(inp.x, ref["row_of_slot"], n_pad)
+        oracle.fill_pad_rows(ref, r_q, scales=r_s)
+        q = torch.full((n_pad, H), SENT8, dtype=torch.uint8, device="cuda")
+        sc = torch.full((n_pad, H // 128), -1.0, dtype=torch.float32, device="cuda")
+        ep.ep_dispatch(h, _dev(inp.x.view(np.int16)), ep.EP_DTYPE_FP8_E4M3, q, n_pad, recv_scales=sc)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(q.cpu().numpy(), r_q)
+        np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint32), r_s.view(np.uint32))
+    # combine over a padded expert-output buffer
+    y = gi.normal_bf16(np.random.SeedSequence(A), n_pad, H)
+    out = torch.full((T, H), SENT16, dtype=torch.int16, device="cuda")
+    ep.ep_combine(h, _dev(y.view(np.int16)) if n_pad else torch.empty((1, H), dtype=torch.int16, device="cuda"),
+                  out, topk_weights=_dev(inp.topk_weights), y_rows=n_pad)
+    torch.cuda.synchronize()
+    assert_combine(out.cpu().numpy().view(np.uint16), oracle.combine(y, ref["row_of_slot"], inp.topk_weights))
+    # the padded total is exactly enough; one row fewer is refused
+    if n_pad > 0:
+        small = torch.zeros((n_pad - 1, H), dtype=torch.int16, device="cuda")
+        with pytest.raises(ep.EPError) as e:
+            ep.ep_dispatch(h, _dev(inp.x.view(np.int16)), ep.EP_DTYPE_BF16, small, n_pad - 1)
+        assert e.value.status == ep.EP_ERR_CAPACITY
+    h.destroy()
+
+
+@pytest.mark.parametrize("name,A,T", [("tiny", 3, None), ("decode", 16, None), ("skewed", 64, None),
+                                      ("prefill", 128, None), ("fp8", 32, 1001), ("skewed", 7, 777)])
+def test_aligned_workloads(ep, name, A, T):
+    full_path_aligned(ep, gi.make(name, 1, T=T), A)
+
+
+@pytest.mark.parametrize("w,A", [
+    (_workload(50, 256, 8, 2, 2, drop_p=1.0), 8),                     # nothing routed: no pad rows
+    (_workload(1, 128, 1, 1, 1), 1024),                               # maximum alignment
+    (_workload(40000, 128, 64, 8, 4, routing="zipf", drop_p=0.05), 32),   # multi-block layout path
+    (_workload(300, 128, 512, 8, 64), 5),                             # R > 32
+])
+def test_aligned_edges(ep, w, A):
+    full_path_aligned(ep, gi.make(w, 2), A)
+
+
+def test_aligned_rejects_bad_alignment(ep):
+    idx = torch.zeros((4, 2), dtype=torch.int64, device="cuda")
+    o = [torch.empty(8, dtype=torch.int32, device="cuda"), torch.empty(2, dtype=torch.int32, device="cuda"),
+         torch.empty(8, dtype=torch.uint8, device="cuda"), torch.empty(9, dtype=torch.int32, device="cuda")]
+    for A in (0, -1, 1025):
+        with pytest.raises(ep.EPError) as e:
+            ep.ep_layout_aligned(idx, 8, 2, A, *o)
+        assert e.value.status == ep.EP_ERR_INVALID_ARG
