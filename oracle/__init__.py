@@ -51,6 +51,10 @@ def _lib():
             L.orc_layout_aligned.restype = i32
             L.orc_fill_pad_rows.argtypes = [P, P, i32, i64, P, P, i32, P, P]
             L.orc_fill_pad_rows.restype = None
+            L.orc_combine_backward.argtypes = [P, P, i32, P, i64, i32, P, P, P]
+            L.orc_combine_backward.restype = None
+            L.orc_dispatch_backward.argtypes = [P, P, i32, P, i64, i32, P, P]
+            L.orc_dispatch_backward.restype = None
             L.orc_dispatch_bf16.argtypes = [P, i64, i32, P, i32, P, P, P, P]
             L.orc_dispatch_bf16.restype = None
             L.orc_dispatch_e4m3.argtypes = [P, i64, i32, P, i32, P, P, P, P, P]
@@ -195,6 +199,34 @@ def combine_tokens(y: np.ndarray, row_of_slot: np.ndarray, topk_weights: np.ndar
         o = out[i]
         L.orc_combine_row(_p(y), H, _p(r), _p(wt), K, o.ctypes.data)
     return out
+
+
+def combine_backward(grad_out: np.ndarray, y: np.ndarray, row_of_slot: np.ndarray,
+                     topk_weights: np.ndarray | None, num_rows: int):
+    """(grad_y [num_rows, H] bf16 bits, zero where no slot writes; grad_w [T, K] float64)."""
+    g = _c(grad_out, np.uint16)
+    y = _c(y, np.uint16)
+    rows = _c(row_of_slot, np.int32)
+    T, K = rows.shape
+    H = g.shape[1]
+    w = _c(topk_weights, np.float32) if topk_weights is not None else None
+    gy = np.zeros((num_rows, H), np.uint16)
+    gw = np.zeros((T, K), np.float64)
+    _lib().orc_combine_backward(_p(g), _p(y), H, _p(rows), T, K, _p(w), _p(gy), _p(gw))
+    return gy, gw
+
+
+def dispatch_backward(grad_recv: np.ndarray, grad_recv_weights: np.ndarray | None, row_of_slot: np.ndarray):
+    """(grad_x [T, H] bf16 bits, grad_topk_weights [T, K] fp32 or None)."""
+    g = _c(grad_recv, np.uint16)
+    rows = _c(row_of_slot, np.int32)
+    T, K = rows.shape
+    H = g.shape[1]
+    gx = np.zeros((T, H), np.uint16)
+    gw = np.zeros((T, K), np.float32) if grad_recv_weights is not None else None
+    rw = _c(grad_recv_weights, np.float32) if grad_recv_weights is not None else None
+    _lib().orc_dispatch_backward(_p(g), _p(rw), H, _p(rows), T, K, _p(gx), _p(gw))
+    return gx, gw
 
 
 def f32_to_bf16(a: np.ndarray) -> np.ndarray:

@@ -339,3 +339,46 @@ void orc_fill_pad_rows(const int32_t* num_tokens_per_expert, const int32_t* expe
         }
     }
 }
+
+/* ---------------------------------------------------------------- backward */
+
+/* Backward of the weighted combine out[t] = sum_k w[t,k] * y[row(t,k)]
+ * (DeepEP API docs, README training snippet: the backward of combine is a
+ * dispatch; nccl_ep.cc, ncclEpCombine: the high-throughput backward mode also
+ * reduces the probabilities):
+ *   grad_y[row(t,k), h] = bf16( w[t,k] * grad_out[t, h] )   (fp32 product, one round)
+ *   grad_w[t, k]        = sum_h grad_out[t, h] * y[row(t,k), h]   (in double here)
+ * Dropped slots get grad_w = 0 and write no row. w == NULL means all ones. */
+void orc_combine_backward(const uint16_t* grad_out, const uint16_t* y, int H, const int32_t* row_of_slot,
+                          int64_t T, int K, const float* w, uint16_t* grad_y, double* grad_w) {
+    for (int64_t t = 0; t < T; ++t) {
+        for (int k = 0; k < K; ++k) {
+            int32_t row = row_of_slot[t * K + k];
+            double dot = 0.0;
+            if (row >= 0) {
+                float wk = w ? w[t * K + k] : 1.0f;
+                for (int h = 0; h < H; ++h) {
+                    float g = orc_bf16_to_f32(grad_out[t * H + h]);
+                    if (grad_y) grad_y[(int64_t)row * H + h] = orc_f32_to_bf16(wk * g);
+                    dot += (double)g * (double)orc_bf16_to_f32(y[(int64_t)row * H + h]);
+                }
+            }
+            if (grad_w) grad_w[t * K + k] = dot;
+        }
+    }
+}
+
+/* Backward of dispatch: grad_x[t] = bf16( sum over valid k of grad_recv[row(t,k)] )
+ * (fp32 adds in ascending k from +0, one round; the unweighted combine), and
+ * grad_topk_weights[t, k] = grad_recv_weights[row(t,k)], 0 for dropped slots. */
+void orc_dispatch_backward(const uint16_t* grad_recv, const float* grad_recv_weights, int H,
+                           const int32_t* row_of_slot, int64_t T, int K, uint16_t* grad_x,
+                           float* grad_topk_weights) {
+    orc_combine(grad_recv, H, row_of_slot, T, K, 0, grad_x);
+    if (grad_topk_weights) {
+        for (int64_t s = 0; s < T * (int64_t)K; ++s) {
+            int32_t row = row_of_slot[s];
+            grad_topk_weights[s] = row >= 0 ? grad_recv_weights[row] : 0.0f;
+        }
+    }
+}

@@ -350,3 +350,74 @@ def test_layout_aligned_one_is_plain_layout():
     a, b = oracle.layout_aligned(inp.topk_idx, w.E, w.R, 1), oracle.layout(inp.topk_idx, w.E, w.R)
     for key in ["expert_offsets", "row_of_slot", "num_tokens_per_expert"]:
         np.testing.assert_array_equal(a[key], b[key])
+
+
+# ------------------------------------------------------------------ backward
+
+def _small_routed(seed, T=40, K=3, E=8, R=2, H=24, drop_p=0.2):
+    rng = np.random.default_rng(seed)
+    idx = _random_routing(rng, T, K, E, drop_p, True, 0.0)
+    L = oracle.layout(idx, E, R)
+    N = int(L["expert_offsets"][-1])
+    y = gi.f32_to_bf16_bits(rng.standard_normal((N, H)).astype(np.float32))
+    g = gi.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    w = rng.random((T, K)).astype(np.float32)
+    return idx, L, N, y, g, w
+
+
+def test_combine_backward_vs_numpy():
+    idx, L, N, y, g, w = _small_routed(0)
+    rows = L["row_of_slot"]
+    gy, gw = oracle.combine_backward(g, y, rows, w, N)
+    gf, yf = gi.bf16_bits_to_f32(g), gi.bf16_bits_to_f32(y)
+    for t in range(rows.shape[0]):
+        for k in range(rows.shape[1]):
+            r = rows[t, k]
+            if r < 0:
+                assert gw[t, k] == 0.0
+                continue
+            # grad_y: the fp32 product rounded once to bf16 (torch's cast as the rounder)
+            prod = (np.float32(w[t, k]) * gf[t]).astype(np.float32)
+            want = torch.from_numpy(prod).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+            np.testing.assert_array_equal(gy[r], want)
+            np.testing.assert_allclose(gw[t, k], np.dot(gf[t].astype(np.float64), yf[r].astype(np.float64)),
+                                       rtol=1e-12, atol=1e-12)
+    covered = np.zeros(N, bool)
+    covered[rows[rows >= 0]] = True
+    assert covered.all()
+
+
+def test_combine_backward_adjoint_identity():
+    """<grad_out, combine(y)> equals sum over slots of w * <grad_out[t], y[row]> (exact in float64)."""
+    idx, L, N, y, g, w = _small_routed(1, T=60, K=4, E=12, R=3, H=40)
+    rows = L["row_of_slot"]
+    _, gw = oracle.combine_backward(g, y, rows, w, N)
+    gf, yf = gi.bf16_bits_to_f32(g).astype(np.float64), gi.bf16_bits_to_f32(y).astype(np.float64)
+    fwd = brute.combine_f64(gi.bf16_bits_to_f32(y), rows, w)
+    lhs = float((gf * fwd).sum())
+    rhs = float((w.astype(np.float64) * gw).sum())
+    assert abs(lhs - rhs) <= 1e-9 * max(1.0, abs(lhs))
+
+
+def test_combine_backward_unit_weights_copy_rows():
+    idx, L, N, y, g, w = _small_routed(2)
+    rows = L["row_of_slot"]
+    gy, _ = oracle.combine_backward(g, y, rows, None, N)
+    for t, k in zip(*np.nonzero(rows >= 0)):
+        np.testing.assert_array_equal(gy[rows[t, k]], g[t])   # w = 1: exact copy
+
+
+def test_dispatch_backward_is_unweighted_combine_and_gather():
+    idx, L, N, y, g, w = _small_routed(3)
+    rows = L["row_of_slot"]
+    rng = np.random.default_rng(9)
+    grw = rng.standard_normal(N).astype(np.float32)
+    gx, gtw = oracle.dispatch_backward(y, grw, rows)
+    np.testing.assert_array_equal(gx, oracle.combine(y, rows, None))
+    want = np.where(rows >= 0, grw[np.maximum(rows, 0)], 0.0).astype(np.float32)
+    np.testing.assert_array_equal(gtw, want)
+    # grad_x is the sum of the copies: against float64 within one bf16 rounding plus fp32 adds
+    ref = brute.combine_f64(gi.bf16_bits_to_f32(y), rows, None)
+    got = gi.bf16_bits_to_f32(gx).astype(np.float64)
+    mag = brute.combine_f64(np.abs(gi.bf16_bits_to_f32(y)), rows, None)
+    assert (np.abs(got - ref) <= 2.0**-8 * np.abs(ref) + rows.shape[1] * 2.0**-24 * mag + 1e-30).all()
