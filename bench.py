@@ -286,6 +286,30 @@ def gpu_arm(args, rank, world, local):
     ms_fp8 = float(np.mean([ev8[i].elapsed_time(ev8[i + 1]) for i in range(reps8)]))
     b_fp8 = bytes_dispatch_fp8(T, K, H, fp8.num_valid)
 
+    # backward passes on the same routing: combine backward (x stands in for
+    # grad_out, y for the forward expert outputs, recv receives grad_y) and
+    # dispatch backward (y stands in for grad_recv, out receives grad_x)
+    with torch.cuda.stream(stream):
+        gw = torch.empty(T, K, dtype=torch.float32, device=dev)
+        grw = torch.randn(N, dtype=torch.float32, device=dev)
+        gtw = torch.empty(T, K, dtype=torch.float32, device=dev)
+    reps_b = max(3, min(args.steps, 100))
+    ev_b = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps_b)]
+    for i in range(-3, reps_b):
+        if i >= 0:
+            ev_b[i][0].record(stream)
+        ep.ep_combine_backward(handle, x, y=y, topk_weights=wt, grad_y=recv, grad_topk_weights=gw, stream=stream)
+        if i >= 0:
+            ev_b[i][1].record(stream)
+        ep.ep_dispatch_backward(handle, y, out, grad_recv_weights=grw, grad_topk_weights=gtw, stream=stream)
+        if i >= 0:
+            ev_b[i][2].record(stream)
+    stream.synchronize()
+    ms_cbw = float(np.mean([e[0].elapsed_time(e[1]) for e in ev_b]))
+    ms_dbw = float(np.mean([e[1].elapsed_time(e[2]) for e in ev_b]))
+    b_cbw = 2 * T * H + 4 * N * H + 4 * T * K * 3
+    b_dbw = bytes_combine(T, K, H, N) + 4 * T * K + 4 * N + 4 * T * K
+
     # aligned layout (expert rows start on multiples of 128) + bf16 dispatch
     # including the pad rows' zero fill, on the prefill routing
     A = 128
@@ -363,6 +387,12 @@ def gpu_arm(args, rank, world, local):
                                          "gbs": round(b_dis_a / (ms_dis_a * 1e-3) / 1e9, 1),
                                          "frac_of_measured": round(b_dis_a / (ms_dis_a * 1e-3) / 1e9 / peak, 4),
                                          "frac_of_8tbs": round(b_dis_a / (ms_dis_a * 1e-3) / 8e12, 4)},
+            "combine_backward": {"us": round(ms_cbw * 1e3, 2), "bytes": b_cbw,
+                                 "gbs": round(b_cbw / (ms_cbw * 1e-3) / 1e9, 1),
+                                 "frac_of_measured": round(b_cbw / (ms_cbw * 1e-3) / 1e9 / peak, 4)},
+            "dispatch_backward": {"us": round(ms_dbw * 1e3, 2), "bytes": b_dbw,
+                                  "gbs": round(b_dbw / (ms_dbw * 1e-3) / 1e9, 1),
+                                  "frac_of_measured": round(b_dbw / (ms_dbw * 1e-3) / 1e9 / peak, 4)},
             "dispatch_fp8": {"workload": "fp8: x ~N(0,2^2) + 7 outlier channels x50, same shapes",
                              "us": round(ms_fp8 * 1e3, 2), "bytes": b_fp8,
                              "gbs": round(b_fp8 / (ms_fp8 * 1e-3) / 1e9, 1),

@@ -19,7 +19,8 @@ EP_OK, EP_ERR_INVALID_ARG, EP_ERR_INVALID_EXPERT, EP_ERR_CAPACITY, EP_ERR_CUDA, 
 EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3 = 0, 1
 
 # Exported symbols declared in include/ep.h.
-EXPORTS = ("ep_layout", "ep_layout_aligned", "ep_dispatch", "ep_combine", "ep_handle_query",
+EXPORTS = ("ep_layout", "ep_layout_aligned", "ep_dispatch", "ep_combine", "ep_combine_backward",
+           "ep_dispatch_backward", "ep_handle_query",
            "ep_handle_copy_row_of_slot", "ep_handle_destroy", "ep_handle_layout_kernels",
            "ep_layout_noalloc", "ep_status_string")
 
@@ -45,6 +46,8 @@ def lib() -> ctypes.CDLL:
         L.ep_layout_aligned.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, P, P, ctypes.POINTER(P), P]
         L.ep_dispatch.argtypes = [P, P, i32, i32, P, P, P, P, P, i64, P]
         L.ep_combine.argtypes = [P, P, i64, i32, P, P, P]
+        L.ep_combine_backward.argtypes = [P, P, P, i64, i32, P, P, i64, P, P]
+        L.ep_dispatch_backward.argtypes = [P, P, i64, i32, P, P, P, P]
         L.ep_handle_query.argtypes = [P, ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_int32)]
         L.ep_handle_copy_row_of_slot.argtypes = [P, P, P]
         L.ep_handle_destroy.argtypes = [P]
@@ -158,6 +161,28 @@ def ep_combine(handle: Handle, y, out, topk_weights=None, y_rows: int | None = N
     rows = int(y.shape[0]) if y_rows is None else int(y_rows)
     st = lib().ep_combine(handle.ptr, _ptr(y), rows, H, _ptr(topk_weights), _ptr(out), _stream(stream))
     _check(st, "ep_combine")
+
+
+def ep_combine_backward(handle: Handle, grad_out, y=None, topk_weights=None, grad_y=None,
+                        grad_topk_weights=None, y_rows: int | None = None, grad_y_capacity: int | None = None,
+                        stream=None) -> None:
+    """grad_y[row] = bf16(w * grad_out[t]); grad_topk_weights[t,k] = <grad_out[t], y[row]>."""
+    H = grad_out.shape[-1]
+    rows = (int(y.shape[0]) if y is not None else 0) if y_rows is None else int(y_rows)
+    cap = (int(grad_y.shape[0]) if grad_y is not None else 0) if grad_y_capacity is None else int(grad_y_capacity)
+    st = lib().ep_combine_backward(handle.ptr, _ptr(grad_out), _ptr(y), rows, H, _ptr(topk_weights), _ptr(grad_y),
+                                   cap, _ptr(grad_topk_weights), _stream(stream))
+    _check(st, "ep_combine_backward")
+
+
+def ep_dispatch_backward(handle: Handle, grad_recv, grad_x, grad_recv_weights=None, grad_topk_weights=None,
+                         grad_rows: int | None = None, stream=None) -> None:
+    """grad_x[t] = bf16(sum_k grad_recv[row(t,k)]); grad_topk_weights[t,k] = grad_recv_weights[row]."""
+    H = grad_x.shape[-1]
+    rows = int(grad_recv.shape[0]) if grad_rows is None else int(grad_rows)
+    st = lib().ep_dispatch_backward(handle.ptr, _ptr(grad_recv), rows, H, _ptr(grad_recv_weights), _ptr(grad_x),
+                                    _ptr(grad_topk_weights), _stream(stream))
+    _check(st, "ep_dispatch_backward")
 
 
 def ep_handle_query(handle: Handle) -> tuple[int, int]:

@@ -306,6 +306,61 @@ ep_status_t ep_combine(ep_handle_t handle, const void* y, int64_t y_rows, int H,
     return err == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
 
+ep_status_t ep_combine_backward(ep_handle_t handle, const void* grad_out, const void* y, int64_t y_rows, int H,
+                                const float* topk_weights, void* grad_y, int64_t grad_y_capacity,
+                                float* grad_topk_weights, void* stream) {
+    if (!handle) return EP_ERR_INVALID_ARG;
+    if (H < 8 || H % 8 != 0 || y_rows < 0 || grad_y_capacity < 0) return EP_ERR_INVALID_ARG;
+    if (handle->T > 0 && !grad_out) return EP_ERR_INVALID_ARG;
+    if (grad_topk_weights && y_rows > 0 && !y) return EP_ERR_INVALID_ARG;
+    if (grad_y_capacity > 0 && !grad_y) return EP_ERR_INVALID_ARG;
+    if (!aligned(grad_out, 16) || !aligned(y, 16) || !aligned(grad_y, 16) || !aligned(topk_weights, 4) ||
+        !aligned(grad_topk_weights, 4))
+        return EP_ERR_INVALID_ARG;
+    ep_status_t st = current_device_is(handle);
+    if (st != EP_OK) return st;
+    if (grad_y) {
+        st = check_rows(handle, grad_y_capacity);
+        if (st != EP_OK) return st;
+    }
+    if (grad_topk_weights) {
+        st = check_rows(handle, y_rows);
+        if (st != EP_OK) return st;
+    }
+    ep::CombineBackwardArgs a{};
+    a.grad_out = grad_out;
+    a.y = grad_topk_weights ? y : nullptr;
+    a.row_of_slot = handle->row_of_slot;
+    a.topk_weights = topk_weights;
+    a.grad_y = grad_y;
+    a.grad_w = grad_topk_weights;
+    a.T = handle->T;
+    a.K = handle->K;
+    a.H = H;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t err = cudaSuccess;
+    if (grad_y || grad_topk_weights) err = ep::launch_combine_backward(a, s);
+    if (err == cudaSuccess && grad_y && handle->align > 1 && handle->T > 0)
+        err = ep::launch_fill_pad_rows(handle->counts, handle->offsets, handle->E, static_cast<int64_t>(H) * 2,
+                                       grad_y, nullptr, 0, nullptr, nullptr, s, handle->align - 1);
+    return err == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+ep_status_t ep_dispatch_backward(ep_handle_t handle, const void* grad_recv, int64_t grad_rows, int H,
+                                 const float* grad_recv_weights, void* grad_x, float* grad_topk_weights,
+                                 void* stream) {
+    if (!handle) return EP_ERR_INVALID_ARG;
+    if (grad_topk_weights && !grad_recv_weights) return EP_ERR_INVALID_ARG;
+    if (!aligned(grad_recv_weights, 4) || !aligned(grad_topk_weights, 4)) return EP_ERR_INVALID_ARG;
+    ep_status_t st = ep_combine(handle, grad_recv, grad_rows, H, nullptr, grad_x, stream);
+    if (st != EP_OK || !grad_topk_weights) return st;
+    const int64_t slots = static_cast<int64_t>(handle->T) * handle->K;
+    return ep::launch_gather_slot_weights(handle->row_of_slot, grad_recv_weights, grad_topk_weights, slots,
+                                          static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? EP_OK
+               : EP_ERR_CUDA;
+}
+
 ep_status_t ep_handle_query(ep_handle_t handle, int64_t* num_recv_rows, int32_t* device_error) {
     if (!handle) return EP_ERR_INVALID_ARG;
     ep_status_t st = current_device_is(handle);

@@ -94,6 +94,20 @@ struct CombineArgs {
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
 
+struct CombineBackwardArgs {
+    const void* grad_out;      // bf16 [T, H]
+    const void* y;             // bf16 [rows, H] forward expert outputs
+    const int32_t* row_of_slot;
+    const float* topk_weights; // [T, K] or null (all ones)
+    void* grad_y;              // bf16 [rows, H] or null
+    float* grad_w;             // [T, K] or null
+    int T, K, H;
+};
+
+cudaError_t launch_combine_backward(const CombineBackwardArgs& a, cudaStream_t stream);
+cudaError_t launch_gather_slot_weights(const int32_t* row_of_slot, const float* row_weights, float* slot_weights,
+                                       int64_t slots, cudaStream_t stream);
+
 int device_sm_count();
 
 }  // namespace ep

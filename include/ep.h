@@ -196,6 +196,39 @@ EP_API ep_status_t ep_combine(ep_handle_t handle, const void* y, int64_t y_rows,
                        const float* topk_weights, void* out, void* stream);
 
 /*
+ * ep_combine_backward -- gradients of ep_combine (DeepEP API docs, README
+ * training snippet: the backward of combine is a dispatch; nccl_ep.cc,
+ * ncclEpCombine: its backward mode also reduces the probabilities).
+ *
+ *   grad_y[row(t,k), h]  = bf16_rne( w[t,k] * grad_out[t, h] )  (fp32 product)
+ *   grad_topk_weights[t,k] = sum over h of grad_out[t,h] * y[row(t,k), h]
+ *                          (fp32; 0 for dropped slots; a fixed reduction
+ *                          order, so repeated calls give the same bits)
+ * grad_out is bf16 [T, H]; y is the forward expert output bf16 [y_rows, H]
+ * (needed only for grad_topk_weights); topk_weights fp32 [T, K] or NULL (all
+ * ones); grad_y bf16 [grad_y_capacity, H] or NULL; grad_topk_weights fp32
+ * [T, K] or NULL. After an aligned layout the pad rows of grad_y are zeroed.
+ * Buffers smaller than the most rows the routing can need trigger one stream
+ * synchronise and EP_ERR_CAPACITY if they hold fewer than N rows.
+ */
+EP_API ep_status_t ep_combine_backward(ep_handle_t handle, const void* grad_out, const void* y, int64_t y_rows,
+                                       int H, const float* topk_weights, void* grad_y,
+                                       int64_t grad_y_capacity, float* grad_topk_weights, void* stream);
+
+/*
+ * ep_dispatch_backward -- gradients of ep_dispatch (bf16 path): the
+ * unweighted combine of the row gradients (DeepEP API docs, README training
+ * snippet: the backward of dispatch is a combine),
+ *   grad_x[t] = bf16_rne( sum over valid k, ascending, of grad_recv[row(t,k)] ),
+ * and, if grad_recv_weights (fp32 [rows], the gradient of recv_weights) is
+ * given, grad_topk_weights[t,k] = grad_recv_weights[row(t,k)] (0 if dropped).
+ * grad_recv is bf16 [grad_rows, H]; grad_x is bf16 [T, H]. Errors as ep_combine.
+ */
+EP_API ep_status_t ep_dispatch_backward(ep_handle_t handle, const void* grad_recv, int64_t grad_rows, int H,
+                                        const float* grad_recv_weights, void* grad_x, float* grad_topk_weights,
+                                        void* stream);
+
+/*
  * ep_handle_query -- synchronous read of the handle's device state after the
  * last ep_layout: N (number of valid slots = receive rows) and the device
  * error word (0, or EP_ERR_INVALID_EXPERT). Synchronises the layout stream.

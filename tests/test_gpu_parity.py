@@ -587,3 +587,105 @@ def test_aligned_rejects_bad_alignment(ep):
         with pytest.raises(ep.EPError) as e:
             ep.ep_layout_aligned(idx, 8, 2, A, *o)
         assert e.value.status == ep.EP_ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------------ backward
+
+def _grad_w_bound(g_bits, y_bits, rows, H):
+    """|fp32 kernel - float64| bound for the weight gradient: each thread sums
+    8 * ceil(H/8/128) products with fused multiply-adds, then a 5-level shuffle
+    tree and a 4-term sum, each step adding at most 2^-24 relative to the sum
+    of |terms|."""
+    n_terms = 8 * (-(-(H // 8) // 128)) + 8
+    gf = np.abs(gi.bf16_bits_to_f32(g_bits).astype(np.float64))
+    yf = np.abs(gi.bf16_bits_to_f32(y_bits).astype(np.float64))
+    T, K = rows.shape
+    mag = np.zeros((T, K))
+    for k in range(K):
+        v = rows[:, k] >= 0
+        mag[v, k] = (gf[v] * yf[rows[v, k]]).sum(axis=1)
+    return 1.01 * n_terms * 2.0**-24 * mag + 1e-30
+
+
+def backward_path(ep, inp, A=1, weights=True):
+    w = inp.w
+    T, K, E, R, H = w.T, w.K, w.E, w.R, w.H
+    ref = oracle.layout_aligned(inp.topk_idx, E, R, A)
+    n = int(ref["expert_offsets"][-1])
+    idx = _dev(inp.topk_idx)
+    o = [torch.empty(E, dtype=torch.int32, device="cuda"), torch.empty(R, dtype=torch.int32, device="cuda"),
+         torch.empty(T, R, dtype=torch.uint8, device="cuda"), torch.empty(E + 1, dtype=torch.int32, device="cuda")]
+    h = ep.ep_layout_aligned(idx, E, R, A, *o)
+    rows = ref["row_of_slot"]
+    y = gi.normal_bf16(np.random.SeedSequence(21), n, H)
+    g = gi.normal_bf16(np.random.SeedSequence(22), T, H)
+    wt = inp.topk_weights if weights else None
+    # combine backward
+    gy = torch.full((n + GUARD, H), SENT16, dtype=torch.int16, device="cuda")
+    gw = torch.full((T, K), -9.0, dtype=torch.float32, device="cuda")
+    ep.ep_combine_backward(h, _dev(g.view(np.int16)), y=_dev(y.view(np.int16)) if n else None,
+                           topk_weights=_dev(wt) if wt is not None else None, grad_y=gy, grad_topk_weights=gw,
+                           y_rows=n, grad_y_capacity=n + GUARD)
+    torch.cuda.synchronize()
+    r_gy, r_gw = oracle.combine_backward(g, y, rows, wt, n)
+    got_gy = gy.cpu().numpy().view(np.uint16)
+    np.testing.assert_array_equal(got_gy[:n], r_gy)         # pad rows are zero in both
+    assert (got_gy[n:] == SENT16).all()
+    got_gw = gw.cpu().numpy().astype(np.float64)
+    assert (np.abs(got_gw - r_gw) <= _grad_w_bound(g, y, rows, H)).all()
+    assert (got_gw[rows < 0] == 0).all()
+    # repeated call: same bits
+    gw2 = torch.empty_like(gw)
+    ep.ep_combine_backward(h, _dev(g.view(np.int16)), y=_dev(y.view(np.int16)) if n else None,
+                           topk_weights=_dev(wt) if wt is not None else None, grad_topk_weights=gw2, y_rows=n)
+    torch.cuda.synchronize()
+    assert torch.equal(gw, gw2)
+    # dispatch backward: grad_x = unweighted combine, weight gradients gathered
+    grw = np.random.default_rng(23).standard_normal(max(n, 1)).astype(np.float32)[:n]
+    gx = torch.full((T, H), SENT16, dtype=torch.int16, device="cuda")
+    gtw = torch.full((T, K), -9.0, dtype=torch.float32, device="cuda")
+    ep.ep_dispatch_backward(h, _dev(y.view(np.int16)) if n else torch.empty((1, H), dtype=torch.int16, device="cuda"),
+                            gx, grad_recv_weights=_dev(grw) if n else torch.empty(1, device="cuda"),
+                            grad_topk_weights=gtw, grad_rows=n)
+    torch.cuda.synchronize()
+    r_gx, r_gtw = oracle.dispatch_backward(y, grw if n else np.zeros(1, np.float32), rows)
+    assert_combine(gx.cpu().numpy().view(np.uint16), r_gx)
+    np.testing.assert_array_equal(gtw.cpu().numpy().view(np.uint32), r_gtw.view(np.uint32))
+    h.destroy()
+
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("decode", None), ("skewed", 3000), ("prefill", 1024)])
+def test_backward_workloads(ep, name, T):
+    backward_path(ep, gi.make(name, 4, T=T, with_y=False))
+
+
+def test_backward_full_prefill(ep):
+    backward_path(ep, gi.make("prefill", 0, with_y=False))
+
+
+@pytest.mark.parametrize("A,weights", [(16, True), (1, False)])
+def test_backward_aligned_and_unweighted(ep, A, weights):
+    backward_path(ep, gi.make("skewed", 5, T=2000, with_y=False), A=A, weights=weights)
+
+
+def test_backward_all_dropped(ep):
+    backward_path(ep, gi.make(_workload(30, 128, 8, 2, 2, drop_p=1.0), 0, with_y=False))
+
+
+def test_combine_backward_exact_arithmetic(ep):
+    """Small-integer gradients and outputs make every product and partial sum
+    exact in fp32, so the weight gradient must equal the exact dot product."""
+    rng = np.random.default_rng(31)
+    T, K, E, R, H = 96, 4, 16, 4, 1024
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :K].astype(np.int64)
+    ref = oracle.layout(idx, E, R)
+    n = int(ref["expert_offsets"][-1])
+    y = gi.f32_to_bf16_bits(rng.integers(-3, 4, size=(n, H)).astype(np.float32))
+    g = gi.f32_to_bf16_bits(rng.integers(-3, 4, size=(T, H)).astype(np.float32))
+    run = Run(ep, idx, E, R)
+    gw = torch.empty(T, K, dtype=torch.float32, device="cuda")
+    ep.ep_combine_backward(run.h, _dev(g.view(np.int16)), y=_dev(y.view(np.int16)), grad_topk_weights=gw)
+    torch.cuda.synchronize()
+    _, r_gw = oracle.combine_backward(g, y, ref["row_of_slot"], None, n)
+    np.testing.assert_array_equal(gw.cpu().numpy().astype(np.float64), r_gw)
+    run.h.destroy()
