@@ -51,6 +51,12 @@ def _lib():
             L.orc_layout_aligned.restype = i32
             L.orc_fill_pad_rows.argtypes = [P, P, i32, i64, P, P, i32, P, P]
             L.orc_fill_pad_rows.restype = None
+            L.orc_pow2_ceil.argtypes = [ctypes.c_float]
+            L.orc_pow2_ceil.restype = ctypes.c_float
+            L.orc_quant_row_e4m3_pow2.argtypes = [P, i32, i32, P, P, P]
+            L.orc_quant_row_e4m3_pow2.restype = None
+            L.orc_dispatch_rows.argtypes = [P, i64, i64, P, i32, P]
+            L.orc_dispatch_rows.restype = None
             L.orc_combine_backward.argtypes = [P, P, i32, P, i64, i32, P, P, P]
             L.orc_combine_backward.restype = None
             L.orc_dispatch_backward.argtypes = [P, P, i32, P, i64, i32, P, P]
@@ -169,6 +175,49 @@ def quant_row_e4m3(xrow: np.ndarray):
     s = np.zeros(H // 128, np.float32)
     _lib().orc_quant_row_e4m3(_p(xrow), H, _p(q), _p(s))
     return q, s
+
+
+def pow2_ceil(s: float) -> float:
+    return float(_lib().orc_pow2_ceil(float(s)))
+
+
+def quant_row_e4m3_pow2(xrow: np.ndarray, ue8m0: bool = False):
+    """(codes [H] u8, scales [H/128] fp32 powers of two, or u8 exponent bytes if ue8m0)."""
+    xrow = _c(xrow, np.uint16)
+    H = xrow.shape[0]
+    q = np.zeros(H, np.uint8)
+    s = np.zeros(H // 128, np.uint8 if ue8m0 else np.float32)
+    if ue8m0:
+        _lib().orc_quant_row_e4m3_pow2(_p(xrow), H, 1, _p(q), None, _p(s))
+    else:
+        _lib().orc_quant_row_e4m3_pow2(_p(xrow), H, 0, _p(q), _p(s), None)
+    return q, s
+
+
+def dispatch_e4m3_pow2(x: np.ndarray, row_of_slot: np.ndarray, num_rows: int, ue8m0: bool = False):
+    """Power-of-two-scale quantise-permute: (codes [rows, H], scales [rows, H/128])."""
+    x = _c(x, np.uint16)
+    T, H = x.shape
+    q = np.zeros((T, H), np.uint8)
+    s = np.zeros((T, H // 128), np.uint8 if ue8m0 else np.float32)
+    for t in range(T):
+        q[t], s[t] = quant_row_e4m3_pow2(x[t], ue8m0)
+    rq = dispatch_rows(q, row_of_slot, num_rows)
+    rs = dispatch_rows(s, row_of_slot, num_rows)
+    return rq, rs
+
+
+def dispatch_rows(src: np.ndarray, row_of_slot: np.ndarray, num_rows: int, fill: int = 0) -> np.ndarray:
+    """Byte permute of rows of any dtype: out[row_of_slot[t,k]] = src[t]."""
+    src = np.ascontiguousarray(src)
+    rows = _c(row_of_slot, np.int32)
+    T = src.shape[0]
+    K = rows.shape[1]
+    out = np.full((num_rows,) + src.shape[1:], fill, src.dtype)
+    row_bytes = src.strides[0] if T else 0
+    _lib().orc_dispatch_rows(_p(src.view(np.uint8).reshape(T, -1)) if T else None, T, row_bytes, _p(rows), K,
+                             _p(out))
+    return out
 
 
 def combine(y: np.ndarray, row_of_slot: np.ndarray, topk_weights: np.ndarray | None):

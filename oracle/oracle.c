@@ -382,3 +382,61 @@ void orc_dispatch_backward(const uint16_t* grad_recv, const float* grad_recv_wei
         }
     }
 }
+
+/* ---------------------------------------------------------------- fp8 variants */
+
+/* Smallest power of two >= s (s > 0, finite fp32), found by exponent
+ * arithmetic on the exact value: frexp gives s = fr * 2^ex, fr in [0.5, 1);
+ * s is itself a power of two iff fr == 0.5. */
+float orc_pow2_ceil(float s) {
+    int ex;
+    double fr = frexp((double)s, &ex);
+    return (float)ldexp(1.0, fr == 0.5 ? ex - 1 : ex);
+}
+
+/* Quantise one row with power-of-two block scales (nccl_ep.cc, ncclEpDispatch:
+ * round_scales; DeepEP API docs: use_ue8m0 scale factors):
+ *   s = amax / 448 (fp32 division), scale = smallest power of two >= s,
+ *   q = e4m3_rne_satfinite(x / scale).
+ * ue8m0 != 0: the scale is stored as its biased exponent byte (value
+ * 2^(byte - 127)); powers below 2^-127 are raised to 2^-127 (byte 0) before
+ * quantising. An all-zero block gives zero codes and scale 0 (byte 0).
+ * Scales go to srow[b] as fp32, or to sbytes[b] as bytes when ue8m0. */
+void orc_quant_row_e4m3_pow2(const uint16_t* xrow, int H, int ue8m0, uint8_t* qrow, float* srow,
+                             uint8_t* sbytes) {
+    for (int b = 0; b < H / 128; ++b) {
+        float amax = 0.0f;
+        for (int i = 0; i < 128; ++i) {
+            float v = fabsf(orc_bf16_to_f32(xrow[b * 128 + i]));
+            if (v > amax) amax = v;
+        }
+        if (amax == 0.0f) {
+            if (ue8m0) sbytes[b] = 0; else srow[b] = 0.0f;
+            for (int i = 0; i < 128; ++i) qrow[b * 128 + i] = 0x00;
+            continue;
+        }
+        float scale = orc_pow2_ceil(amax / 448.0f);
+        if (ue8m0) {
+            if (scale < ldexpf(1.0f, -127)) scale = ldexpf(1.0f, -127);
+            int ex;
+            (void)frexpf(scale, &ex);          /* scale = 0.5 * 2^ex = 2^(ex-1) */
+            sbytes[b] = (uint8_t)(ex - 1 + 127);
+        } else {
+            srow[b] = scale;
+        }
+        for (int i = 0; i < 128; ++i)
+            qrow[b * 128 + i] = orc_f32_to_e4m3(orc_bf16_to_f32(xrow[b * 128 + i]) / scale);
+    }
+}
+
+/* Byte permute of whole rows: recv[row_of_slot[t,k]] = src[t] (row_bytes
+ * each) for every used slot -- fp8 input pass-through of codes and of scale
+ * rows (DeepEP API docs, dispatch(): x may be an (fp8 data, scales) tuple). */
+void orc_dispatch_rows(const uint8_t* src, int64_t T, int64_t row_bytes, const int32_t* row_of_slot, int K,
+                       uint8_t* recv) {
+    for (int64_t t = 0; t < T; ++t)
+        for (int k = 0; k < K; ++k) {
+            int32_t row = row_of_slot[t * K + k];
+            if (row >= 0) memcpy(recv + (int64_t)row * row_bytes, src + t * row_bytes, (size_t)row_bytes);
+        }
+}

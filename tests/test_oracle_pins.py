@@ -421,3 +421,72 @@ def test_dispatch_backward_is_unweighted_combine_and_gather():
     got = gi.bf16_bits_to_f32(gx).astype(np.float64)
     mag = brute.combine_f64(np.abs(gi.bf16_bits_to_f32(y)), rows, None)
     assert (np.abs(got - ref) <= 2.0**-8 * np.abs(ref) + rows.shape[1] * 2.0**-24 * mag + 1e-30).all()
+
+
+# ------------------------------------------------------------------ fp8 variants
+
+def test_fp8_pow2_golden(golden):
+    g = golden("fp8_pow2_hand.txt")
+    x = np.zeros(128, np.float32)
+    for kv in g["x"]:
+        i, v = kv.split(":")
+        x[int(i)] = float(v)
+    xb = gi.f32_to_bf16_bits(x)
+    q, s = oracle.quant_row_e4m3_pow2(xb)
+    assert s[0] == np.float32(float(g["scale"][0]))
+    _, sb = oracle.quant_row_e4m3_pow2(xb, ue8m0=True)
+    assert sb[0] == int(g["ue8m0"][0])
+    want = np.zeros(128, np.uint8)
+    for kv in g["q"]:
+        i, v = kv.split(":")
+        want[int(i)] = int(v, 16)
+    np.testing.assert_array_equal(q, want)
+
+
+def test_pow2_ceil_vs_numpy():
+    rng = np.random.default_rng(4)
+    s = np.concatenate([np.exp2(rng.integers(-140, 120, 200)).astype(np.float32),
+                        (rng.random(2000) * 10.0 ** rng.integers(-30, 30, 2000)).astype(np.float32)])
+    s = s[(s > 0) & np.isfinite(s)]
+    got = np.array([oracle.pow2_ceil(v) for v in s], np.float64)
+    want = np.exp2(np.ceil(np.log2(s.astype(np.float64))))
+    np.testing.assert_array_equal(got, want)
+
+
+def test_fp8_pow2_closed_forms():
+    rng = np.random.default_rng(5)
+    H = 1024
+    xf = (rng.standard_normal((32, H)) * 3).astype(np.float32)
+    xf[0, :128] = 0.0
+    xf[1, 128:256] = 1e-39            # amax/448 below 2^-127: UE8M0 clamps
+    xb = gi.f32_to_bf16_bits(xf)
+    xv = gi.bf16_bits_to_f32(xb).reshape(32, H // 128, 128)
+    for t in range(32):
+        q, s = oracle.quant_row_e4m3_pow2(xb[t])
+        qu, sb = oracle.quant_row_e4m3_pow2(xb[t], ue8m0=True)
+        for b in range(H // 128):
+            blk = xv[t, b]
+            amax = np.abs(blk).max()
+            if amax == 0:
+                assert s[b] == 0 and sb[b] == 0 and (q[b*128:(b+1)*128] == 0).all()
+                continue
+            s0 = np.float32(amax) / np.float32(448.0)
+            m, e = np.frexp(np.float64(s[b]))
+            assert m == 0.5 and s[b] >= s0 and (s[b] / 2 < s0)      # minimal power of two
+            # codes: x / scale is exact, so they equal torch's clamped cast of it
+            want = _torch_e4m3_bits((blk / s[b]).astype(np.float32))
+            np.testing.assert_array_equal(q[b*128:(b+1)*128], want)
+            ue_scale = max(float(s[b]), 2.0**-127)
+            assert sb[b] == int(np.log2(ue_scale)) + 127
+            want_u = _torch_e4m3_bits((blk / np.float32(ue_scale)).astype(np.float32))
+            np.testing.assert_array_equal(qu[b*128:(b+1)*128], want_u)
+
+
+def test_dispatch_rows_moves_any_row_type():
+    idx = _random_routing(np.random.default_rng(6), 30, 3, 8, 0.2, True, 0.0)
+    L = oracle.layout(idx, 8, 2)
+    N = int(L["expert_offsets"][-1])
+    src = np.random.default_rng(7).integers(0, 256, (30, 48), dtype=np.uint8)
+    out = oracle.dispatch_rows(src, L["row_of_slot"], N)
+    for t, k in zip(*np.nonzero(L["row_of_slot"] >= 0)):
+        np.testing.assert_array_equal(out[L["row_of_slot"][t, k]], src[t])
