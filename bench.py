@@ -286,6 +286,35 @@ def gpu_arm(args, rank, world, local):
     ms_fp8 = float(np.mean([ev8[i].elapsed_time(ev8[i + 1]) for i in range(reps8)]))
     b_fp8 = bytes_dispatch_fp8(T, K, H, fp8.num_valid)
 
+    # fp8 variants on the same routing: power-of-two scales; UE8M0 byte scales
+    # in column-major layout; fp8 input pass-through (codes and scales moved)
+    n8, nb = fp8.num_valid, H // 128
+    with torch.cuda.stream(stream):
+        sc_u = torch.empty(nb * n8, dtype=torch.uint8, device=dev)
+        codes_in = torch.randint(0, 256, (T, H), dtype=torch.uint8, device=dev)
+        scales_in = torch.rand(T, nb, dtype=torch.float32, device=dev)
+
+    def time_variant(fn):
+        for _ in range(3):
+            fn()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps8 + 1)]
+        for i in range(reps8):
+            evs[i].record(stream)
+            fn()
+        evs[reps8].record(stream)
+        stream.synchronize()
+        return float(np.mean([evs[i].elapsed_time(evs[i + 1]) for i in range(reps8)]))
+
+    ms_pow2 = time_variant(lambda: ep.ep_dispatch_ex(h8, x8, q, n8, scale_mode=ep.EP_SCALE_POW2, recv_scales=sc,
+                                                     stream=stream))
+    ms_ue8 = time_variant(lambda: ep.ep_dispatch_ex(h8, x8, q, n8, scale_mode=ep.EP_SCALE_UE8M0, recv_scales=sc_u,
+                                                    scales_col_major=True, scales_ld=n8, stream=stream))
+    ms_pass = time_variant(lambda: ep.ep_dispatch_ex(h8, codes_in, q, n8, in_dtype=ep.EP_DTYPE_FP8_E4M3,
+                                                     x_scales=scales_in, recv_scales=sc, H=H, stream=stream))
+    b_ue8 = 2 * T * H + n8 * H + n8 * nb + 4 * T * K
+    b_pass = T * H + 4 * T * nb + n8 * H + 4 * n8 * nb + 4 * T * K
+    del codes_in, scales_in, sc_u
+
     # backward passes on the same routing: combine backward (x stands in for
     # grad_out, y for the forward expert outputs, recv receives grad_y) and
     # dispatch backward (y stands in for grad_recv, out receives grad_x)
@@ -387,6 +416,15 @@ def gpu_arm(args, rank, world, local):
                                          "gbs": round(b_dis_a / (ms_dis_a * 1e-3) / 1e9, 1),
                                          "frac_of_measured": round(b_dis_a / (ms_dis_a * 1e-3) / 1e9 / peak, 4),
                                          "frac_of_8tbs": round(b_dis_a / (ms_dis_a * 1e-3) / 8e12, 4)},
+            "dispatch_fp8_pow2": {"us": round(ms_pow2 * 1e3, 2), "bytes": b_fp8,
+                                  "gbs": round(b_fp8 / (ms_pow2 * 1e-3) / 1e9, 1),
+                                  "frac_of_measured": round(b_fp8 / (ms_pow2 * 1e-3) / 1e9 / peak, 4)},
+            "dispatch_fp8_ue8m0_colmajor": {"us": round(ms_ue8 * 1e3, 2), "bytes": b_ue8,
+                                            "gbs": round(b_ue8 / (ms_ue8 * 1e-3) / 1e9, 1),
+                                            "frac_of_measured": round(b_ue8 / (ms_ue8 * 1e-3) / 1e9 / peak, 4)},
+            "dispatch_fp8_passthrough": {"us": round(ms_pass * 1e3, 2), "bytes": b_pass,
+                                         "gbs": round(b_pass / (ms_pass * 1e-3) / 1e9, 1),
+                                         "frac_of_measured": round(b_pass / (ms_pass * 1e-3) / 1e9 / peak, 4)},
             "combine_backward": {"us": round(ms_cbw * 1e3, 2), "bytes": b_cbw,
                                  "gbs": round(b_cbw / (ms_cbw * 1e-3) / 1e9, 1),
                                  "frac_of_measured": round(b_cbw / (ms_cbw * 1e-3) / 1e9 / peak, 4)},

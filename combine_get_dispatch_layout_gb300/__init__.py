@@ -17,9 +17,16 @@ from .build import LIB as _LIB_PATH, build
 
 EP_OK, EP_ERR_INVALID_ARG, EP_ERR_INVALID_EXPERT, EP_ERR_CAPACITY, EP_ERR_CUDA, EP_ERR_ALLOC = range(6)
 EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3 = 0, 1
+EP_SCALE_FP32, EP_SCALE_POW2, EP_SCALE_UE8M0 = 0, 1, 2
+
+
+class DispatchConfig(ctypes.Structure):
+    """ep_dispatch_config_t (include/ep.h)."""
+    _fields_ = [("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int), ("scale_mode", ctypes.c_int),
+                ("scales_col_major", ctypes.c_int), ("scales_ld", ctypes.c_int64)]
 
 # Exported symbols declared in include/ep.h.
-EXPORTS = ("ep_layout", "ep_layout_aligned", "ep_dispatch", "ep_combine", "ep_combine_backward",
+EXPORTS = ("ep_layout", "ep_layout_aligned", "ep_dispatch", "ep_dispatch_ex", "ep_combine", "ep_combine_backward",
            "ep_dispatch_backward", "ep_handle_query",
            "ep_handle_copy_row_of_slot", "ep_handle_destroy", "ep_handle_layout_kernels",
            "ep_layout_noalloc", "ep_status_string")
@@ -45,6 +52,7 @@ def lib() -> ctypes.CDLL:
         L.ep_layout.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, ctypes.POINTER(P), P]
         L.ep_layout_aligned.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, P, P, ctypes.POINTER(P), P]
         L.ep_dispatch.argtypes = [P, P, i32, i32, P, P, P, P, P, i64, P]
+        L.ep_dispatch_ex.argtypes = [P, P, P, i32, ctypes.POINTER(DispatchConfig), P, P, P, P, P, i64, P]
         L.ep_combine.argtypes = [P, P, i64, i32, P, P, P]
         L.ep_combine_backward.argtypes = [P, P, P, i64, i32, P, P, i64, P, P]
         L.ep_dispatch_backward.argtypes = [P, P, i64, i32, P, P, P, P]
@@ -153,6 +161,19 @@ def ep_dispatch(handle: Handle, x, out_dtype: int, recv_x, recv_capacity: int, r
                            _ptr(recv_scales), _ptr(recv_src_token), _ptr(recv_weights),
                            int(recv_capacity), _stream(stream))
     _check(st, "ep_dispatch")
+
+
+def ep_dispatch_ex(handle: Handle, x, recv_x, recv_capacity: int, out_dtype: int = EP_DTYPE_FP8_E4M3,
+                   in_dtype: int = EP_DTYPE_BF16, scale_mode: int = EP_SCALE_FP32, x_scales=None, recv_scales=None,
+                   scales_col_major: bool = False, scales_ld: int = 0, recv_src_token=None, recv_weights=None,
+                   topk_weights=None, H: int | None = None, stream=None) -> None:
+    """ep_dispatch with fp8 scale modes, column-major scales and fp8 input pass-through."""
+    H = int(x.shape[-1]) if H is None else int(H)
+    cfg = DispatchConfig(in_dtype, out_dtype, scale_mode, 1 if scales_col_major else 0, int(scales_ld))
+    st = lib().ep_dispatch_ex(handle.ptr, _ptr(x), _ptr(x_scales), H, ctypes.byref(cfg), _ptr(topk_weights),
+                              _ptr(recv_x), _ptr(recv_scales), _ptr(recv_src_token), _ptr(recv_weights),
+                              int(recv_capacity), _stream(stream))
+    _check(st, "ep_dispatch_ex")
 
 
 def ep_combine(handle: Handle, y, out, topk_weights=None, y_rows: int | None = None, stream=None) -> None:

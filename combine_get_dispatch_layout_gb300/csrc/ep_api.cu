@@ -237,15 +237,26 @@ ep_status_t ep_layout_aligned(const int64_t* topk_idx, int T, int K, int E, int 
                        is_token_in_rank, expert_offsets, alloc_fn, free_fn, handle, stream);
 }
 
-ep_status_t ep_dispatch(ep_handle_t handle, const void* x, int H, ep_dtype_t out_dtype,
-                        const float* topk_weights,
-                        void* recv_x, float* recv_scales, int32_t* recv_src_token,
-                        float* recv_weights, int64_t recv_capacity, void* stream) {
+ep_status_t ep_dispatch_ex(ep_handle_t handle, const void* x, const void* x_scales, int H,
+                           const ep_dispatch_config_t* config, const float* topk_weights,
+                           void* recv_x, void* recv_scales, int32_t* recv_src_token,
+                           float* recv_weights, int64_t recv_capacity, void* stream) {
     if (!handle) return EP_ERR_INVALID_ARG;
+    ep_dispatch_config_t cfg{};
+    if (config) cfg = *config;
+    if (cfg.in_dtype != EP_DTYPE_BF16 && cfg.in_dtype != EP_DTYPE_FP8_E4M3) return EP_ERR_INVALID_ARG;
+    if (cfg.out_dtype != EP_DTYPE_BF16 && cfg.out_dtype != EP_DTYPE_FP8_E4M3) return EP_ERR_INVALID_ARG;
+    if (cfg.in_dtype == EP_DTYPE_FP8_E4M3 && cfg.out_dtype != EP_DTYPE_FP8_E4M3) return EP_ERR_INVALID_ARG;
+    if (cfg.scale_mode != EP_SCALE_FP32 && cfg.scale_mode != EP_SCALE_POW2 && cfg.scale_mode != EP_SCALE_UE8M0)
+        return EP_ERR_INVALID_ARG;
+    const bool fp8 = cfg.out_dtype == EP_DTYPE_FP8_E4M3;
+    const bool fp8_in = cfg.in_dtype == EP_DTYPE_FP8_E4M3;
     if (H < 8 || H % 8 != 0 || recv_capacity < 0) return EP_ERR_INVALID_ARG;
-    if (out_dtype != EP_DTYPE_BF16 && out_dtype != EP_DTYPE_FP8_E4M3) return EP_ERR_INVALID_ARG;
-    const bool fp8 = out_dtype == EP_DTYPE_FP8_E4M3;
-    if (fp8 && (H % 128 != 0 || !aligned(recv_scales, 4))) return EP_ERR_INVALID_ARG;
+    if (fp8 && H % 128 != 0) return EP_ERR_INVALID_ARG;
+    const size_t scale_bytes = cfg.scale_mode == EP_SCALE_UE8M0 ? 1 : 4;
+    if (fp8 && !aligned(recv_scales, scale_bytes)) return EP_ERR_INVALID_ARG;
+    if (fp8 && cfg.scales_col_major && cfg.scales_ld < recv_capacity) return EP_ERR_INVALID_ARG;
+    if (fp8_in && handle->T > 0 && (!x_scales || !aligned(x_scales, scale_bytes))) return EP_ERR_INVALID_ARG;
     if (recv_weights && !topk_weights) return EP_ERR_INVALID_ARG;
     if (handle->T > 0 && !x) return EP_ERR_INVALID_ARG;
     // zero-row receive buffers may be NULL; the capacity check below then
@@ -271,14 +282,39 @@ ep_status_t ep_dispatch(ep_handle_t handle, const void* x, int H, ep_dtype_t out
     a.T = handle->T;
     a.K = handle->K;
     a.H = H;
+    a.scale_mode = cfg.scale_mode;
+    a.scale_col_major = cfg.scales_col_major ? 1 : 0;
+    a.scale_ld = cfg.scales_ld;
+    a.x_scales = x_scales;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t err = fp8 ? ep::launch_dispatch_fp8(a, s) : ep::launch_dispatch_bf16(a, s);
-    if (err == cudaSuccess && handle->align > 1 && handle->T > 0)
+    cudaError_t err = fp8_in ? ep::launch_dispatch_fp8_passthrough(a, s)
+                      : fp8  ? ep::launch_dispatch_fp8(a, s)
+                             : ep::launch_dispatch_bf16(a, s);
+    if (err == cudaSuccess && handle->align > 1 && handle->T > 0) {
+        ep::PadScales ps;
+        if (fp8) {
+            ps.ptr = recv_scales;
+            ps.nb = H / 128;
+            ps.bytes = static_cast<int>(scale_bytes);
+            ps.col_major = a.scale_col_major;
+            ps.ld = cfg.scales_ld;
+        }
         err = ep::launch_fill_pad_rows(handle->counts, handle->offsets, handle->E,
-                                       fp8 ? static_cast<int64_t>(H) : static_cast<int64_t>(H) * 2, recv_x,
-                                       fp8 ? recv_scales : nullptr, H / 128, recv_src_token, recv_weights, s,
-                                       handle->align - 1);
+                                       fp8 ? static_cast<int64_t>(H) : static_cast<int64_t>(H) * 2, recv_x, ps,
+                                       recv_src_token, recv_weights, s, handle->align - 1);
+    }
     return err == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+ep_status_t ep_dispatch(ep_handle_t handle, const void* x, int H, ep_dtype_t out_dtype,
+                        const float* topk_weights,
+                        void* recv_x, float* recv_scales, int32_t* recv_src_token,
+                        float* recv_weights, int64_t recv_capacity, void* stream) {
+    ep_dispatch_config_t cfg{};
+    cfg.in_dtype = EP_DTYPE_BF16;
+    cfg.out_dtype = out_dtype;
+    return ep_dispatch_ex(handle, x, nullptr, H, &cfg, topk_weights, recv_x, recv_scales, recv_src_token,
+                          recv_weights, recv_capacity, stream);
 }
 
 ep_status_t ep_combine(ep_handle_t handle, const void* y, int64_t y_rows, int H,
@@ -342,7 +378,7 @@ ep_status_t ep_combine_backward(ep_handle_t handle, const void* grad_out, const 
     if (grad_y || grad_topk_weights) err = ep::launch_combine_backward(a, s);
     if (err == cudaSuccess && grad_y && handle->align > 1 && handle->T > 0)
         err = ep::launch_fill_pad_rows(handle->counts, handle->offsets, handle->E, static_cast<int64_t>(H) * 2,
-                                       grad_y, nullptr, 0, nullptr, nullptr, s, handle->align - 1);
+                                       grad_y, ep::PadScales{}, nullptr, nullptr, s, handle->align - 1);
     return err == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
 

@@ -88,6 +88,28 @@ __device__ __forceinline__ unsigned short e4m3x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(unsigned u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(unsigned u) { return __uint_as_float(u & 0xffff0000u); }
 
+// Smallest power of two >= s (s > 0, finite), from the bit pattern: a
+// normal s with a zero mantissa is already a power of two, otherwise the next
+// exponent; a subnormal s (value f * 2^-149) rounds its mantissa f up to a
+// power of two, which is itself the bit pattern of the result (2^23 being the
+// smallest normal).
+__device__ __forceinline__ float pow2_ceil(float s) {
+    const unsigned u = __float_as_uint(s);
+    const unsigned e = u >> 23, f = u & 0x7fffffu;
+    if (e == 0) return __uint_as_float((f & (f - 1u)) == 0u ? f : (1u << (32 - __clz(f))));
+    return f == 0u ? s : __uint_as_float((e + 1u) << 23);
+}
+
+// Where block b of receive row r keeps its scale.
+template <bool kColMajor>
+__device__ __forceinline__ int64_t scale_index(const DispatchArgs& a, int64_t r, int b, int nb) {
+    return kColMajor ? static_cast<int64_t>(b) * a.scale_ld + r : r * nb + b;
+}
+
+// kMode: EP_SCALE_FP32 (scale = amax/448), EP_SCALE_POW2 (smallest power of
+// two >= amax/448, stored as fp32) or EP_SCALE_UE8M0 (that power, at least
+// 2^-127, stored as its biased exponent byte).
+template <int kMode, bool kColMajor>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 dispatch_fp8_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
     const int lane = threadIdx.x & 31;
@@ -121,7 +143,9 @@ dispatch_fp8_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
             scale[u] = 0.0f;
             q[u] = make_uint2(0u, 0u);
         } else {
-            const float s = __fdiv_rn(m, 448.0f);
+            float s = __fdiv_rn(m, 448.0f);
+            if (kMode != EP_SCALE_FP32) s = pow2_ceil(s);
+            if (kMode == EP_SCALE_UE8M0) s = fmaxf(s, __uint_as_float(0x00400000u));   // 2^-127
             scale[u] = s;
             unsigned w[4];
 #pragma unroll
@@ -137,13 +161,70 @@ dispatch_fp8_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
         const int r = __shfl_sync(kFullMask, row, k);
         if (r < 0) continue;
         uint2* d = dst + static_cast<int64_t>(r) * H16;
-        float* srow = a.recv_scales + static_cast<int64_t>(r) * nb;
 #pragma unroll
         for (int u = 0; u < kFp8Unroll; ++u) {
             const int g = g0 + u * 32;
             if (g < H16) {
                 __stcs(d + g, q[u]);
-                if ((lane & 15) == 0) __stcs(srow + g / 16, scale[u]);
+                if ((lane & 15) == 0) {
+                    const int64_t si = scale_index<kColMajor>(a, r, g / 16, nb);
+                    if (kMode == EP_SCALE_UE8M0) {
+                        // a power of two >= 2^-127: normal -> exponent field, 2^-127 -> 0
+                        const unsigned bits = __float_as_uint(scale[u]);
+                        static_cast<uint8_t*>(a.recv_scales)[si] = static_cast<uint8_t>(bits >> 23);
+                    } else {
+                        __stcs(static_cast<float*>(a.recv_scales) + si, scale[u]);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// fp8 input pass-through: one warp per (token, column segment) copies the
+// token's e4m3 codes to each of its K rows with 16-byte vectors; the warp of
+// segment 0 also copies the token's scale row (fp32, or bytes in UE8M0 mode)
+// into every receive row's scales, in the requested layout.
+template <bool kColMajor>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+dispatch_fp8_passthrough_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
+    const int lane = threadIdx.x & 31;
+    const int64_t item = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (item >= num_items) return;
+    const int t = static_cast<int>(item / num_segments);
+    const int seg = static_cast<int>(item - static_cast<int64_t>(t) * num_segments);
+    const int V = a.H / 16;                           // 16-byte vectors of codes per row
+    const int nb = a.H / 128;
+    const int row = slot_row(a.row_of_slot, t, a.K, lane);
+    const int4* src = reinterpret_cast<const int4*>(a.x) + static_cast<int64_t>(t) * V;
+    int4* dst = reinterpret_cast<int4*>(a.recv_x);
+    const int j0 = seg * (32 * kBf16Unroll) + lane;
+    int4 v[kBf16Unroll];
+#pragma unroll
+    for (int u = 0; u < kBf16Unroll; ++u) {
+        const int j = j0 + u * 32;
+        if (j < V) v[u] = ld_stream(src + j);
+    }
+    const bool ue = a.scale_mode == EP_SCALE_UE8M0;
+    if (seg == 0) write_side_outputs(a, t, lane, row);
+    for (int k = 0; k < a.K; ++k) {
+        const int r = __shfl_sync(kFullMask, row, k);
+        if (r < 0) continue;
+        int4* d = dst + static_cast<int64_t>(r) * V;
+#pragma unroll
+        for (int u = 0; u < kBf16Unroll; ++u) {
+            const int j = j0 + u * 32;
+            if (j < V) __stcs(d + j, v[u]);
+        }
+        if (seg == 0) {
+            for (int b = lane; b < nb; b += 32) {
+                const int64_t si = scale_index<kColMajor>(a, r, b, nb);
+                if (ue)
+                    static_cast<uint8_t*>(a.recv_scales)[si] =
+                        static_cast<const uint8_t*>(a.x_scales)[static_cast<int64_t>(t) * nb + b];
+                else
+                    static_cast<float*>(a.recv_scales)[si] =
+                        __ldg(static_cast<const float*>(a.x_scales) + static_cast<int64_t>(t) * nb + b);
             }
         }
     }
@@ -152,7 +233,7 @@ dispatch_fp8_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
 // One warp per (expert, pad row): zero a pad row of an aligned layout.
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 fill_pad_rows_kernel(const int32_t* counts, const int32_t* offsets, int E, int max_pad, int64_t row_bytes,
-                     char* recv, float* scales, int nb, int32_t* src, float* weights) {
+                     char* recv, PadScales sc, int32_t* src, float* weights) {
     const int lane = threadIdx.x & 31;
     const int64_t item = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
     const int e = static_cast<int>(item / max_pad);
@@ -162,8 +243,12 @@ fill_pad_rows_kernel(const int32_t* counts, const int32_t* offsets, int E, int m
     if (row >= offsets[e + 1]) return;
     int4* d = reinterpret_cast<int4*>(recv + row * row_bytes);   // row_bytes % 16 == 0
     for (int64_t j = lane; j < row_bytes / 16; j += 32) d[j] = make_int4(0, 0, 0, 0);
-    if (scales)
-        for (int b = lane; b < nb; b += 32) scales[row * nb + b] = 0.0f;
+    if (sc.ptr)
+        for (int b = lane; b < sc.nb; b += 32) {
+            const int64_t si = sc.col_major ? static_cast<int64_t>(b) * sc.ld + row : row * sc.nb + b;
+            if (sc.bytes == 1) static_cast<uint8_t*>(sc.ptr)[si] = 0;
+            else static_cast<float*>(sc.ptr)[si] = 0.0f;
+        }
     if (lane == 0) {
         if (src) src[row] = -1;
         if (weights) weights[row] = 0.0f;
@@ -184,13 +269,27 @@ cudaError_t launch_dispatch_bf16(const DispatchArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_fill_pad_rows(const int32_t* counts, const int32_t* offsets, int E, int64_t row_bytes,
-                                 void* recv, float* scales, int nb, int32_t* src, float* weights,
+                                 void* recv, const PadScales& scales, int32_t* src, float* weights,
                                  cudaStream_t stream, int max_pad) {
     if (E == 0 || max_pad <= 0) return cudaSuccess;
     const int64_t items = static_cast<int64_t>(E) * max_pad;
     const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
     fill_pad_rows_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(
-        counts, offsets, E, max_pad, row_bytes, static_cast<char*>(recv), scales, nb, src, weights);
+        counts, offsets, E, max_pad, row_bytes, static_cast<char*>(recv), scales, src, weights);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_fp8_passthrough(const DispatchArgs& a, cudaStream_t stream) {
+    const int V = a.H / 16;
+    const int per_item = 32 * kBf16Unroll;
+    const int segs = (V + per_item - 1) / per_item;
+    const int64_t items = static_cast<int64_t>(a.T) * segs;
+    if (items == 0) return cudaSuccess;
+    const unsigned g = static_cast<unsigned>((items + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    if (a.scale_col_major)
+        dispatch_fp8_passthrough_kernel<true><<<g, kWarpsPerBlock * 32, 0, stream>>>(a, items, segs);
+    else
+        dispatch_fp8_passthrough_kernel<false><<<g, kWarpsPerBlock * 32, 0, stream>>>(a, items, segs);
     return cudaGetLastError();
 }
 
@@ -201,7 +300,19 @@ cudaError_t launch_dispatch_fp8(const DispatchArgs& a, cudaStream_t stream) {
     const int64_t items = static_cast<int64_t>(a.T) * segs;
     if (items == 0) return cudaSuccess;
     const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    dispatch_fp8_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a, items, segs);
+    const unsigned g = static_cast<unsigned>(blocks);
+    const int tpb = kWarpsPerBlock * 32;
+    const bool col = a.scale_col_major != 0;
+    if (a.scale_mode == EP_SCALE_POW2) {
+        if (col) dispatch_fp8_kernel<EP_SCALE_POW2, true><<<g, tpb, 0, stream>>>(a, items, segs);
+        else dispatch_fp8_kernel<EP_SCALE_POW2, false><<<g, tpb, 0, stream>>>(a, items, segs);
+    } else if (a.scale_mode == EP_SCALE_UE8M0) {
+        if (col) dispatch_fp8_kernel<EP_SCALE_UE8M0, true><<<g, tpb, 0, stream>>>(a, items, segs);
+        else dispatch_fp8_kernel<EP_SCALE_UE8M0, false><<<g, tpb, 0, stream>>>(a, items, segs);
+    } else {
+        if (col) dispatch_fp8_kernel<EP_SCALE_FP32, true><<<g, tpb, 0, stream>>>(a, items, segs);
+        else dispatch_fp8_kernel<EP_SCALE_FP32, false><<<g, tpb, 0, stream>>>(a, items, segs);
+    }
     return cudaGetLastError();
 }
 

@@ -65,22 +65,35 @@ struct DispatchArgs {
     const int32_t* row_of_slot;
     const float* topk_weights; // [T, K] or null
     void* recv_x;
-    float* recv_scales;
+    void* recv_scales;         // fp32, or uint8 exponents in UE8M0 mode
     int32_t* recv_src_token;
     float* recv_weights;
     int64_t recv_capacity;
     int T, K, H;
+    int scale_mode;            // EP_SCALE_FP32 / EP_SCALE_POW2 / EP_SCALE_UE8M0
+    int scale_col_major;       // 0: scales [rows, H/128]; 1: [H/128, scale_ld]
+    int64_t scale_ld;
+    const void* x_scales;      // fp8 input: [T, H/128] fp32 (uint8 in UE8M0 mode)
 };
 
 cudaError_t launch_dispatch_bf16(const DispatchArgs& a, cudaStream_t stream);
 cudaError_t launch_dispatch_fp8(const DispatchArgs& a, cudaStream_t stream);
+// fp8 input: codes [T, H] bytes and scale rows moved unchanged to every slot's row
+cudaError_t launch_dispatch_fp8_passthrough(const DispatchArgs& a, cudaStream_t stream);
 
 // Zero the pad rows of an aligned layout: for each expert e the rows from
 // offsets[e] + counts[e] up to offsets[e+1] (at most max_pad of them) get
-// zero bytes (row_bytes each, a multiple of 16), scale 0 (if scales), source
-// -1 (if src) and weight 0 (if weights).
+// zero bytes (row_bytes each, a multiple of 16), zero scales (if any, in their
+// layout), source -1 (if src) and weight 0 (if weights).
+struct PadScales {
+    void* ptr = nullptr;       // null: no scales
+    int nb = 0;                // blocks per row
+    int bytes = 4;             // 4 (fp32) or 1 (UE8M0)
+    int col_major = 0;
+    int64_t ld = 0;
+};
 cudaError_t launch_fill_pad_rows(const int32_t* counts, const int32_t* offsets, int E, int64_t row_bytes,
-                                 void* recv, float* scales, int nb, int32_t* src, float* weights,
+                                 void* recv, const PadScales& scales, int32_t* src, float* weights,
                                  cudaStream_t stream, int max_pad);
 
 struct CombineArgs {

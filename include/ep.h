@@ -66,6 +66,24 @@ typedef enum {
     EP_DTYPE_FP8_E4M3 = 1      /* receive rows are e4m3 bytes + fp32 scales   */
 } ep_dtype_t;
 
+/* How fp8 block scales are formed and stored (one per 128 channels). */
+typedef enum {
+    EP_SCALE_FP32 = 0,  /* scale = amax / 448 (IEEE fp32 division), stored as fp32        */
+    EP_SCALE_POW2 = 1,  /* smallest power of two >= amax / 448, stored as fp32          */
+    EP_SCALE_UE8M0 = 2  /* that power (at least 2^-127) stored as its biased exponent
+                           byte b, value 2^(b - 127)                                    */
+} ep_scale_mode_t;
+
+/* Options of ep_dispatch_ex; an all-zero struct means bf16 in, bf16 out. */
+typedef struct {
+    int in_dtype;          /* EP_DTYPE_BF16: x is bf16 [T, H]; EP_DTYPE_FP8_E4M3: x is e4m3
+                              codes [T, H] with x_scales, moved unchanged (needs fp8 out) */
+    int out_dtype;         /* EP_DTYPE_BF16 or EP_DTYPE_FP8_E4M3                          */
+    int scale_mode;        /* ep_scale_mode_t for fp8 output (and the x_scales type)      */
+    int scales_col_major;  /* 0: recv_scales [cap, H/128]; 1: [H/128, scales_ld]          */
+    int64_t scales_ld;     /* rows of the column-major scale matrix (>= recv_capacity)    */
+} ep_dispatch_config_t;
+
 /* Opaque routing handle: owns the slot -> row map [T*K] int32, the layout
  * scratch and a small pinned host mirror. Keeps no pointer to topk_idx. */
 typedef struct ep_handle* ep_handle_t;
@@ -180,6 +198,31 @@ EP_API ep_status_t ep_dispatch(ep_handle_t handle, const void* x, int H, ep_dtyp
                         const float* topk_weights,
                         void* recv_x, float* recv_scales, int32_t* recv_src_token,
                         float* recv_weights, int64_t recv_capacity, void* stream);
+
+/*
+ * ep_dispatch_ex -- ep_dispatch with the fp8 options of the pages: power-of-two
+ * and UE8M0 scales (nccl_ep.cc, ncclEpDispatch: round_scales; DeepEP API docs,
+ * "dispatch()": use_ue8m0), a column-major scale layout (DeepEP
+ * "dispatch()": use_tma_aligned_col_major_sf), and fp8 input pass-through
+ * (DeepEP "dispatch()": x as an (fp8 data, scales) tuple; nccl_ep.cc: fp8
+ * tokens with their scales in the high-throughput path).
+ *
+ * With in_dtype = EP_DTYPE_BF16 and fp8 output, each 128-channel block of
+ * token t gets s = amax / 448 and, by scale_mode: FP32 -> scale = s;
+ * POW2 -> the smallest power of two >= s; UE8M0 -> that power raised to at
+ * least 2^-127 and stored as its exponent byte. Codes are
+ * e4m3_rne_satfinite(x / scale). An all-zero block has zero codes and scale 0
+ * (UE8M0 byte 0). With in_dtype = EP_DTYPE_FP8_E4M3, x holds codes [T, H]
+ * (bytes) and x_scales [T, H/128] (fp32, or bytes in UE8M0 mode); both are
+ * copied to every slot's row. recv_scales is fp32 (bytes in UE8M0 mode),
+ * [cap, H/128] row-major or, with scales_col_major, element (row n, block b)
+ * at n + b * scales_ld. Other arguments and errors as ep_dispatch; config may
+ * be NULL (bf16 in and out).
+ */
+EP_API ep_status_t ep_dispatch_ex(ep_handle_t handle, const void* x, const void* x_scales, int H,
+                                  const ep_dispatch_config_t* config, const float* topk_weights,
+                                  void* recv_x, void* recv_scales, int32_t* recv_src_token,
+                                  float* recv_weights, int64_t recv_capacity, void* stream);
 
 /*
  * ep_combine -- weighted top-k gather-reduce back to token order.

@@ -689,3 +689,112 @@ def test_combine_backward_exact_arithmetic(ep):
     _, r_gw = oracle.combine_backward(g, y, ref["row_of_slot"], None, n)
     np.testing.assert_array_equal(gw.cpu().numpy().astype(np.float64), r_gw)
     run.h.destroy()
+
+
+# ------------------------------------------------------------------ fp8 variants
+
+def _layout_dev(ep, inp, A=1):
+    w = inp.w
+    o = [torch.empty(w.E, dtype=torch.int32, device="cuda"), torch.empty(w.R, dtype=torch.int32, device="cuda"),
+         torch.empty(w.T, w.R, dtype=torch.uint8, device="cuda"), torch.empty(w.E + 1, dtype=torch.int32, device="cuda")]
+    return ep.ep_layout_aligned(_dev(inp.topk_idx), w.E, w.R, A, *o)
+
+
+def fp8_variant(ep, inp, mode, col_major=False, A=1):
+    w = inp.w
+    ref = oracle.layout_aligned(inp.topk_idx, w.E, w.R, A)
+    n = int(ref["expert_offsets"][-1])
+    nb = w.H // 128
+    ue = mode == ep.EP_SCALE_UE8M0
+    h = _layout_dev(ep, inp, A)
+    if mode == ep.EP_SCALE_FP32:
+        r_q, r_s, _, _ = oracle.dispatch_e4m3(inp.x, ref["row_of_slot"], n)
+    else:
+        r_q, r_s = oracle.dispatch_e4m3_pow2(inp.x, ref["row_of_slot"], n, ue8m0=ue)
+    if A > 1:
+        oracle.fill_pad_rows(ref, r_q, scales=None if ue else r_s)
+        if ue:   # byte scales of pad rows: 0
+            for e in range(w.E):
+                lo = ref["expert_offsets"][e] + ref["num_tokens_per_expert"][e]
+                r_s[lo:ref["expert_offsets"][e + 1]] = 0
+    ld = (n + 3) // 4 * 4 + 4
+    sdt = torch.uint8 if ue else torch.float32
+    sent = 0xEE if ue else -1.0
+    q = torch.full((max(n, 1), w.H), SENT8, dtype=torch.uint8, device="cuda")
+    sc = torch.full((nb * ld,) if col_major else (max(n, 1), nb), sent, dtype=sdt, device="cuda")
+    ep.ep_dispatch_ex(h, _dev(inp.x.view(np.int16)), q, n, scale_mode=mode, recv_scales=sc,
+                      scales_col_major=col_major, scales_ld=ld if col_major else 0)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(q.cpu().numpy()[:n], r_q)
+    g = sc.cpu().numpy()
+    if col_major:
+        g = g.reshape(nb, ld)
+        got = g[:, :n].T
+        assert (g[:, n:] == sent).all(), "column-major scales written past N"
+    else:
+        got = g[:n]
+    if ue:
+        np.testing.assert_array_equal(got, r_s)
+    else:
+        np.testing.assert_array_equal(got.view(np.uint32), r_s.view(np.uint32))
+    h.destroy()
+
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("decode", None), ("fp8", 1001), ("skewed", 2000)])
+@pytest.mark.parametrize("mode", [1, 2])
+def test_fp8_pow2_and_ue8m0(ep, name, T, mode):
+    fp8_variant(ep, gi.make(name, 7, T=T, with_y=False), mode)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_fp8_col_major_scales(ep, mode):
+    fp8_variant(ep, gi.make("fp8", 8, T=600, with_y=False), mode, col_major=True)
+
+
+@pytest.mark.parametrize("mode,col", [(0, True), (2, False), (1, True)])
+def test_fp8_variants_aligned(ep, mode, col):
+    fp8_variant(ep, gi.make("skewed", 9, T=1500, with_y=False), mode, col_major=col, A=32)
+
+
+def test_fp8_pow2_special_blocks(ep):
+    rng = np.random.default_rng(12)
+    T, H = 40, 1024
+    xf = (rng.standard_normal((T, H)) * 2).astype(np.float32)
+    xf[0, :128] = 0.0
+    xf[1, 128:256] = 1e-39
+    xf[2, 256:384] = 2.0 ** -130
+    xf[3, 384:512] = 3e38
+    xf[4, :] = np.float32(2.0 ** -133)
+    x = gi.f32_to_bf16_bits(xf)
+    idx = np.argsort(rng.random((T, 16)), axis=1)[:, :3].astype(np.int64)
+    inp = gi.Inputs(w=_workload(T, H, 16, 3, 4), seed=0, x=x, topk_idx=idx,
+                    topk_weights=np.full((T, 3), 1 / 3, np.float32), y=None, num_valid=3 * T)
+    for mode in (1, 2):
+        fp8_variant(ep, inp, mode)
+
+
+@pytest.mark.parametrize("ue", [False, True])
+def test_fp8_input_passthrough(ep, ue):
+    inp = gi.make("fp8", 10, T=700, with_y=False)
+    w = inp.w
+    nb = w.H // 128
+    # fp8 tokens and their scales, made by the oracle's quantiser
+    codes = np.zeros((w.T, w.H), np.uint8)
+    scales = np.zeros((w.T, nb), np.uint8 if ue else np.float32)
+    for t in range(w.T):
+        codes[t], scales[t] = oracle.quant_row_e4m3_pow2(inp.x[t], ue8m0=ue)
+    ref = oracle.layout(inp.topk_idx, w.E, w.R)
+    n = int(ref["expert_offsets"][-1])
+    h = _layout_dev(ep, inp)
+    q = torch.full((n, w.H), SENT8, dtype=torch.uint8, device="cuda")
+    sc = torch.full((n, nb), 0xEE if ue else -1.0, dtype=torch.uint8 if ue else torch.float32, device="cuda")
+    src = torch.full((n,), -5, dtype=torch.int32, device="cuda")
+    ep.ep_dispatch_ex(h, _dev(codes), q, n, in_dtype=ep.EP_DTYPE_FP8_E4M3,
+                      scale_mode=ep.EP_SCALE_UE8M0 if ue else ep.EP_SCALE_FP32,
+                      x_scales=_dev(scales), recv_scales=sc, recv_src_token=src, H=w.H)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(q.cpu().numpy(), oracle.dispatch_rows(codes, ref["row_of_slot"], n))
+    np.testing.assert_array_equal(sc.cpu().numpy(), oracle.dispatch_rows(scales, ref["row_of_slot"], n))
+    _, r_src, _ = oracle.dispatch_bf16(inp.x, ref["row_of_slot"], n)
+    np.testing.assert_array_equal(src.cpu().numpy(), r_src)
+    h.destroy()
