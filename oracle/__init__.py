@@ -57,6 +57,10 @@ def _lib():
             L.orc_quant_row_e4m3_pow2.restype = None
             L.orc_dispatch_rows.argtypes = [P, i64, i64, P, i32, P]
             L.orc_dispatch_rows.restype = None
+            L.orc_topk_to_routing_map.argtypes = [P, P, i64, i32, i32, P, P]
+            L.orc_topk_to_routing_map.restype = i32
+            L.orc_routing_map_to_topk.argtypes = [P, P, i64, i32, i32, P, P]
+            L.orc_routing_map_to_topk.restype = i32
             L.orc_combine_backward.argtypes = [P, P, i32, P, i64, i32, P, P, P]
             L.orc_combine_backward.restype = None
             L.orc_dispatch_backward.argtypes = [P, P, i32, P, i64, i32, P, P]
@@ -276,6 +280,28 @@ def dispatch_backward(grad_recv: np.ndarray, grad_recv_weights: np.ndarray | Non
     rw = _c(grad_recv_weights, np.float32) if grad_recv_weights is not None else None
     _lib().orc_dispatch_backward(_p(g), _p(rw), H, _p(rows), T, K, _p(gx), _p(gw))
     return gx, gw
+
+
+def topk_to_routing_map(topk_idx: np.ndarray, topk_weights: np.ndarray | None, E: int):
+    """(routing_map [T, E] u8, probs [T, E] fp32 or None, status)."""
+    idx = _c(topk_idx, np.int64)
+    T, K = idx.shape
+    rm = np.zeros((T, E), np.uint8)
+    pr = np.zeros((T, E), np.float32) if topk_weights is not None else None
+    w = _c(topk_weights, np.float32) if topk_weights is not None else None
+    st = _lib().orc_topk_to_routing_map(_p(idx), _p(w), T, K, E, _p(rm), _p(pr))
+    return rm, pr, int(st)
+
+
+def routing_map_to_topk(routing_map: np.ndarray, probs: np.ndarray | None, K: int):
+    """(topk_idx [T, K] int64, topk_weights [T, K] fp32, status)."""
+    rm = _c(routing_map, np.uint8)
+    T, E = rm.shape
+    idx = np.zeros((T, K), np.int64)
+    w = np.zeros((T, K), np.float32)
+    pr = _c(probs, np.float32) if probs is not None else None
+    st = _lib().orc_routing_map_to_topk(_p(rm), _p(pr), T, E, K, _p(idx), _p(w))
+    return idx, w, int(st)
 
 
 def f32_to_bf16(a: np.ndarray) -> np.ndarray:

@@ -440,3 +440,60 @@ void orc_dispatch_rows(const uint8_t* src, int64_t T, int64_t row_bytes, const i
             if (row >= 0) memcpy(recv + (int64_t)row * row_bytes, src + t * row_bytes, (size_t)row_bytes);
         }
 }
+
+/* ---------------------------------------------------------------- dense maps */
+
+/* Sparse top-k routing -> dense routing map and probabilities (nccl_ep.cc,
+ * ncclEpCreateHandle: convert_topk_to_routing_map; ncclEpDispatch:
+ * sparse_to_dense_prob; NeMo fused_a2a HybridEPDispatch: routing_map [T, E]
+ * bool with probs [T, E]):
+ *   routing_map[t, e] = 1 if some slot of t names e, else 0
+ *   probs[t, e]       = sum over those slots, ascending k, of w[t, k] (fp32), else 0
+ * Ids outside [0, E) are skipped. Returns ORC_ERR_EXPERT if any id lies
+ * outside [-1, E). */
+int orc_topk_to_routing_map(const int64_t* topk_idx, const float* w, int64_t T, int K, int E,
+                            uint8_t* routing_map, float* probs) {
+    int status = ORC_OK;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int e = 0; e < E; ++e) {
+            routing_map[t * E + e] = 0;
+            if (probs) probs[t * E + e] = 0.0f;
+        }
+        for (int k = 0; k < K; ++k) {
+            int64_t e = topk_idx[t * K + k];
+            if (e == -1) continue;
+            if (e < -1 || e >= E) { status = ORC_ERR_EXPERT; continue; }
+            routing_map[t * E + e] = 1;
+            if (probs && w) probs[t * E + e] += w[t * K + k];
+        }
+    }
+    return status;
+}
+
+/* Dense routing map -> sparse top-k (nccl_ep.cc: dense_to_sparse_prob): the
+ * experts of token t with routing_map[t, e] != 0, in ascending e, fill slots
+ * 0, 1, ...; the remaining slots are -1 with weight 0; topk_weights take
+ * probs[t, e] (or 1 if probs is NULL). Returns ORC_ERR_ARG (and keeps the
+ * first K experts) if a token has more than K experts. */
+int orc_routing_map_to_topk(const uint8_t* routing_map, const float* probs, int64_t T, int E, int K,
+                            int64_t* topk_idx, float* topk_weights) {
+    int status = ORC_OK;
+    for (int64_t t = 0; t < T; ++t) {
+        int k = 0;
+        for (int e = 0; e < E; ++e) {
+            if (!routing_map[t * E + e]) continue;
+            if (k < K) {
+                topk_idx[t * K + k] = e;
+                if (topk_weights) topk_weights[t * K + k] = probs ? probs[t * E + e] : 1.0f;
+            } else {
+                status = ORC_ERR_ARG;
+            }
+            ++k;
+        }
+        for (; k < K; ++k) {
+            topk_idx[t * K + k] = -1;
+            if (topk_weights) topk_weights[t * K + k] = 0.0f;
+        }
+    }
+    return status;
+}

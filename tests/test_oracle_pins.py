@@ -490,3 +490,55 @@ def test_dispatch_rows_moves_any_row_type():
     out = oracle.dispatch_rows(src, L["row_of_slot"], N)
     for t, k in zip(*np.nonzero(L["row_of_slot"] >= 0)):
         np.testing.assert_array_equal(out[L["row_of_slot"][t, k]], src[t])
+
+
+# ------------------------------------------------------------------ dense routing maps
+
+def test_routing_map_golden(golden):
+    g = golden("routing_map_hand.txt")
+    T, K, E = (int(g[k][0]) for k in "TKE")
+    idx = _ints(g["topk_idx"]).reshape(T, K)
+    w = np.array([float(v) for v in g["topk_weights"]], np.float32).reshape(T, K)
+    rm, pr, st = oracle.topk_to_routing_map(idx, w, E)
+    assert st == oracle.OK
+    np.testing.assert_array_equal(rm.ravel(), _ints(g["routing_map"]))
+    np.testing.assert_array_equal(pr.ravel(), np.array([float(v) for v in g["probs"]], np.float32))
+    bi, bw, st = oracle.routing_map_to_topk(rm, pr, K)
+    assert st == oracle.OK
+    np.testing.assert_array_equal(bi.ravel(), _ints(g["back_topk_idx"]))
+    np.testing.assert_array_equal(bw.ravel(), np.array([float(v) for v in g["back_topk_weights"]], np.float32))
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_routing_map_round_trip_vs_numpy(seed):
+    inp = gi.make("skewed", seed, T=500, with_y=False)
+    w_ = inp.w
+    rm, pr, st = oracle.topk_to_routing_map(inp.topk_idx, inp.topk_weights, w_.E)
+    # numpy: scatter the valid slots
+    want = np.zeros((w_.T, w_.E), np.uint8)
+    want_p = np.zeros((w_.T, w_.E), np.float32)
+    t, k = np.nonzero(inp.topk_idx >= 0)
+    want[t, inp.topk_idx[t, k]] = 1
+    want_p[t, inp.topk_idx[t, k]] = inp.topk_weights[t, k]
+    np.testing.assert_array_equal(rm, want)
+    np.testing.assert_array_equal(pr, want_p)
+    # back to sparse: each token's experts sorted ascending, weights follow
+    bi, bw, st = oracle.routing_map_to_topk(rm, pr, w_.K)
+    for tt in range(w_.T):
+        valid = inp.topk_idx[tt] >= 0
+        order = np.argsort(inp.topk_idx[tt][valid])
+        n = int(valid.sum())
+        np.testing.assert_array_equal(bi[tt, :n], inp.topk_idx[tt][valid][order])
+        np.testing.assert_array_equal(bw[tt, :n], inp.topk_weights[tt][valid][order])
+        assert (bi[tt, n:] == -1).all() and (bw[tt, n:] == 0).all()
+    # the layout of the converted routing differs only in slot order inside tokens
+    a = oracle.layout(inp.topk_idx, w_.E, w_.R)
+    b = oracle.layout(bi, w_.E, w_.R)
+    for key in ["num_tokens_per_expert", "num_tokens_per_rank", "is_token_in_rank", "expert_offsets"]:
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_routing_map_too_many_experts():
+    rm = np.ones((2, 8), np.uint8)
+    _, _, st = oracle.routing_map_to_topk(rm, None, 4)
+    assert st == oracle.ERR_ARG
