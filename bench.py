@@ -339,6 +339,29 @@ def gpu_arm(args, rank, world, local):
     b_cbw = 2 * T * H + 4 * N * H + 4 * T * K * 3
     b_dbw = bytes_combine(T, K, H, N) + 4 * T * K + 4 * N + 4 * T * K
 
+    # dense routing map <-> sparse top-k conversions on the prefill routing
+    with torch.cuda.stream(stream):
+        rmap = torch.empty(T, E, dtype=torch.uint8, device=dev)
+        probs = torch.empty(T, E, dtype=torch.float32, device=dev)
+        idx_back = torch.empty(T, K, dtype=torch.int64, device=dev)
+        w_back = torch.empty(T, K, dtype=torch.float32, device=dev)
+    ev_c = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps_b)]
+    for i in range(-3, reps_b):
+        if i >= 0:
+            ev_c[i][0].record(stream)
+        ep.ep_topk_to_routing_map(idx, E, rmap, topk_weights=wt, probs=probs, stream=stream)
+        if i >= 0:
+            ev_c[i][1].record(stream)
+        ep.ep_routing_map_to_topk(rmap, K, idx_back, probs=probs, topk_weights=w_back, stream=stream)
+        if i >= 0:
+            ev_c[i][2].record(stream)
+    stream.synchronize()
+    ms_t2m = float(np.mean([e[0].elapsed_time(e[1]) for e in ev_c]))
+    ms_m2t = float(np.mean([e[1].elapsed_time(e[2]) for e in ev_c]))
+    b_t2m = 12 * T * K + 5 * T * E
+    b_m2t = 5 * T * E + 12 * T * K
+    del rmap, probs, idx_back, w_back
+
     # aligned layout (expert rows start on multiples of 128) + bf16 dispatch
     # including the pad rows' zero fill, on the prefill routing
     A = 128
@@ -425,6 +448,10 @@ def gpu_arm(args, rank, world, local):
             "dispatch_fp8_passthrough": {"us": round(ms_pass * 1e3, 2), "bytes": b_pass,
                                          "gbs": round(b_pass / (ms_pass * 1e-3) / 1e9, 1),
                                          "frac_of_measured": round(b_pass / (ms_pass * 1e-3) / 1e9 / peak, 4)},
+            "topk_to_routing_map": {"us": round(ms_t2m * 1e3, 2), "bytes": b_t2m,
+                                    "gbs": round(b_t2m / (ms_t2m * 1e-3) / 1e9, 1)},
+            "routing_map_to_topk": {"us": round(ms_m2t * 1e3, 2), "bytes": b_m2t,
+                                    "gbs": round(b_m2t / (ms_m2t * 1e-3) / 1e9, 1)},
             "combine_backward": {"us": round(ms_cbw * 1e3, 2), "bytes": b_cbw,
                                  "gbs": round(b_cbw / (ms_cbw * 1e-3) / 1e9, 1),
                                  "frac_of_measured": round(b_cbw / (ms_cbw * 1e-3) / 1e9 / peak, 4)},

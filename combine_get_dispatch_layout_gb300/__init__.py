@@ -27,7 +27,7 @@ class DispatchConfig(ctypes.Structure):
 
 # Exported symbols declared in include/ep.h.
 EXPORTS = ("ep_layout", "ep_layout_aligned", "ep_dispatch", "ep_dispatch_ex", "ep_combine", "ep_combine_backward",
-           "ep_dispatch_backward", "ep_handle_query",
+           "ep_dispatch_backward", "ep_topk_to_routing_map", "ep_routing_map_to_topk", "ep_handle_query",
            "ep_handle_copy_row_of_slot", "ep_handle_destroy", "ep_handle_layout_kernels",
            "ep_layout_noalloc", "ep_status_string")
 
@@ -54,6 +54,8 @@ def lib() -> ctypes.CDLL:
         L.ep_dispatch.argtypes = [P, P, i32, i32, P, P, P, P, P, i64, P]
         L.ep_dispatch_ex.argtypes = [P, P, P, i32, ctypes.POINTER(DispatchConfig), P, P, P, P, P, i64, P]
         L.ep_combine.argtypes = [P, P, i64, i32, P, P, P]
+        L.ep_topk_to_routing_map.argtypes = [P, P, i32, i32, i32, P, P, P, P]
+        L.ep_routing_map_to_topk.argtypes = [P, P, i32, i32, i32, P, P, P, P]
         L.ep_combine_backward.argtypes = [P, P, P, i64, i32, P, P, i64, P, P]
         L.ep_dispatch_backward.argtypes = [P, P, i64, i32, P, P, P, P]
         L.ep_handle_query.argtypes = [P, ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_int32)]
@@ -204,6 +206,24 @@ def ep_dispatch_backward(handle: Handle, grad_recv, grad_x, grad_recv_weights=No
     st = lib().ep_dispatch_backward(handle.ptr, _ptr(grad_recv), rows, H, _ptr(grad_recv_weights), _ptr(grad_x),
                                     _ptr(grad_topk_weights), _stream(stream))
     _check(st, "ep_dispatch_backward")
+
+
+def ep_topk_to_routing_map(topk_idx, num_experts: int, routing_map, topk_weights=None, probs=None,
+                           device_error=None, stream=None) -> None:
+    """routing_map [T, E] u8 (and probs [T, E] fp32) from topk_idx [T, K]."""
+    T, K = topk_idx.shape
+    st = lib().ep_topk_to_routing_map(_ptr(topk_idx), _ptr(topk_weights), T, K, num_experts, _ptr(routing_map),
+                                      _ptr(probs), _ptr(device_error), _stream(stream))
+    _check(st, "ep_topk_to_routing_map")
+
+
+def ep_routing_map_to_topk(routing_map, num_topk: int, topk_idx, probs=None, topk_weights=None,
+                           device_error=None, stream=None) -> None:
+    """topk_idx [T, K] int64 (and weights) from routing_map [T, E], experts ascending."""
+    T, E = routing_map.shape
+    st = lib().ep_routing_map_to_topk(_ptr(routing_map), _ptr(probs), T, E, num_topk, _ptr(topk_idx),
+                                      _ptr(topk_weights), _ptr(device_error), _stream(stream))
+    _check(st, "ep_routing_map_to_topk")
 
 
 def ep_handle_query(handle: Handle) -> tuple[int, int]:

@@ -397,6 +397,33 @@ ep_status_t ep_dispatch_backward(ep_handle_t handle, const void* grad_recv, int6
                : EP_ERR_CUDA;
 }
 
+ep_status_t ep_topk_to_routing_map(const int64_t* topk_idx, const float* topk_weights, int T, int K, int E,
+                                   uint8_t* routing_map, float* probs, int32_t* device_error, void* stream) {
+    if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS) return EP_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !routing_map)) return EP_ERR_INVALID_ARG;
+    if (probs && !topk_weights) return EP_ERR_INVALID_ARG;
+    if (!aligned(topk_idx, 8) || !aligned(topk_weights, 4) || !aligned(probs, 4) || !aligned(device_error, 4))
+        return EP_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t err = device_error ? cudaMemsetAsync(device_error, 0, sizeof(int32_t), s) : cudaSuccess;
+    if (err == cudaSuccess)
+        err = ep::launch_topk_to_routing_map(topk_idx, topk_weights, T, K, E, routing_map, probs, device_error, s);
+    return err == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+ep_status_t ep_routing_map_to_topk(const uint8_t* routing_map, const float* probs, int T, int E, int K,
+                                   int64_t* topk_idx, float* topk_weights, int32_t* device_error, void* stream) {
+    if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS) return EP_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !routing_map)) return EP_ERR_INVALID_ARG;
+    if (!aligned(topk_idx, 8) || !aligned(topk_weights, 4) || !aligned(probs, 4) || !aligned(device_error, 4))
+        return EP_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t err = device_error ? cudaMemsetAsync(device_error, 0, sizeof(int32_t), s) : cudaSuccess;
+    if (err == cudaSuccess)
+        err = ep::launch_routing_map_to_topk(routing_map, probs, T, E, K, topk_idx, topk_weights, device_error, s);
+    return err == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
 ep_status_t ep_handle_query(ep_handle_t handle, int64_t* num_recv_rows, int32_t* device_error) {
     if (!handle) return EP_ERR_INVALID_ARG;
     ep_status_t st = current_device_is(handle);

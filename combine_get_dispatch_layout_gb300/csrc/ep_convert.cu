@@ -1,0 +1,105 @@
+// Conversions between sparse top-k routing (topk_idx / topk_weights [T, K])
+// and a dense routing map with probabilities (routing_map / probs [T, E]).
+//
+// nccl_ep.cc converts top-k indices to a per-token routing map
+// (convert_topk_to_routing_map) and probabilities between the two forms
+// (sparse_to_dense_prob, dense_to_sparse_prob); NeMo fused_a2a's
+// HybridEPDispatch takes routing_map [T, E] bool and probs [T, E]. Reading:
+// the dense-to-sparse direction lists a token's experts in ascending id, and
+// a dense probability is the fp32 sum, in ascending k, of the weights of the
+// slots naming that expert.
+//
+// GPU design: one warp per token. topk -> map: lane k holds slot k, every
+// lane owns experts lane, lane + 32, ... and tests them against the K
+// broadcast slots, so the byte and fp32 rows are written coalesced.
+// map -> topk: each 32-expert chunk is one ballot; a set bit's slot is the
+// count of set bits before it.
+#include "ep_internal.cuh"
+
+namespace ep {
+
+namespace {
+
+constexpr int kConvWarps = 8;
+
+__global__ void __launch_bounds__(kConvWarps * 32)
+topk_to_routing_map_kernel(const int64_t* topk_idx, const float* w, int T, int K, int E, uint8_t* routing_map,
+                           float* probs, int32_t* device_error) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kConvWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int64_t my_e = -1;
+    float my_w = 0.0f;
+    if (lane < K) {
+        my_e = topk_idx[static_cast<int64_t>(t) * K + lane];
+        if (w) my_w = w[static_cast<int64_t>(t) * K + lane];
+    }
+    const bool bad = my_e < -1 || my_e >= E;
+    if (__any_sync(kFullMask, bad) && lane == 0 && device_error) atomicExch(device_error, EP_ERR_INVALID_EXPERT);
+    const int key = (my_e >= 0 && my_e < E) ? static_cast<int>(my_e) : -1;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        uint8_t hit = 0;
+        float p = 0.0f;
+        for (int k = 0; k < K; ++k) {
+            const int ek = __shfl_sync(kFullMask, key, k);
+            const float wk = __shfl_sync(kFullMask, my_w, k);
+            if (ek == e) {
+                hit = 1;
+                p = p + wk;
+            }
+        }
+        if (e < E) {
+            routing_map[static_cast<int64_t>(t) * E + e] = hit;
+            if (probs) probs[static_cast<int64_t>(t) * E + e] = p;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kConvWarps * 32)
+routing_map_to_topk_kernel(const uint8_t* routing_map, const float* probs, int T, int E, int K, int64_t* topk_idx,
+                           float* topk_weights, int32_t* device_error) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kConvWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const unsigned lt = (1u << lane) - 1u;
+    int base = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        const bool on = e < E && routing_map[static_cast<int64_t>(t) * E + e] != 0;
+        const unsigned m = __ballot_sync(kFullMask, on);
+        const int pos = base + __popc(m & lt);
+        if (on && pos < K) {
+            topk_idx[static_cast<int64_t>(t) * K + pos] = e;
+            if (topk_weights) topk_weights[static_cast<int64_t>(t) * K + pos] = probs ? probs[static_cast<int64_t>(t) * E + e] : 1.0f;
+        }
+        base += __popc(m);
+    }
+    for (int k = base + lane; k < K; k += 32) {
+        topk_idx[static_cast<int64_t>(t) * K + k] = -1;
+        if (topk_weights) topk_weights[static_cast<int64_t>(t) * K + k] = 0.0f;
+    }
+    if (base > K && lane == 0 && device_error) atomicExch(device_error, EP_ERR_CAPACITY);
+}
+
+}  // namespace
+
+cudaError_t launch_topk_to_routing_map(const int64_t* topk_idx, const float* w, int T, int K, int E,
+                                       uint8_t* routing_map, float* probs, int32_t* device_error,
+                                       cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    topk_to_routing_map_kernel<<<(T + kConvWarps - 1) / kConvWarps, kConvWarps * 32, 0, stream>>>(
+        topk_idx, w, T, K, E, routing_map, probs, device_error);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_routing_map_to_topk(const uint8_t* routing_map, const float* probs, int T, int E, int K,
+                                       int64_t* topk_idx, float* topk_weights, int32_t* device_error,
+                                       cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    routing_map_to_topk_kernel<<<(T + kConvWarps - 1) / kConvWarps, kConvWarps * 32, 0, stream>>>(
+        routing_map, probs, T, E, K, topk_idx, topk_weights, device_error);
+    return cudaGetLastError();
+}
+
+}  // namespace ep

@@ -121,6 +121,11 @@ cudaError_t launch_combine_backward(const CombineBackwardArgs& a, cudaStream_t s
 cudaError_t launch_gather_slot_weights(const int32_t* row_of_slot, const float* row_weights, float* slot_weights,
                                        int64_t slots, cudaStream_t stream);
 
-int device_sm_count();
+cudaError_t launch_topk_to_routing_map(const int64_t* topk_idx, const float* w, int T, int K, int E,
+                                       uint8_t* routing_map, float* probs, int32_t* device_error,
+                                       cudaStream_t stream);
+cudaError_t launch_routing_map_to_topk(const uint8_t* routing_map, const float* probs, int T, int E, int K,
+                                       int64_t* topk_idx, float* topk_weights, int32_t* device_error,
+                                       cudaStream_t stream);
 
 }  // namespace ep

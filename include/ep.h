@@ -272,6 +272,33 @@ EP_API ep_status_t ep_dispatch_backward(ep_handle_t handle, const void* grad_rec
                                         void* stream);
 
 /*
+ * ep_topk_to_routing_map -- sparse top-k routing to a dense routing map
+ * (nccl_ep.cc: convert_topk_to_routing_map and sparse_to_dense_prob; NeMo
+ * fused_a2a, HybridEPDispatch: routing_map [T, E] and probs [T, E]).
+ *   routing_map[t, e] = 1 if some slot of token t names expert e, else 0
+ *   probs[t, e]       = fp32 sum in ascending k of those slots' weights, else 0
+ * topk_idx int64 [T, K] (-1 = unused), topk_weights fp32 [T, K] (needed for
+ * probs), routing_map uint8 [T, E], probs fp32 [T, E] or NULL. Every element
+ * of the outputs is written. device_error (int32 [1] or NULL) is set to 0, or
+ * EP_ERR_INVALID_EXPERT if an id outside [-1, E) was seen (and skipped).
+ */
+EP_API ep_status_t ep_topk_to_routing_map(const int64_t* topk_idx, const float* topk_weights, int T, int K,
+                                          int E, uint8_t* routing_map, float* probs, int32_t* device_error,
+                                          void* stream);
+
+/*
+ * ep_routing_map_to_topk -- dense routing map to sparse top-k (nccl_ep.cc:
+ * dense_to_sparse_prob). The experts e with routing_map[t, e] != 0, in
+ * ascending e, fill slots 0, 1, ... of token t; the rest are -1 with weight 0.
+ * topk_weights takes probs[t, e] (1 if probs is NULL). device_error (int32
+ * [1] or NULL) is set to 0, or EP_ERR_CAPACITY if a token has more than K
+ * experts (the first K are kept). The result feeds ep_layout directly.
+ */
+EP_API ep_status_t ep_routing_map_to_topk(const uint8_t* routing_map, const float* probs, int T, int E, int K,
+                                          int64_t* topk_idx, float* topk_weights, int32_t* device_error,
+                                          void* stream);
+
+/*
  * ep_handle_query -- synchronous read of the handle's device state after the
  * last ep_layout: N (number of valid slots = receive rows) and the device
  * error word (0, or EP_ERR_INVALID_EXPERT). Synchronises the layout stream.

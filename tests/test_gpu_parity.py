@@ -798,3 +798,50 @@ def test_fp8_input_passthrough(ep, ue):
     _, r_src, _ = oracle.dispatch_bf16(inp.x, ref["row_of_slot"], n)
     np.testing.assert_array_equal(src.cpu().numpy(), r_src)
     h.destroy()
+
+
+# ------------------------------------------------------------------ dense routing maps
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("skewed", 3000), ("prefill", 2048)])
+def test_routing_map_conversions(ep, name, T):
+    inp = gi.make(name, 13, T=T, with_y=False)
+    w = inp.w
+    r_map, r_probs, st = oracle.topk_to_routing_map(inp.topk_idx, inp.topk_weights, w.E)
+    rm = torch.full((w.T, w.E), SENT8, dtype=torch.uint8, device="cuda")
+    pr = torch.full((w.T, w.E), -1.0, dtype=torch.float32, device="cuda")
+    err = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    ep.ep_topk_to_routing_map(_dev(inp.topk_idx), w.E, rm, topk_weights=_dev(inp.topk_weights), probs=pr,
+                              device_error=err)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(rm.cpu().numpy(), r_map)
+    np.testing.assert_array_equal(pr.cpu().numpy().view(np.uint32), r_probs.view(np.uint32))
+    assert err.item() == 0
+    r_idx, r_w, _ = oracle.routing_map_to_topk(r_map, r_probs, w.K)
+    idx = torch.full((w.T, w.K), -9, dtype=torch.int64, device="cuda")
+    wt = torch.full((w.T, w.K), -1.0, dtype=torch.float32, device="cuda")
+    ep.ep_routing_map_to_topk(rm, w.K, idx, probs=pr, topk_weights=wt, device_error=err)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(idx.cpu().numpy(), r_idx)
+    np.testing.assert_array_equal(wt.cpu().numpy().view(np.uint32), r_w.view(np.uint32))
+    assert err.item() == 0
+    # the converted routing runs the whole path like any other
+    inp2 = gi.Inputs(w=w, seed=0, x=inp.x, topk_idx=r_idx, topk_weights=r_w,
+                     y=gi.normal_bf16(np.random.SeedSequence(14), int((r_idx >= 0).sum()), w.H)
+                     if w.y != "identity" else None, num_valid=int((r_idx >= 0).sum()))
+    full_path(ep, inp2, fp8=(w.H % 128 == 0))
+
+
+def test_routing_map_errors(ep):
+    idx = torch.tensor([[0, 9], [1, -3]], dtype=torch.int64, device="cuda")
+    rm = torch.empty((2, 8), dtype=torch.uint8, device="cuda")
+    err = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    ep.ep_topk_to_routing_map(idx, 8, rm, device_error=err)
+    torch.cuda.synchronize()
+    assert err.item() == ep.EP_ERR_INVALID_EXPERT
+    assert rm.cpu().numpy().tolist() == [[1, 0, 0, 0, 0, 0, 0, 0], [0, 1, 0, 0, 0, 0, 0, 0]]
+    full = torch.ones((3, 40), dtype=torch.uint8, device="cuda")
+    out = torch.empty((3, 4), dtype=torch.int64, device="cuda")
+    ep.ep_routing_map_to_topk(full, 4, out, device_error=err)
+    torch.cuda.synchronize()
+    assert err.item() == ep.EP_ERR_CAPACITY
+    assert out.cpu().numpy().tolist() == [[0, 1, 2, 3]] * 3
