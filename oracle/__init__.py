@@ -23,7 +23,7 @@ _SO = os.path.join(_HERE, "liboracle.so")
 _LIB = None
 _LOCK = threading.Lock()
 
-OK, ERR_ARG, ERR_EXPERT = 0, 1, 2
+OK, ERR_ARG, ERR_EXPERT, ERR_CAPACITY = 0, 1, 2, 3
 
 
 def build(force: bool = False) -> str:
@@ -49,6 +49,8 @@ def _lib():
             L.orc_layout.restype = i32
             L.orc_layout_aligned.argtypes = [P, i64, i32, i32, i32, i32, P, P, P, P, P]
             L.orc_layout_aligned.restype = i32
+            L.orc_layout_strided.argtypes = [P, i64, i32, i32, i32, i32, P, P, P, P, P]
+            L.orc_layout_strided.restype = i32
             L.orc_fill_pad_rows.argtypes = [P, P, i32, i64, P, P, i32, P, P]
             L.orc_fill_pad_rows.restype = None
             L.orc_pow2_ceil.argtypes = [ctypes.c_float]
@@ -124,6 +126,24 @@ def layout_aligned(topk_idx: np.ndarray, E: int, R: int, alignment: int) -> dict
         row_of_slot=np.zeros((T, K), np.int32),
     )
     st = _lib().orc_layout_aligned(_p(idx), T, K, E, R, alignment, _p(out["num_tokens_per_expert"]),
+                                   _p(out["num_tokens_per_rank"]), _p(out["is_token_in_rank"]),
+                                   _p(out["expert_offsets"]), _p(out["row_of_slot"]))
+    out["status"] = int(st)
+    return out
+
+
+def layout_strided(topk_idx: np.ndarray, E: int, R: int, cap: int) -> dict:
+    """Layout with expert e's rows at e * cap + 0, 1, ... (slots past cap dropped)."""
+    idx = _c(topk_idx, np.int64)
+    T, K = idx.shape
+    out = dict(
+        num_tokens_per_expert=np.zeros(E, np.int32),
+        num_tokens_per_rank=np.zeros(R, np.int32),
+        is_token_in_rank=np.zeros((T, R), np.uint8),
+        expert_offsets=np.zeros(E + 1, np.int32),
+        row_of_slot=np.zeros((T, K), np.int32),
+    )
+    st = _lib().orc_layout_strided(_p(idx), T, K, E, R, cap, _p(out["num_tokens_per_expert"]),
                                    _p(out["num_tokens_per_rank"]), _p(out["is_token_in_rank"]),
                                    _p(out["expert_offsets"]), _p(out["row_of_slot"]))
     out["status"] = int(st)

@@ -55,6 +55,22 @@ def layout_aligned(topk_idx: np.ndarray, E: int, R: int, A: int) -> dict:
     return out
 
 
+def layout_strided(topk_idx: np.ndarray, E: int, R: int, cap: int) -> dict:
+    """Strided layout from the sorted order: rank inside the expert, then e * cap."""
+    base = layout(topk_idx, E, R)
+    idx = np.asarray(topk_idx, np.int64)
+    rows = base["row_of_slot"].astype(np.int64)
+    valid = rows >= 0
+    e = np.where(valid, idx, 0)
+    rank_in_expert = rows - base["expert_offsets"][e]
+    keep = valid & (rank_in_expert < cap)
+    out = dict(base)
+    out["expert_offsets"] = (np.arange(E + 1) * cap).astype(np.int32)
+    out["row_of_slot"] = np.where(keep, e * cap + rank_in_expert, -1).astype(np.int32)
+    out["status"] = 3 if (valid & ~keep).any() else base["status"]
+    return out
+
+
 def e4m3_values() -> tuple[np.ndarray, np.ndarray]:
     """(codes, values) of the 254 finite OCP E4M3 codes, decoded from their bits."""
     codes, vals = [], []

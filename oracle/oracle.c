@@ -497,3 +497,41 @@ int orc_routing_map_to_topk(const uint8_t* routing_map, const float* probs, int6
     }
     return status;
 }
+
+/* ---------------------------------------------------------------- strided layout */
+
+#define ORC_ERR_CAPACITY 3
+
+/* Routing layout with a fixed row stride per expert: the padded 3-D receive
+ * buffer [E, cap, H] of nccl_ep.cc's low-latency dispatch (recv_x
+ * [num_local_experts, num_ranks * max_tokens_per_rank, hidden] with
+ * per-expert receive counts). expert_offsets[e] = e * cap,
+ * expert_offsets[E] = E * cap; expert e's slots take rows e * cap + 0, 1, ...
+ * in (t, k) order. A slot whose rank inside its expert reaches cap is dropped
+ * (row -1) and the call returns ORC_ERR_CAPACITY; the counts stay the full
+ * counts. Rows past an expert's count are not part of the layout. */
+int orc_layout_strided(const int64_t* topk_idx, int64_t T, int K, int E, int R, int cap,
+                       int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                       uint8_t* is_token_in_rank, int32_t* expert_offsets, int32_t* row_of_slot) {
+    if (cap < 1) return ORC_ERR_ARG;
+    int32_t* packed = (int32_t*)malloc(sizeof(int32_t) * (size_t)(E + 1));
+    if (!packed) return ORC_ERR_ARG;
+    int status = orc_layout(topk_idx, T, K, E, R, num_tokens_per_expert, num_tokens_per_rank,
+                            is_token_in_rank, packed, row_of_slot);
+    if (status == ORC_ERR_ARG) { free(packed); return status; }
+    if ((int64_t)E * cap > INT32_MAX) { free(packed); return ORC_ERR_ARG; }
+    for (int e = 0; e <= E; ++e) expert_offsets[e] = e * cap;
+    for (int64_t s = 0; s < T * (int64_t)K; ++s) {
+        if (row_of_slot[s] < 0) continue;
+        int64_t e = topk_idx[s];
+        int32_t rank_in_expert = row_of_slot[s] - packed[e];
+        if (rank_in_expert >= cap) {
+            row_of_slot[s] = -1;
+            if (status == ORC_OK) status = ORC_ERR_CAPACITY;
+        } else {
+            row_of_slot[s] = (int32_t)(e * cap) + rank_in_expert;
+        }
+    }
+    free(packed);
+    return status;
+}

@@ -542,3 +542,32 @@ def test_routing_map_too_many_experts():
     rm = np.ones((2, 8), np.uint8)
     _, _, st = oracle.routing_map_to_topk(rm, None, 4)
     assert st == oracle.ERR_ARG
+
+
+# ------------------------------------------------------------------ strided layout
+
+def test_layout_strided_golden(golden):
+    g = golden("layout_hand_strided.txt")
+    T, K, E, R, C = (int(g[k][0]) for k in "TKERC")
+    idx = _ints(g["topk_idx"]).reshape(T, K)
+    L = oracle.layout_strided(idx, E, R, C)
+    assert L["status"] == oracle.OK
+    np.testing.assert_array_equal(L["num_tokens_per_expert"], _ints(g["num_tokens_per_expert"]))
+    np.testing.assert_array_equal(L["expert_offsets"], _ints(g["expert_offsets"]))
+    np.testing.assert_array_equal(L["row_of_slot"].ravel(), _ints(g["row_of_slot"]))
+
+
+@pytest.mark.parametrize("cap", [1, 2, 5, 64, 1000])
+@pytest.mark.parametrize("case", CORNERS[:8])
+def test_layout_strided_vs_brute(case, cap):
+    T, K, E, R, drop_p, distinct, bad_p = case
+    idx = _random_routing(np.random.default_rng(cap), T, K, E, drop_p, distinct, bad_p)
+    a = oracle.layout_strided(idx, E, R, cap)
+    b = brute.layout_strided(idx, E, R, cap)
+    for key in ["num_tokens_per_expert", "num_tokens_per_rank", "is_token_in_rank", "expert_offsets",
+                "row_of_slot", "status"]:
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    r = a["row_of_slot"]
+    kept = r[r >= 0]
+    assert len(np.unique(kept)) == len(kept)                      # no row used twice
+    assert ((kept // cap) == idx[r >= 0]).all()                   # each row inside its expert's block
