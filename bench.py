@@ -388,6 +388,41 @@ def gpu_arm(args, rank, world, local):
     h_a.destroy()
     del recv_a
 
+    # decode shape through the low-latency padded 3-D layout [E, cap, H]
+    # (cap = T: every token could pick one expert); ~33 MB, L2-resident
+    dec = gi.make("decode", seed=args.seed + rank)
+    wd = dec.w
+    cap = wd.T
+    with torch.cuda.stream(stream):
+        d_idx = torch.from_numpy(dec.topk_idx).to(dev)
+        d_x = torch.from_numpy(dec.x.view(np.int16)).to(dev)
+        d_w = torch.from_numpy(dec.topk_weights).to(dev)
+        d_y = torch.randn(wd.E * cap, wd.H, device=dev).to(torch.bfloat16).view(torch.int16)
+        d_recv = torch.empty(wd.E * cap, wd.H, dtype=torch.int16, device=dev)
+        d_out = torch.empty(wd.T, wd.H, dtype=torch.int16, device=dev)
+        d_cnt = torch.empty(wd.E, dtype=torch.int32, device=dev)
+        d_ntr = torch.empty(wd.R, dtype=torch.int32, device=dev)
+        d_itr = torch.empty(wd.T, wd.R, dtype=torch.uint8, device=dev)
+        d_off = torch.empty(wd.E + 1, dtype=torch.int32, device=dev)
+    h_d = ep.ep_layout_strided(d_idx, wd.E, wd.R, cap, d_cnt, d_ntr, d_itr, d_off, stream=stream)
+    ev_d = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps_b)]
+    for i in range(-3, reps_b):
+        if i >= 0:
+            ev_d[i][0].record(stream)
+        ep.ep_layout_strided(d_idx, wd.E, wd.R, cap, d_cnt, d_ntr, d_itr, d_off, handle=h_d, stream=stream)
+        if i >= 0:
+            ev_d[i][1].record(stream)
+        ep.ep_dispatch(h_d, d_x, ep.EP_DTYPE_BF16, d_recv, wd.E * cap, stream=stream)
+        if i >= 0:
+            ev_d[i][2].record(stream)
+        ep.ep_combine(h_d, d_y, d_out, topk_weights=d_w, stream=stream)
+        if i >= 0:
+            ev_d[i][3].record(stream)
+    stream.synchronize()
+    ms_d = [float(np.mean([e[j].elapsed_time(e[j + 1]) for e in ev_d])) for j in range(3)]
+    h_d.destroy()
+    del d_y, d_recv
+
     # end to end through the public API with pinned host buffers
     e2e = e2e_measure(torch, ep, dev, inp, args, stream)
     e2e["ms_per_step"], _ = aggregate_over_ranks(e2e["ms_per_step"], 0, device=dev)
@@ -452,6 +487,11 @@ def gpu_arm(args, rank, world, local):
                                     "gbs": round(b_t2m / (ms_t2m * 1e-3) / 1e9, 1)},
             "routing_map_to_topk": {"us": round(ms_m2t * 1e3, 2), "bytes": b_m2t,
                                     "gbs": round(b_m2t / (ms_m2t * 1e-3) / 1e9, 1)},
+            "decode_ll_step": {"workload": "decode T=256 H=7168 E=256 K=8 R=8, strided layout cap=256, "
+                                           "L2-resident (33 MB), warm",
+                               "layout_strided_us": round(ms_d[0] * 1e3, 2),
+                               "dispatch_us": round(ms_d[1] * 1e3, 2), "combine_us": round(ms_d[2] * 1e3, 2),
+                               "tokens_per_s": round(wd.T / (sum(ms_d) * 1e-3), 1)},
             "combine_backward": {"us": round(ms_cbw * 1e3, 2), "bytes": b_cbw,
                                  "gbs": round(b_cbw / (ms_cbw * 1e-3) / 1e9, 1),
                                  "frac_of_measured": round(b_cbw / (ms_cbw * 1e-3) / 1e9 / peak, 4)},

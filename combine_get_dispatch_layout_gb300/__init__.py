@@ -26,7 +26,7 @@ class DispatchConfig(ctypes.Structure):
                 ("scales_col_major", ctypes.c_int), ("scales_ld", ctypes.c_int64)]
 
 # Exported symbols declared in include/ep.h.
-EXPORTS = ("ep_layout", "ep_layout_aligned", "ep_dispatch", "ep_dispatch_ex", "ep_combine", "ep_combine_backward",
+EXPORTS = ("ep_layout", "ep_layout_aligned", "ep_layout_strided", "ep_dispatch", "ep_dispatch_ex", "ep_combine", "ep_combine_backward",
            "ep_dispatch_backward", "ep_topk_to_routing_map", "ep_routing_map_to_topk", "ep_handle_query",
            "ep_handle_copy_row_of_slot", "ep_handle_destroy", "ep_handle_layout_kernels",
            "ep_layout_noalloc", "ep_status_string")
@@ -51,6 +51,7 @@ def lib() -> ctypes.CDLL:
         P, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
         L.ep_layout.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, ctypes.POINTER(P), P]
         L.ep_layout_aligned.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, P, P, ctypes.POINTER(P), P]
+        L.ep_layout_strided.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, P, P, ctypes.POINTER(P), P]
         L.ep_dispatch.argtypes = [P, P, i32, i32, P, P, P, P, P, i64, P]
         L.ep_dispatch_ex.argtypes = [P, P, P, i32, ctypes.POINTER(DispatchConfig), P, P, P, P, P, i64, P]
         L.ep_combine.argtypes = [P, P, i64, i32, P, P, P]
@@ -155,6 +156,20 @@ def ep_layout_aligned(topk_idx, num_experts: int, num_ranks: int, expert_alignme
     return h
 
 
+def ep_layout_strided(topk_idx, num_experts: int, num_ranks: int, expert_capacity: int,
+                      num_tokens_per_expert, num_tokens_per_rank, is_token_in_rank, expert_offsets,
+                      handle: Handle | None = None, stream=None, alloc_fn=None, free_fn=None) -> Handle:
+    """ep_layout into the padded 3-D receive buffer [E, expert_capacity, H]."""
+    T, K = topk_idx.shape
+    h = handle if handle is not None else Handle()
+    st = lib().ep_layout_strided(_ptr(topk_idx), T, K, num_experts, num_ranks, int(expert_capacity),
+                                 _ptr(num_tokens_per_expert), _ptr(num_tokens_per_rank), _ptr(is_token_in_rank),
+                                 _ptr(expert_offsets), _fnptr(alloc_fn), _fnptr(free_fn), ctypes.byref(h.ptr),
+                                 _stream(stream))
+    _check(st, "ep_layout_strided")
+    return h
+
+
 def ep_dispatch(handle: Handle, x, out_dtype: int, recv_x, recv_capacity: int, recv_scales=None,
                 recv_src_token=None, recv_weights=None, topk_weights=None, stream=None) -> None:
     """Permute x [T, H] bf16 into recv_x (bf16 [cap, H] or uint8 [cap, H] for fp8)."""
@@ -231,7 +246,7 @@ def ep_handle_query(handle: Handle) -> tuple[int, int]:
     n = ctypes.c_int64(0)
     err = ctypes.c_int32(0)
     st = lib().ep_handle_query(handle.ptr, ctypes.byref(n), ctypes.byref(err))
-    if st not in (EP_OK, EP_ERR_INVALID_EXPERT):
+    if st not in (EP_OK, EP_ERR_INVALID_EXPERT, EP_ERR_CAPACITY):
         _check(st, "ep_handle_query")
     return n.value, err.value
 

@@ -20,6 +20,7 @@ struct ep_handle {
     // routing of the last ep_layout
     int T = 0, K = 0, E = 0, R = 0;
     int align = 1;              // expert row alignment of the last layout
+    int stride = 0;             // > 0: fixed rows per expert (strided layout)
     ep::LayoutPlan plan{};
     cudaStream_t layout_stream = nullptr;
     bool error_latched = false;
@@ -102,12 +103,15 @@ ep_status_t read_meta(ep_handle* h, int64_t* rows, int32_t* err) {
     if (cudaStreamSynchronize(h->layout_stream) != cudaSuccess) return EP_ERR_CUDA;
     if (rows) *rows = h->host_meta[ep::kMetaRows];
     if (err) *err = h->host_meta[ep::kMetaError];
-    if (h->host_meta[ep::kMetaError] != 0) h->error_latched = true;
+    // an invalid expert id blocks later calls; a strided overflow only drops slots
+    if (h->host_meta[ep::kMetaError] == EP_ERR_INVALID_EXPERT) h->error_latched = true;
     return EP_OK;
 }
 
-// Most receive rows a routing can need: every slot valid, every expert padded.
-int64_t max_rows_of(int T, int K, int E, int align) {
+// Most receive rows a routing can need: every slot valid, every expert padded;
+// a strided layout always spans E * stride rows.
+int64_t max_rows_of(int T, int K, int E, int align, int stride = 0) {
+    if (stride > 0) return static_cast<int64_t>(E) * stride;
     return static_cast<int64_t>(T) * K + static_cast<int64_t>(E) * (align - 1);
 }
 
@@ -115,13 +119,14 @@ int64_t max_rows_of(int T, int K, int E, int align) {
 // buffer holds the most a routing can produce.
 ep_status_t check_rows(ep_handle* h, int64_t capacity) {
     if (h->error_latched) return EP_ERR_INVALID_EXPERT;
-    const int64_t max_rows = max_rows_of(h->T, h->K, h->E, h->align);
+    const int64_t max_rows = max_rows_of(h->T, h->K, h->E, h->align, h->stride);
     if (capacity >= max_rows) return EP_OK;
+    if (h->stride > 0) return EP_ERR_CAPACITY;   // a strided buffer must span E * stride rows
     int64_t n = 0;
     int32_t err = 0;
     ep_status_t st = read_meta(h, &n, &err);
     if (st != EP_OK) return st;
-    if (err != 0) return EP_ERR_INVALID_EXPERT;
+    if (err == EP_ERR_INVALID_EXPERT) return EP_ERR_INVALID_EXPERT;
     return n > capacity ? EP_ERR_CAPACITY : EP_OK;
 }
 
@@ -129,7 +134,7 @@ ep_status_t check_rows(ep_handle* h, int64_t capacity) {
 
 namespace {
 
-ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int align,
+ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int align, int stride,
                         int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
                         uint8_t* is_token_in_rank, int32_t* expert_offsets,
                         ep_alloc_fn alloc_fn, ep_free_fn free_fn,
@@ -139,8 +144,9 @@ ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int
     if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS || R < 1 || R > EP_MAX_RANKS ||
         E % R != 0)
         return EP_ERR_INVALID_ARG;
-    if (align < 1 || align > EP_MAX_ALIGNMENT) return EP_ERR_INVALID_ARG;
+    if (align < 1 || align > EP_MAX_ALIGNMENT || stride < 0 || (stride > 0 && align != 1)) return EP_ERR_INVALID_ARG;
     if (max_rows_of(T, K, E, align) >= (int64_t{1} << 31)) return EP_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(E) * stride >= (int64_t{1} << 31)) return EP_ERR_INVALID_ARG;
     if (T > 0 && (!topk_idx || !is_token_in_rank)) return EP_ERR_INVALID_ARG;
     if ((alloc_fn == nullptr) != (free_fn == nullptr)) return EP_ERR_INVALID_ARG;
     if (!aligned(topk_idx, 8) || !aligned(num_tokens_per_expert, 4) || !aligned(num_tokens_per_rank, 4) ||
@@ -169,6 +175,7 @@ ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int
 
     ep::LayoutPlan plan = ep::make_layout_plan(T, K, E, R);
     plan.align = align;
+    plan.stride = stride;
     ep_status_t st = ensure_block(h, static_cast<int64_t>(T) * K,
                                   static_cast<int64_t>(E) * plan.num_chunks,
                                   static_cast<int64_t>(R) * plan.num_blocks, E, s);
@@ -184,6 +191,7 @@ ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int
     }
     h->T = T; h->K = K; h->E = E; h->R = R;
     h->align = align;
+    h->stride = stride;
     h->plan = plan;
     h->layout_stream = s;
     h->error_latched = false;
@@ -224,7 +232,7 @@ ep_status_t ep_layout(const int64_t* topk_idx, int T, int K, int E, int R,
                       uint8_t* is_token_in_rank, int32_t* expert_offsets,
                       ep_alloc_fn alloc_fn, ep_free_fn free_fn,
                       ep_handle_t* handle, void* stream) {
-    return layout_impl(topk_idx, T, K, E, R, 1, num_tokens_per_expert, num_tokens_per_rank, is_token_in_rank,
+    return layout_impl(topk_idx, T, K, E, R, 1, 0, num_tokens_per_expert, num_tokens_per_rank, is_token_in_rank,
                        expert_offsets, alloc_fn, free_fn, handle, stream);
 }
 
@@ -233,7 +241,17 @@ ep_status_t ep_layout_aligned(const int64_t* topk_idx, int T, int K, int E, int 
                               uint8_t* is_token_in_rank, int32_t* expert_offsets,
                               ep_alloc_fn alloc_fn, ep_free_fn free_fn,
                               ep_handle_t* handle, void* stream) {
-    return layout_impl(topk_idx, T, K, E, R, expert_alignment, num_tokens_per_expert, num_tokens_per_rank,
+    return layout_impl(topk_idx, T, K, E, R, expert_alignment, 0, num_tokens_per_expert, num_tokens_per_rank,
+                       is_token_in_rank, expert_offsets, alloc_fn, free_fn, handle, stream);
+}
+
+ep_status_t ep_layout_strided(const int64_t* topk_idx, int T, int K, int E, int R, int expert_capacity,
+                              int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                              uint8_t* is_token_in_rank, int32_t* expert_offsets,
+                              ep_alloc_fn alloc_fn, ep_free_fn free_fn,
+                              ep_handle_t* handle, void* stream) {
+    if (expert_capacity < 1) return EP_ERR_INVALID_ARG;
+    return layout_impl(topk_idx, T, K, E, R, 1, expert_capacity, num_tokens_per_expert, num_tokens_per_rank,
                        is_token_in_rank, expert_offsets, alloc_fn, free_fn, handle, stream);
 }
 
@@ -434,7 +452,7 @@ ep_status_t ep_handle_query(ep_handle_t handle, int64_t* num_recv_rows, int32_t*
     if (st != EP_OK) return st;
     if (num_recv_rows) *num_recv_rows = n;
     if (device_error) *device_error = err;
-    return err != 0 ? EP_ERR_INVALID_EXPERT : EP_OK;
+    return err != 0 ? static_cast<ep_status_t>(err) : EP_OK;
 }
 
 ep_status_t ep_handle_copy_row_of_slot(ep_handle_t handle, int32_t* dst, void* stream) {

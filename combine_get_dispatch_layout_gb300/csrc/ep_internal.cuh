@@ -24,6 +24,7 @@ struct LayoutPlan {
     int T, K, E, R, L;
     int key_bits;            // bits of (expert id + 1)
     int align;               // expert row alignment (1 = packed)
+    int stride;              // > 0: expert e's rows start at e * stride (fixed capacity)
     int chunk_tokens;
     int num_chunks;
     int warps_per_block;

@@ -245,13 +245,26 @@ layout_assign_kernel(LayoutPlan p, LayoutArgs a) {
     int* warp_tmp = smem + p.E;                        // [33]
     int* run = smem + p.E + 33 + warp * p.E;           // this warp's running rows
     // every block rebuilds the E offsets from the totals (E <= 4096 values)
+    __shared__ int s_over;
+    if (threadIdx.x == 0) s_over = 0;
+    __syncthreads();
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
         const int c = a.num_tokens_per_expert[e];
-        offs[e] = round_up_to(c, p.align);
+        offs[e] = p.stride > 0 ? c : round_up_to(c, p.align);
+        if (p.stride > 0 && c > p.stride) s_over = 1;
         if (blockIdx.x == 0 && a.h_counts) a.h_counts[e] = c;
     }
     __syncthreads();
-    const int n_rows = block_exclusive_scan(offs, p.E, warp_tmp);
+    int n_rows = block_exclusive_scan(offs, p.E, warp_tmp);
+    if (p.stride > 0) {
+        // fixed stride: expert e's block starts at e * stride
+        for (int e = threadIdx.x; e < p.E; e += blockDim.x) offs[e] = e * p.stride;
+        n_rows = p.E * p.stride;
+        __syncthreads();
+        // the scan kernel wrote the invalid-id word; a capacity overflow adds to it
+        if (blockIdx.x == 0 && threadIdx.x == 0 && s_over && a.meta[kMetaError] == 0)
+            a.meta[kMetaError] = EP_ERR_CAPACITY;
+    }
     if (blockIdx.x == 0) {
         for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
             a.expert_offsets[e] = offs[e];
@@ -288,7 +301,10 @@ layout_assign_kernel(LayoutPlan p, LayoutArgs a) {
             const int key = slot_key(e_r[j], p.E, bad);
             const unsigned peers = peer_mask(key, p.key_bits);
             int row = -1;
-            if (key >= 0) row = run[key] + __popc(peers & lt);
+            if (key >= 0) {
+                row = run[key] + __popc(peers & lt);
+                if (p.stride > 0 && row - key * p.stride >= p.stride) row = -1;   // past the expert's capacity
+            }
             __syncwarp();
             if (key >= 0 && lane == __ffs(peers) - 1) run[key] += __popc(peers);
             __syncwarp();
@@ -335,6 +351,7 @@ __device__ __forceinline__ unsigned rank_of(unsigned e, const LayoutPlan& p) {
 __global__ void __launch_bounds__(1024, 1)
 layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
     extern __shared__ int smem[];
+    __shared__ int s_over;
     cg::cluster_group cluster = cg::this_cluster();
     const int cta = static_cast<int>(cluster.block_rank());
     const int C = p.cl_ctas, W = p.cl_warps, E = p.E, R = p.R, ct = p.cl_chunk_tokens;
@@ -356,7 +373,10 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
     for (int e = lane; e < E; e += 32) mine[e] = 0;
     if (small_r)
         for (int i = lane; i < ct; i += 32) my_mask[i] = 0u;
-    if (threadIdx.x == 0) all_bad[cta] = 0;   // own entry only: peers write their own
+    if (threadIdx.x == 0) {
+        all_bad[cta] = 0;   // own entry only: peers write their own
+        s_over = 0;
+    }
     __syncthreads();
 
     // ---- phase 1: stable local ranks, the warp's histogram, token rank masks
@@ -493,26 +513,32 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
             total += v;
         }
         cta_base[e] = below;
-        offs[e] = round_up_to(total, p.align);
+        offs[e] = p.stride > 0 ? e * p.stride : round_up_to(total, p.align);
+        if (p.stride > 0 && total > p.stride) s_over = 1;
         if (cta == 0) {
             a.num_tokens_per_expert[e] = total;
             if (a.h_counts) a.h_counts[e] = total;
         }
     }
-    if (cta == 0) {
+    if (cta == 0)
         for (int r = threadIdx.x; r < R; r += blockDim.x) {
             int total = 0;
             for (int c = 0; c < C; ++c) total += all_rank[c * R + r];
             a.num_tokens_per_rank[r] = total;
         }
-        if (threadIdx.x == 0) {
-            int bad = 0;
-            for (int c = 0; c < C; ++c) bad |= all_bad[c];
-            a.meta[kMetaError] = bad ? EP_ERR_INVALID_EXPERT : 0;
-        }
-    }
     __syncthreads();
-    if (warp == 0) {
+    if (cta == 0 && threadIdx.x == 0) {
+        int bad = 0;
+        for (int c = 0; c < C; ++c) bad |= all_bad[c];
+        a.meta[kMetaError] = bad ? EP_ERR_INVALID_EXPERT : (s_over ? EP_ERR_CAPACITY : 0);
+    }
+    if (p.stride > 0) {
+        if (cta == 0 && threadIdx.x == 0) {
+            a.expert_offsets[E] = E * p.stride;
+            if (a.h_offsets) a.h_offsets[E] = E * p.stride;
+            a.meta[kMetaRows] = E * p.stride;
+        }
+    } else if (warp == 0) {
         const int n_rows = warp_exclusive_scan(offs, E, lane);
         if (cta == 0 && lane == 0) {
             a.expert_offsets[E] = n_rows;
@@ -534,7 +560,11 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
         if (j >= nr) break;
         const int64_t s = s0 + j * 32 + lane;
         const int key = key_r[j];
-        const int row = key >= 0 ? offs[key] + cta_base[key] + mine[key] + loc_r[j] : -1;
+        int row = -1;
+        if (key >= 0) {
+            const int local = cta_base[key] + mine[key] + loc_r[j];   // rank inside the expert
+            row = (p.stride > 0 && local >= p.stride) ? -1 : offs[key] + local;
+        }
         if (s < s1) a.row_of_slot[s] = row;
     }
 }
@@ -545,6 +575,7 @@ LayoutPlan make_layout_plan(int T, int K, int E, int R) {
     LayoutPlan p{};
     p.T = T; p.K = K; p.E = E; p.R = R; p.L = E / R;
     p.align = 1;
+    p.stride = 0;
     p.key_bits = 1;
     while ((1 << p.key_bits) < E + 1) ++p.key_bits;   // keys -1..E-1 shift to 0..E
     // About 256 warp-chunks: enough parallelism for a latency-bound pass while

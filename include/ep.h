@@ -168,6 +168,27 @@ EP_API ep_status_t ep_layout_aligned(const int64_t* topk_idx, int T, int K, int 
                                      ep_handle_t* handle, void* stream);
 
 /*
+ * ep_layout_strided -- ep_layout for the padded 3-D receive buffer of the
+ * low-latency path (nccl_ep.cc, ncclEpDispatch low-latency branch: recv_x
+ * [num_local_experts, num_ranks * max_tokens_per_rank, hidden] with
+ * per-expert receive counts): expert e owns the fixed row block
+ * [e * expert_capacity, (e + 1) * expert_capacity), its slots taking the first
+ * rows in (token, k) order; num_tokens_per_expert says how many are valid.
+ * expert_offsets[e] = e * expert_capacity and expert_offsets[E] = E *
+ * expert_capacity, the rows every receive / expert-output buffer must hold.
+ * Rows past an expert's count are never written. Reading: a slot whose rank
+ * inside its expert reaches the capacity is dropped (row -1, skipped by
+ * dispatch and combine) and ep_handle_query then returns EP_ERR_CAPACITY;
+ * later calls on the handle still run. E * expert_capacity < 2^31.
+ */
+EP_API ep_status_t ep_layout_strided(const int64_t* topk_idx, int T, int K, int E, int R,
+                                     int expert_capacity,
+                                     int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                                     uint8_t* is_token_in_rank, int32_t* expert_offsets,
+                                     ep_alloc_fn alloc_fn, ep_free_fn free_fn,
+                                     ep_handle_t* handle, void* stream);
+
+/*
  * ep_dispatch -- stable expert-major permute of the token rows.
  *
  * For every valid slot (t, k) with receive row n = row_of_slot[t, k]:
@@ -300,10 +321,12 @@ EP_API ep_status_t ep_routing_map_to_topk(const uint8_t* routing_map, const floa
 
 /*
  * ep_handle_query -- synchronous read of the handle's device state after the
- * last ep_layout: N (number of valid slots = receive rows) and the device
- * error word (0, or EP_ERR_INVALID_EXPERT). Synchronises the layout stream.
- * Returns EP_ERR_INVALID_EXPERT if the error word is set (outputs still
- * filled). Either output pointer may be NULL.
+ * last layout call: N (receive rows: valid slots, the padded total after
+ * ep_layout_aligned, E * capacity after ep_layout_strided) and the device
+ * error word (0, EP_ERR_INVALID_EXPERT, or EP_ERR_CAPACITY when a strided
+ * layout dropped slots). Synchronises the layout stream. Returns the error
+ * word's code if it is set (outputs still filled). Either output pointer may
+ * be NULL.
  */
 EP_API ep_status_t ep_handle_query(ep_handle_t handle, int64_t* num_recv_rows, int32_t* device_error);
 

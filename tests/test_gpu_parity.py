@@ -845,3 +845,63 @@ def test_routing_map_errors(ep):
     torch.cuda.synchronize()
     assert err.item() == ep.EP_ERR_CAPACITY
     assert out.cpu().numpy().tolist() == [[0, 1, 2, 3]] * 3
+
+
+# ------------------------------------------------------------------ strided (padded 3-D) layout
+
+def strided_path(ep, inp, cap):
+    w = inp.w
+    T, K, E, R, H = w.T, w.K, w.E, w.R, w.H
+    ref = oracle.layout_strided(inp.topk_idx, E, R, cap)
+    rows_total = E * cap
+    o = [torch.full((E,), -7, dtype=torch.int32, device="cuda"), torch.full((R,), -7, dtype=torch.int32, device="cuda"),
+         torch.full((T, R), SENT8, dtype=torch.uint8, device="cuda"),
+         torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")]
+    h = ep.ep_layout_strided(_dev(inp.topk_idx), E, R, cap, *o)
+    rows = torch.full((T, K), -9, dtype=torch.int32, device="cuda")
+    ep.ep_handle_copy_row_of_slot(h, rows)
+    torch.cuda.synchronize()
+    for got, key in zip(o, ["num_tokens_per_expert", "num_tokens_per_rank", "is_token_in_rank", "expert_offsets"]):
+        np.testing.assert_array_equal(got.cpu().numpy(), ref[key], err_msg=key)
+    np.testing.assert_array_equal(rows.cpu().numpy(), ref["row_of_slot"])
+    n, err = ep.ep_handle_query(h)
+    assert n == rows_total
+    assert err == (ep.EP_ERR_CAPACITY if ref["status"] == oracle.ERR_CAPACITY else 0)
+    # dispatch into [E, cap, H]: valid rows get their token, the rest keep the sentinel
+    recv = torch.full((rows_total, H), SENT16, dtype=torch.int16, device="cuda")
+    ep.ep_dispatch(h, _dev(inp.x.view(np.int16)), ep.EP_DTYPE_BF16, recv, rows_total)
+    torch.cuda.synchronize()
+    want = np.full((rows_total, H), SENT16, np.uint16)
+    r_x, _, _ = oracle.dispatch_bf16(inp.x, ref["row_of_slot"], rows_total)
+    used = np.zeros(rows_total, bool)
+    used[ref["row_of_slot"][ref["row_of_slot"] >= 0]] = True
+    want[used] = r_x[used]
+    np.testing.assert_array_equal(recv.cpu().numpy().view(np.uint16), want)
+    # combine over [E, cap, H] expert outputs skips dropped slots like the oracle
+    y = gi.normal_bf16(np.random.SeedSequence(cap), rows_total, H)
+    out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    ep.ep_combine(h, _dev(y.view(np.int16)), out, topk_weights=_dev(inp.topk_weights))
+    torch.cuda.synchronize()
+    assert_combine(out.cpu().numpy().view(np.uint16), oracle.combine(y, ref["row_of_slot"], inp.topk_weights))
+    # a buffer smaller than E * cap rows is refused
+    with pytest.raises(ep.EPError) as e:
+        ep.ep_dispatch(h, _dev(inp.x.view(np.int16)), ep.EP_DTYPE_BF16, recv, rows_total - 1)
+    assert e.value.status == ep.EP_ERR_CAPACITY
+    h.destroy()
+
+
+def test_strided_decode(ep):
+    strided_path(ep, gi.make("decode", 3, with_y=False), 32)
+
+
+def test_strided_overflow_drops_slots(ep):
+    strided_path(ep, gi.make("skewed", 3, T=2000, with_y=False), 100)
+
+
+def test_strided_multiblock_path(ep):
+    w = _workload(40000, 64, 64, 8, 4, routing="zipf", drop_p=0.05)
+    strided_path(ep, gi.make(w, 4, with_y=False), 9000)
+
+
+def test_strided_tiny_capacity(ep):
+    strided_path(ep, gi.make("tiny", 4, with_y=False), 1)
