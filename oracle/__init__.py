@@ -51,6 +51,10 @@ def _lib():
             L.orc_layout_aligned.restype = i32
             L.orc_layout_strided.argtypes = [P, i64, i32, i32, i32, i32, P, P, P, P, P]
             L.orc_layout_strided.restype = i32
+            L.orc_layout_nonexpand.argtypes = [P, i64, i32, i32, i32, P, P, P, P, P]
+            L.orc_layout_nonexpand.restype = i32
+            L.orc_nonexpand_recv_topk.argtypes = [P, P, P, i64, i32, i32, i32, P, P]
+            L.orc_nonexpand_recv_topk.restype = None
             L.orc_fill_pad_rows.argtypes = [P, P, i32, i64, P, P, i32, P, P]
             L.orc_fill_pad_rows.restype = None
             L.orc_pow2_ceil.argtypes = [ctypes.c_float]
@@ -148,6 +152,37 @@ def layout_strided(topk_idx: np.ndarray, E: int, R: int, cap: int) -> dict:
                                    _p(out["expert_offsets"]), _p(out["row_of_slot"]))
     out["status"] = int(st)
     return out
+
+
+def layout_nonexpand(topk_idx: np.ndarray, E: int, R: int) -> dict:
+    """One row per (token, rank); rank_offsets in place of expert_offsets."""
+    idx = _c(topk_idx, np.int64)
+    T, K = idx.shape
+    out = dict(
+        num_tokens_per_expert=np.zeros(E, np.int32),
+        num_tokens_per_rank=np.zeros(R, np.int32),
+        is_token_in_rank=np.zeros((T, R), np.uint8),
+        rank_offsets=np.zeros(R + 1, np.int32),
+        row_of_slot=np.zeros((T, K), np.int32),
+    )
+    st = _lib().orc_layout_nonexpand(_p(idx), T, K, E, R, _p(out["num_tokens_per_expert"]),
+                                     _p(out["num_tokens_per_rank"]), _p(out["is_token_in_rank"]),
+                                     _p(out["rank_offsets"]), _p(out["row_of_slot"]))
+    out["status"] = int(st)
+    return out
+
+
+def nonexpand_recv_topk(topk_idx: np.ndarray, topk_weights: np.ndarray | None, row_of_slot: np.ndarray,
+                        E: int, R: int, num_rows: int):
+    """(recv_topk_idx [rows, K] int64 rank-local ids or -1, recv_topk_weights [rows, K])."""
+    idx = _c(topk_idx, np.int64)
+    rows = _c(row_of_slot, np.int32)
+    T, K = idx.shape
+    ri = np.full((num_rows, K), -9, np.int64)
+    rw = np.full((num_rows, K), np.nan, np.float32)
+    w = _c(topk_weights, np.float32) if topk_weights is not None else None
+    _lib().orc_nonexpand_recv_topk(_p(idx), _p(w), _p(rows), T, K, E, R, _p(ri), _p(rw))
+    return ri, rw
 
 
 def fill_pad_rows(layout: dict, recv: np.ndarray, scales=None, src=None, weights=None) -> None:

@@ -71,6 +71,32 @@ def layout_strided(topk_idx: np.ndarray, E: int, R: int, cap: int) -> dict:
     return out
 
 
+def layout_nonexpand(topk_idx: np.ndarray, E: int, R: int) -> dict:
+    """Non-expand layout from the unique (token, rank) pairs sorted by (rank, token)."""
+    idx = np.asarray(topk_idx, np.int64)
+    T, K = idx.shape
+    L = E // R
+    base = layout(idx, E, R)
+    valid = (idx >= 0) & (idx < E)
+    rank = np.where(valid, idx // L, -1)
+    rows = np.full((T, K), -1, np.int64)
+    pairs = sorted({(int(r), t) for t in range(T) for r in rank[t] if r >= 0})
+    row_of_pair = {p: i for i, p in enumerate(pairs)}
+    for t in range(T):
+        seen = set()
+        for k in range(K):
+            r = int(rank[t, k])
+            if r < 0 or r in seen:
+                continue
+            seen.add(r)
+            rows[t, k] = row_of_pair[(r, t)]
+    per_rank = base["num_tokens_per_rank"]
+    return dict(num_tokens_per_expert=base["num_tokens_per_expert"], num_tokens_per_rank=per_rank,
+                is_token_in_rank=base["is_token_in_rank"],
+                rank_offsets=np.concatenate([[0], np.cumsum(per_rank)]).astype(np.int32),
+                row_of_slot=rows.astype(np.int32), status=base["status"])
+
+
 def e4m3_values() -> tuple[np.ndarray, np.ndarray]:
     """(codes, values) of the 254 finite OCP E4M3 codes, decoded from their bits."""
     codes, vals = [], []

@@ -535,3 +535,72 @@ int orc_layout_strided(const int64_t* topk_idx, int64_t T, int K, int E, int R, 
     free(packed);
     return status;
 }
+
+/* ---------------------------------------------------------------- non-expand */
+
+/* Non-expand layout: one receive row per (token, rank) pair (DeepEP API
+ * docs, "Prefix Sum Interpretation for Expert Token Counts", non-expand mode;
+ * nccl_ep.cc, struct ncclEpHandle: sparse_to_dense_map [tokens, ranks] with -1
+ * for "not routed"). Rows are grouped by rank, tokens ascending inside a rank:
+ *   rank_offsets[R + 1] = exclusive prefix sum of num_tokens_per_rank
+ *   row_of_slot[t, k]   = the row of (t, rank(e)) for the FIRST slot of token
+ *                         t on that rank (lowest k), -1 for its other slots on
+ *                         the same rank and for unused slots.
+ * num_tokens_per_expert, num_tokens_per_rank and is_token_in_rank are those of
+ * orc_layout. */
+int orc_layout_nonexpand(const int64_t* topk_idx, int64_t T, int K, int E, int R,
+                         int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                         uint8_t* is_token_in_rank, int32_t* rank_offsets, int32_t* row_of_slot) {
+    int32_t* expert_offsets = (int32_t*)malloc(sizeof(int32_t) * (size_t)(E + 1));
+    if (!expert_offsets) return ORC_ERR_ARG;
+    int status = orc_layout(topk_idx, T, K, E, R, num_tokens_per_expert, num_tokens_per_rank,
+                            is_token_in_rank, expert_offsets, row_of_slot);
+    free(expert_offsets);
+    if (status == ORC_ERR_ARG) return status;
+    int L = E / R;
+    int64_t run = 0;
+    for (int r = 0; r < R; ++r) { rank_offsets[r] = (int32_t)run; run += num_tokens_per_rank[r]; }
+    rank_offsets[R] = (int32_t)run;
+    int64_t* next = (int64_t*)malloc(sizeof(int64_t) * (size_t)R);
+    if (!next) return ORC_ERR_ARG;
+    for (int r = 0; r < R; ++r) next[r] = rank_offsets[r];
+    for (int64_t t = 0; t < T; ++t) {
+        for (int k = 0; k < K; ++k) {
+            int64_t e = topk_idx[t * K + k];
+            row_of_slot[t * K + k] = -1;
+            if (e < 0 || e >= E) continue;
+            int64_t r = e / L;
+            int first = 1;
+            for (int j = 0; j < k; ++j) {
+                int64_t ej = topk_idx[t * K + j];
+                if (ej >= 0 && ej < E && ej / L == r) { first = 0; break; }
+            }
+            if (first) row_of_slot[t * K + k] = (int32_t)next[r]++;
+        }
+    }
+    free(next);
+    return status;
+}
+
+/* What each non-expand receive row carries for its rank's experts (DeepEP API
+ * docs, "dispatch()": recv_topk_idx / recv_topk_weights): for the row of
+ * (t, r), entry k is the rank-local expert id e - r * (E/R) if slot k of t
+ * names an expert of rank r, else -1 (weight w[t, k], else 0). */
+void orc_nonexpand_recv_topk(const int64_t* topk_idx, const float* w, const int32_t* row_of_slot,
+                             int64_t T, int K, int E, int R, int64_t* recv_topk_idx,
+                             float* recv_topk_weights) {
+    int L = E / R;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int k = 0; k < K; ++k) {
+            int32_t row = row_of_slot[t * K + k];
+            if (row < 0) continue;
+            int64_t r = topk_idx[t * K + k] / L;
+            for (int j = 0; j < K; ++j) {
+                int64_t ej = topk_idx[t * K + j];
+                int on = ej >= 0 && ej < E && ej / L == r;
+                recv_topk_idx[(int64_t)row * K + j] = on ? ej - r * L : -1;
+                if (recv_topk_weights) recv_topk_weights[(int64_t)row * K + j] = on && w ? w[t * K + j] : 0.0f;
+            }
+        }
+    }
+}

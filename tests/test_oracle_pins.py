@@ -571,3 +571,35 @@ def test_layout_strided_vs_brute(case, cap):
     kept = r[r >= 0]
     assert len(np.unique(kept)) == len(kept)                      # no row used twice
     assert ((kept // cap) == idx[r >= 0]).all()                   # each row inside its expert's block
+
+
+# ------------------------------------------------------------------ non-expand layout
+
+def test_layout_nonexpand_golden(golden):
+    g = golden("layout_hand_nonexpand.txt")
+    T, K, E, R = (int(g[k][0]) for k in "TKER")
+    idx = _ints(g["topk_idx"]).reshape(T, K)
+    L = oracle.layout_nonexpand(idx, E, R)
+    assert L["status"] == oracle.OK
+    np.testing.assert_array_equal(L["num_tokens_per_rank"], _ints(g["num_tokens_per_rank"]))
+    np.testing.assert_array_equal(L["rank_offsets"], _ints(g["rank_offsets"]))
+    np.testing.assert_array_equal(L["row_of_slot"].ravel(), _ints(g["row_of_slot"]))
+    n = int(L["rank_offsets"][-1])
+    ri, _ = oracle.nonexpand_recv_topk(idx, None, L["row_of_slot"], E, R, n)
+    np.testing.assert_array_equal(ri.ravel(), _ints(g["recv_topk_idx"]))
+
+
+@pytest.mark.parametrize("case", CORNERS)
+def test_layout_nonexpand_vs_brute(case):
+    T, K, E, R, drop_p, distinct, bad_p = case
+    idx = _random_routing(np.random.default_rng(T), T, K, E, drop_p, distinct, bad_p)
+    a = oracle.layout_nonexpand(idx, E, R)
+    b = brute.layout_nonexpand(idx, E, R)
+    for key in ["num_tokens_per_expert", "num_tokens_per_rank", "is_token_in_rank", "rank_offsets",
+                "row_of_slot", "status"]:
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    # each (token, rank) pair owns exactly one row; rows of a rank lie in its range
+    n = int(a["rank_offsets"][-1])
+    r = a["row_of_slot"]
+    assert np.array_equal(np.sort(r[r >= 0]), np.arange(n))
+    assert n == int(a["is_token_in_rank"].sum())
