@@ -388,6 +388,28 @@ def gpu_arm(args, rank, world, local):
     h_a.destroy()
     del recv_a
 
+    # non-expand layout (one row per (token, rank)) + bf16 dispatch, prefill routing
+    with torch.cuda.stream(stream):
+        off_r = torch.empty(R + 1, dtype=torch.int32, device=dev)
+        recv_ne = torch.empty(T * R, H, dtype=torch.bfloat16, device=dev)
+    h_ne = ep.ep_layout_nonexpand(idx, E, R, cnt, ntr, itr, off_r, stream=stream)
+    n_ne, _ = ep.ep_handle_query(h_ne)
+    ev_ne = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps_b)]
+    for i in range(-3, reps_b):
+        if i >= 0:
+            ev_ne[i][0].record(stream)
+        ep.ep_layout_nonexpand(idx, E, R, cnt, ntr, itr, off_r, handle=h_ne, stream=stream)
+        if i >= 0:
+            ev_ne[i][1].record(stream)
+        ep.ep_dispatch(h_ne, x, ep.EP_DTYPE_BF16, recv_ne, T * R, stream=stream)
+        if i >= 0:
+            ev_ne[i][2].record(stream)
+    stream.synchronize()
+    ms_ne = [float(np.mean([e[j].elapsed_time(e[j + 1]) for e in ev_ne])) for j in range(2)]
+    b_ne = 2 * T * H + 2 * n_ne * H + 4 * T * K
+    h_ne.destroy()
+    del recv_ne
+
     # decode shape through the low-latency padded 3-D layout [E, cap, H]
     # (cap = T: every token could pick one expert); ~33 MB, L2-resident
     dec = gi.make("decode", seed=args.seed + rank)
@@ -487,6 +509,10 @@ def gpu_arm(args, rank, world, local):
                                     "gbs": round(b_t2m / (ms_t2m * 1e-3) / 1e9, 1)},
             "routing_map_to_topk": {"us": round(ms_m2t * 1e3, 2), "bytes": b_m2t,
                                     "gbs": round(b_m2t / (ms_m2t * 1e-3) / 1e9, 1)},
+            "dispatch_bf16_nonexpand": {"rows": n_ne, "layout_us": round(ms_ne[0] * 1e3, 2),
+                                        "us": round(ms_ne[1] * 1e3, 2), "bytes": b_ne,
+                                        "gbs": round(b_ne / (ms_ne[1] * 1e-3) / 1e9, 1),
+                                        "frac_of_measured": round(b_ne / (ms_ne[1] * 1e-3) / 1e9 / peak, 4)},
             "decode_ll_step": {"workload": "decode T=256 H=7168 E=256 K=8 R=8, strided layout cap=256, "
                                            "L2-resident (33 MB), warm",
                                "layout_strided_us": round(ms_d[0] * 1e3, 2),

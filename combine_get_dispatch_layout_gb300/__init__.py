@@ -26,7 +26,8 @@ class DispatchConfig(ctypes.Structure):
                 ("scales_col_major", ctypes.c_int), ("scales_ld", ctypes.c_int64)]
 
 # Exported symbols declared in include/ep.h.
-EXPORTS = ("ep_layout", "ep_layout_aligned", "ep_layout_strided", "ep_dispatch", "ep_dispatch_ex", "ep_combine", "ep_combine_backward",
+EXPORTS = ("ep_layout", "ep_layout_aligned", "ep_layout_strided", "ep_layout_nonexpand",
+           "ep_nonexpand_recv_topk", "ep_dispatch", "ep_dispatch_ex", "ep_combine", "ep_combine_backward",
            "ep_dispatch_backward", "ep_topk_to_routing_map", "ep_routing_map_to_topk", "ep_handle_query",
            "ep_handle_copy_row_of_slot", "ep_handle_destroy", "ep_handle_layout_kernels",
            "ep_layout_noalloc", "ep_status_string")
@@ -52,6 +53,8 @@ def lib() -> ctypes.CDLL:
         L.ep_layout.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, ctypes.POINTER(P), P]
         L.ep_layout_aligned.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, P, P, ctypes.POINTER(P), P]
         L.ep_layout_strided.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, P, P, ctypes.POINTER(P), P]
+        L.ep_layout_nonexpand.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, ctypes.POINTER(P), P]
+        L.ep_nonexpand_recv_topk.argtypes = [P, P, P, i32, P, P, i64, P]
         L.ep_dispatch.argtypes = [P, P, i32, i32, P, P, P, P, P, i64, P]
         L.ep_dispatch_ex.argtypes = [P, P, P, i32, ctypes.POINTER(DispatchConfig), P, P, P, P, P, i64, P]
         L.ep_combine.argtypes = [P, P, i64, i32, P, P, P]
@@ -168,6 +171,28 @@ def ep_layout_strided(topk_idx, num_experts: int, num_ranks: int, expert_capacit
                                  _stream(stream))
     _check(st, "ep_layout_strided")
     return h
+
+
+def ep_layout_nonexpand(topk_idx, num_experts: int, num_ranks: int, num_tokens_per_expert,
+                        num_tokens_per_rank, is_token_in_rank, rank_offsets, handle: Handle | None = None,
+                        stream=None, alloc_fn=None, free_fn=None) -> Handle:
+    """Layout with one receive row per (token, rank) pair, grouped by rank."""
+    T, K = topk_idx.shape
+    h = handle if handle is not None else Handle()
+    st = lib().ep_layout_nonexpand(_ptr(topk_idx), T, K, num_experts, num_ranks, _ptr(num_tokens_per_expert),
+                                   _ptr(num_tokens_per_rank), _ptr(is_token_in_rank), _ptr(rank_offsets),
+                                   _fnptr(alloc_fn), _fnptr(free_fn), ctypes.byref(h.ptr), _stream(stream))
+    _check(st, "ep_layout_nonexpand")
+    return h
+
+
+def ep_nonexpand_recv_topk(handle: Handle, topk_idx, num_experts: int, recv_topk_idx, recv_topk_weights=None,
+                           topk_weights=None, recv_capacity: int | None = None, stream=None) -> None:
+    """Per non-expand receive row: rank-local expert ids (or -1) and weights."""
+    cap = int(recv_topk_idx.shape[0]) if recv_capacity is None else int(recv_capacity)
+    st = lib().ep_nonexpand_recv_topk(handle.ptr, _ptr(topk_idx), _ptr(topk_weights), num_experts,
+                                      _ptr(recv_topk_idx), _ptr(recv_topk_weights), cap, _stream(stream))
+    _check(st, "ep_nonexpand_recv_topk")
 
 
 def ep_dispatch(handle: Handle, x, out_dtype: int, recv_x, recv_capacity: int, recv_scales=None,

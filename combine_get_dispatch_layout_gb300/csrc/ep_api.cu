@@ -34,6 +34,9 @@ struct ep_handle {
     int32_t* block_rank = nullptr;  // [cap_rank_cells]
     int32_t* counts = nullptr;      // [cap_experts] copy of num_tokens_per_expert
     int32_t* offsets = nullptr;     // [cap_experts + 1] copy of expert_offsets
+    int64_t cap_keys = 0;
+    int64_t* keys = nullptr;        // [cap_keys] derived (rank) keys of a non-expand layout
+    int32_t* rank_scratch = nullptr;  // [cap_experts] second copy of the key counts
     int32_t* host_meta = nullptr;   // pinned [ep::kMetaWords]
 };
 
@@ -54,15 +57,16 @@ ep_status_t current_device_is(const ep_handle* h) {
 void release_block(ep_handle* h) {
     if (h->dev_block) h->free_fn(h->dev_block);
     h->dev_block = nullptr;
-    h->meta = h->row_of_slot = h->chunk_cnt = h->block_rank = h->counts = h->offsets = nullptr;
-    h->cap_slots = h->cap_chunk_cells = h->cap_rank_cells = h->cap_experts = 0;
+    h->meta = h->row_of_slot = h->chunk_cnt = h->block_rank = h->counts = h->offsets = h->rank_scratch = nullptr;
+    h->keys = nullptr;
+    h->cap_slots = h->cap_chunk_cells = h->cap_rank_cells = h->cap_experts = h->cap_keys = 0;
 }
 
 // (Re)allocate the device block for at least the given sizes; zeroes the state words.
 ep_status_t ensure_block(ep_handle* h, int64_t slots, int64_t chunk_cells, int64_t rank_cells,
-                         int64_t experts, cudaStream_t stream) {
+                         int64_t experts, int64_t keys, cudaStream_t stream) {
     if (h->dev_block && slots <= h->cap_slots && chunk_cells <= h->cap_chunk_cells &&
-        rank_cells <= h->cap_rank_cells && experts <= h->cap_experts)
+        rank_cells <= h->cap_rank_cells && experts <= h->cap_experts && keys <= h->cap_keys)
         return EP_OK;
     if (h->dev_block) {
         // work already enqueued may still read the old block
@@ -74,9 +78,10 @@ ep_status_t ensure_block(ep_handle* h, int64_t slots, int64_t chunk_cells, int64
     const size_t rows_b = round_up(sizeof(int32_t) * static_cast<size_t>(slots > 0 ? slots : 1), a);
     const size_t cnt_b = round_up(sizeof(int32_t) * static_cast<size_t>(chunk_cells > 0 ? chunk_cells : 1), a);
     const size_t rank_b = round_up(sizeof(int32_t) * static_cast<size_t>(rank_cells > 0 ? rank_cells : 1), a);
-    const size_t exp_b = round_up(sizeof(int32_t) * static_cast<size_t>(2 * experts + 1), a);
+    const size_t exp_b = round_up(sizeof(int32_t) * static_cast<size_t>(3 * experts + 1), a);
+    const size_t key_b = round_up(sizeof(int64_t) * static_cast<size_t>(keys > 0 ? keys : 1), a);
     void* block = nullptr;
-    if (h->alloc_fn(&block, meta_b + rows_b + cnt_b + rank_b + exp_b) != 0 || block == nullptr)
+    if (h->alloc_fn(&block, meta_b + rows_b + cnt_b + rank_b + exp_b + key_b) != 0 || block == nullptr)
         return EP_ERR_ALLOC;
     char* base = static_cast<char*>(block);
     h->dev_block = block;
@@ -86,6 +91,9 @@ ep_status_t ensure_block(ep_handle* h, int64_t slots, int64_t chunk_cells, int64
     h->block_rank = reinterpret_cast<int32_t*>(base + meta_b + rows_b + cnt_b);
     h->counts = reinterpret_cast<int32_t*>(base + meta_b + rows_b + cnt_b + rank_b);
     h->offsets = h->counts + experts;
+    h->rank_scratch = h->offsets + experts + 1;
+    h->keys = reinterpret_cast<int64_t*>(base + meta_b + rows_b + cnt_b + rank_b + exp_b);
+    h->cap_keys = keys;
     h->cap_slots = slots;
     h->cap_chunk_cells = chunk_cells;
     h->cap_rank_cells = rank_cells;
@@ -134,7 +142,7 @@ ep_status_t check_rows(ep_handle* h, int64_t capacity) {
 
 namespace {
 
-ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int align, int stride,
+ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int align, int stride, bool nonexpand,
                         int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
                         uint8_t* is_token_in_rank, int32_t* expert_offsets,
                         ep_alloc_fn alloc_fn, ep_free_fn free_fn,
@@ -173,12 +181,16 @@ ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int
         if (st != EP_OK) return st;
     }
 
-    ep::LayoutPlan plan = ep::make_layout_plan(T, K, E, R);
+    // a non-expand layout runs the expert layout over derived rank keys: the
+    // key space is the R ranks (one "expert" per rank)
+    const int KE = nonexpand ? R : E;
+    ep::LayoutPlan plan = ep::make_layout_plan(T, K, KE, R);
     plan.align = align;
     plan.stride = stride;
     ep_status_t st = ensure_block(h, static_cast<int64_t>(T) * K,
-                                  static_cast<int64_t>(E) * plan.num_chunks,
-                                  static_cast<int64_t>(R) * plan.num_blocks, E, s);
+                                  static_cast<int64_t>(KE) * plan.num_chunks,
+                                  static_cast<int64_t>(R) * plan.num_blocks, KE,
+                                  nonexpand ? static_cast<int64_t>(T) * K : 0, s);
     if (st != EP_OK) {
         if (created) {
             cudaFreeHost(h->host_meta);
@@ -189,7 +201,7 @@ ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int
         }
         return st;
     }
-    h->T = T; h->K = K; h->E = E; h->R = R;
+    h->T = T; h->K = K; h->E = KE; h->R = R;
     h->align = align;
     h->stride = stride;
     h->plan = plan;
@@ -200,14 +212,25 @@ ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int
     if (T == 0) {
         err = cudaMemsetAsync(num_tokens_per_expert, 0, sizeof(int32_t) * E, s);
         if (err == cudaSuccess) err = cudaMemsetAsync(num_tokens_per_rank, 0, sizeof(int32_t) * R, s);
-        if (err == cudaSuccess) err = cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E + 1), s);
+        if (err == cudaSuccess) err = cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (KE + 1), s);
         if (err == cudaSuccess) err = cudaMemsetAsync(h->meta, 0, sizeof(int32_t) * ep::kMetaWords, s);
-        if (err == cudaSuccess) err = cudaMemsetAsync(h->counts, 0, sizeof(int32_t) * (2 * E + 1), s);
+        if (err == cudaSuccess) err = cudaMemsetAsync(h->counts, 0, sizeof(int32_t) * (2 * KE + 1), s);
     } else {
         ep::LayoutArgs a{};
         a.topk_idx = topk_idx;
         a.num_tokens_per_expert = num_tokens_per_expert;
         a.num_tokens_per_rank = num_tokens_per_rank;
+        err = cudaSuccess;
+        if (nonexpand) {
+            // expert counts by the key pass; the key layout's per-key counts
+            // are the per-rank token counts
+            err = cudaMemsetAsync(num_tokens_per_expert, 0, sizeof(int32_t) * E, s);
+            if (err == cudaSuccess)
+                err = ep::launch_nonexpand_keys(topk_idx, T, K, E, R, h->keys, num_tokens_per_expert, s);
+            a.topk_idx = h->keys;
+            a.num_tokens_per_expert = num_tokens_per_rank;
+            a.num_tokens_per_rank = h->rank_scratch;
+        }
         a.is_token_in_rank = is_token_in_rank;
         a.expert_offsets = expert_offsets;
         a.row_of_slot = h->row_of_slot;
@@ -216,7 +239,7 @@ ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int
         a.meta = h->meta;
         a.h_counts = h->counts;
         a.h_offsets = h->offsets;
-        err = ep::launch_layout(plan, a, s, &h->layout_kernels);
+        if (err == cudaSuccess) err = ep::launch_layout(plan, a, s, &h->layout_kernels);
     }
     if (T == 0) h->layout_kernels = 0;
     *handle = h;
@@ -232,7 +255,7 @@ ep_status_t ep_layout(const int64_t* topk_idx, int T, int K, int E, int R,
                       uint8_t* is_token_in_rank, int32_t* expert_offsets,
                       ep_alloc_fn alloc_fn, ep_free_fn free_fn,
                       ep_handle_t* handle, void* stream) {
-    return layout_impl(topk_idx, T, K, E, R, 1, 0, num_tokens_per_expert, num_tokens_per_rank, is_token_in_rank,
+    return layout_impl(topk_idx, T, K, E, R, 1, 0, false, num_tokens_per_expert, num_tokens_per_rank, is_token_in_rank,
                        expert_offsets, alloc_fn, free_fn, handle, stream);
 }
 
@@ -241,7 +264,7 @@ ep_status_t ep_layout_aligned(const int64_t* topk_idx, int T, int K, int E, int 
                               uint8_t* is_token_in_rank, int32_t* expert_offsets,
                               ep_alloc_fn alloc_fn, ep_free_fn free_fn,
                               ep_handle_t* handle, void* stream) {
-    return layout_impl(topk_idx, T, K, E, R, expert_alignment, 0, num_tokens_per_expert, num_tokens_per_rank,
+    return layout_impl(topk_idx, T, K, E, R, expert_alignment, 0, false, num_tokens_per_expert, num_tokens_per_rank,
                        is_token_in_rank, expert_offsets, alloc_fn, free_fn, handle, stream);
 }
 
@@ -251,8 +274,38 @@ ep_status_t ep_layout_strided(const int64_t* topk_idx, int T, int K, int E, int 
                               ep_alloc_fn alloc_fn, ep_free_fn free_fn,
                               ep_handle_t* handle, void* stream) {
     if (expert_capacity < 1) return EP_ERR_INVALID_ARG;
-    return layout_impl(topk_idx, T, K, E, R, 1, expert_capacity, num_tokens_per_expert, num_tokens_per_rank,
+    return layout_impl(topk_idx, T, K, E, R, 1, expert_capacity, false, num_tokens_per_expert, num_tokens_per_rank,
                        is_token_in_rank, expert_offsets, alloc_fn, free_fn, handle, stream);
+}
+
+ep_status_t ep_layout_nonexpand(const int64_t* topk_idx, int T, int K, int E, int R,
+                                int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                                uint8_t* is_token_in_rank, int32_t* rank_offsets,
+                                ep_alloc_fn alloc_fn, ep_free_fn free_fn,
+                                ep_handle_t* handle, void* stream) {
+    return layout_impl(topk_idx, T, K, E, R, 1, 0, true, num_tokens_per_expert, num_tokens_per_rank,
+                       is_token_in_rank, rank_offsets, alloc_fn, free_fn, handle, stream);
+}
+
+ep_status_t ep_nonexpand_recv_topk(ep_handle_t handle, const int64_t* topk_idx, const float* topk_weights, int E,
+                                   int64_t* recv_topk_idx, float* recv_topk_weights, int64_t recv_capacity,
+                                   void* stream) {
+    if (!handle) return EP_ERR_INVALID_ARG;
+    const int T = handle->T, K = handle->K, R = handle->R;
+    if (E < 1 || E > EP_MAX_EXPERTS || E % R != 0 || recv_capacity < 0) return EP_ERR_INVALID_ARG;
+    if (T > 0 && !topk_idx) return EP_ERR_INVALID_ARG;
+    if (recv_capacity > 0 && !recv_topk_idx) return EP_ERR_INVALID_ARG;
+    if (!aligned(topk_idx, 8) || !aligned(recv_topk_idx, 8) || !aligned(topk_weights, 4) ||
+        !aligned(recv_topk_weights, 4))
+        return EP_ERR_INVALID_ARG;
+    ep_status_t st = current_device_is(handle);
+    if (st != EP_OK) return st;
+    st = check_rows(handle, recv_capacity);
+    if (st != EP_OK) return st;
+    return ep::launch_nonexpand_recv_topk(topk_idx, topk_weights, handle->row_of_slot, T, K, E, R, recv_topk_idx,
+                                          recv_topk_weights, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? EP_OK
+               : EP_ERR_CUDA;
 }
 
 ep_status_t ep_dispatch_ex(ep_handle_t handle, const void* x, const void* x_scales, int H,

@@ -103,3 +103,106 @@ cudaError_t launch_routing_map_to_topk(const uint8_t* routing_map, const float* 
 }
 
 }  // namespace ep
+
+// ---------------------------------------------------------------- non-expand
+
+namespace ep {
+
+namespace {
+
+// One thread per token: key[t, k] = rank of slot k's expert if it is the
+// token's first slot on that rank, -1 otherwise (repeats, unused slots), -2
+// for an id outside [-1, E) so the layout that follows reports it. Valid
+// slots are counted per expert in a shared-memory histogram that each block
+// adds to the global counts once per non-empty bin (integer adds: exact in
+// any order). Ranks seen so far live in a register mask when R <= 32.
+__global__ void __launch_bounds__(256)
+nonexpand_keys_kernel(const int64_t* topk_idx, int T, int K, int E, int R, int L, int64_t* keys,
+                      int32_t* expert_counts) {
+    extern __shared__ int hist[];                  // [E]
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < T) {
+        const int64_t* row = topk_idx + static_cast<int64_t>(t) * K;
+        int64_t* out = keys + static_cast<int64_t>(t) * K;
+        unsigned seen_small = 0u;
+        for (int k = 0; k < K; ++k) {
+            const int64_t e = row[k];
+            int64_t key = -1;
+            if (e < -1 || e >= E) {
+                key = -2;
+            } else if (e >= 0) {
+                atomicAdd(hist + e, 1);
+                const int r = static_cast<int>(e / L);
+                bool first;
+                if (R <= 32) {
+                    first = !(seen_small & (1u << r));
+                    seen_small |= 1u << r;
+                } else {
+                    first = true;
+                    for (int j = 0; j < k; ++j) {
+                        const int64_t ej = row[j];
+                        if (ej >= 0 && ej < E && ej / L == r) { first = false; break; }
+                    }
+                }
+                if (first) key = r;
+            }
+            out[k] = key;
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        if (hist[e]) atomicAdd(expert_counts + e, hist[e]);
+}
+
+// One warp per token: for each slot that owns a (token, rank) row, write that
+// row's K entries: rank-local expert id (and weight) for the token's slots on
+// the rank, -1 (and 0) for the others.
+__global__ void __launch_bounds__(kConvWarps * 32)
+nonexpand_recv_topk_kernel(const int64_t* topk_idx, const float* w, const int32_t* row_of_slot, int T, int K,
+                           int E, int L, int64_t* recv_topk_idx, float* recv_topk_weights) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kConvWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int64_t e = -1;
+    float wk = 0.0f;
+    int row = -1;
+    if (lane < K) {
+        e = topk_idx[static_cast<int64_t>(t) * K + lane];
+        if (w) wk = w[static_cast<int64_t>(t) * K + lane];
+        row = row_of_slot[static_cast<int64_t>(t) * K + lane];
+    }
+    const int rank = (e >= 0 && e < E) ? static_cast<int>(e / L) : -1;
+    for (int j = 0; j < K; ++j) {
+        const int rj = __shfl_sync(kFullMask, row, j);
+        const int rkj = __shfl_sync(kFullMask, rank, j);
+        if (rj < 0) continue;
+        if (lane < K) {
+            const bool on = rank == rkj;
+            recv_topk_idx[static_cast<int64_t>(rj) * K + lane] = on ? e - static_cast<int64_t>(rkj) * L : -1;
+            if (recv_topk_weights) recv_topk_weights[static_cast<int64_t>(rj) * K + lane] = on ? wk : 0.0f;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_nonexpand_keys(const int64_t* topk_idx, int T, int K, int E, int R, int64_t* keys,
+                                  int32_t* expert_counts, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    nonexpand_keys_kernel<<<(T + 255) / 256, 256, static_cast<size_t>(E) * sizeof(int), stream>>>(
+        topk_idx, T, K, E, R, E / R, keys, expert_counts);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_nonexpand_recv_topk(const int64_t* topk_idx, const float* w, const int32_t* row_of_slot, int T,
+                                       int K, int E, int R, int64_t* recv_topk_idx, float* recv_topk_weights,
+                                       cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    nonexpand_recv_topk_kernel<<<(T + kConvWarps - 1) / kConvWarps, kConvWarps * 32, 0, stream>>>(
+        topk_idx, w, row_of_slot, T, K, E, E / R, recv_topk_idx, recv_topk_weights);
+    return cudaGetLastError();
+}
+
+}  // namespace ep

@@ -125,6 +125,11 @@ cudaError_t launch_gather_slot_weights(const int32_t* row_of_slot, const float* 
 cudaError_t launch_topk_to_routing_map(const int64_t* topk_idx, const float* w, int T, int K, int E,
                                        uint8_t* routing_map, float* probs, int32_t* device_error,
                                        cudaStream_t stream);
+cudaError_t launch_nonexpand_keys(const int64_t* topk_idx, int T, int K, int E, int R, int64_t* keys,
+                                  int32_t* expert_counts, cudaStream_t stream);
+cudaError_t launch_nonexpand_recv_topk(const int64_t* topk_idx, const float* w, const int32_t* row_of_slot, int T,
+                                       int K, int E, int R, int64_t* recv_topk_idx, float* recv_topk_weights,
+                                       cudaStream_t stream);
 cudaError_t launch_routing_map_to_topk(const uint8_t* routing_map, const float* probs, int T, int E, int K,
                                        int64_t* topk_idx, float* topk_weights, int32_t* device_error,
                                        cudaStream_t stream);

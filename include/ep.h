@@ -189,6 +189,41 @@ EP_API ep_status_t ep_layout_strided(const int64_t* topk_idx, int T, int K, int 
                                      ep_handle_t* handle, void* stream);
 
 /*
+ * ep_layout_nonexpand -- layout with one receive row per (token, rank) pair
+ * instead of per (token, expert) (DeepEP API docs, "Prefix Sum Interpretation
+ * for Expert Token Counts", non-expand mode; nccl_ep.cc, struct ncclEpHandle:
+ * sparse_to_dense_map [tokens, ranks], -1 = not routed). Rows are grouped by
+ * rank, tokens ascending inside a rank; rank r owns rows
+ * [rank_offsets[r], rank_offsets[r+1]) (int32 [R + 1], the exclusive scan of
+ * num_tokens_per_rank). In the handle, a token's row for rank r belongs to its
+ * first slot on r (lowest k); its other slots on r hold -1. So ep_dispatch
+ * writes each token once per rank it reaches, and ep_combine with NULL
+ * weights sums one expert-side row per rank (the expert side applies the
+ * per-expert weights, see ep_nonexpand_recv_topk). num_tokens_per_expert,
+ * num_tokens_per_rank and is_token_in_rank are those of ep_layout. Other
+ * arguments and errors as ep_layout.
+ */
+EP_API ep_status_t ep_layout_nonexpand(const int64_t* topk_idx, int T, int K, int E, int R,
+                                       int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                                       uint8_t* is_token_in_rank, int32_t* rank_offsets,
+                                       ep_alloc_fn alloc_fn, ep_free_fn free_fn,
+                                       ep_handle_t* handle, void* stream);
+
+/*
+ * ep_nonexpand_recv_topk -- what each non-expand receive row carries for its
+ * rank's experts (DeepEP API docs, "dispatch()": recv_topk_idx and
+ * recv_topk_weights): for the row of (t, r), entry k is the rank-local expert
+ * id e - r * (E/R) if slot k of token t names an expert e of rank r, else -1;
+ * the weight is topk_weights[t, k] there, else 0. topk_idx / topk_weights are
+ * the ones given to ep_layout_nonexpand (weights may be NULL);
+ * recv_topk_idx int64 [cap, K], recv_topk_weights fp32 [cap, K] or NULL.
+ * Rows >= N are not written.
+ */
+EP_API ep_status_t ep_nonexpand_recv_topk(ep_handle_t handle, const int64_t* topk_idx, const float* topk_weights,
+                                          int E, int64_t* recv_topk_idx, float* recv_topk_weights,
+                                          int64_t recv_capacity, void* stream);
+
+/*
  * ep_dispatch -- stable expert-major permute of the token rows.
  *
  * For every valid slot (t, k) with receive row n = row_of_slot[t, k]:

@@ -905,3 +905,83 @@ def test_strided_multiblock_path(ep):
 
 def test_strided_tiny_capacity(ep):
     strided_path(ep, gi.make("tiny", 4, with_y=False), 1)
+
+
+# ------------------------------------------------------------------ non-expand layout
+
+def nonexpand_path(ep, inp):
+    w = inp.w
+    T, K, E, R, H = w.T, w.K, w.E, w.R, w.H
+    ref = oracle.layout_nonexpand(inp.topk_idx, E, R)
+    n = int(ref["rank_offsets"][-1])
+    o = [torch.full((E,), -7, dtype=torch.int32, device="cuda"), torch.full((R,), -7, dtype=torch.int32, device="cuda"),
+         torch.full((T, R), SENT8, dtype=torch.uint8, device="cuda"),
+         torch.full((R + 1,), -7, dtype=torch.int32, device="cuda")]
+    h = ep.ep_layout_nonexpand(_dev(inp.topk_idx), E, R, *o)
+    rows = torch.full((T, K), -9, dtype=torch.int32, device="cuda")
+    ep.ep_handle_copy_row_of_slot(h, rows)
+    torch.cuda.synchronize()
+    for got, key in zip(o, ["num_tokens_per_expert", "num_tokens_per_rank", "is_token_in_rank", "rank_offsets"]):
+        np.testing.assert_array_equal(got.cpu().numpy(), ref[key], err_msg=key)
+    np.testing.assert_array_equal(rows.cpu().numpy(), ref["row_of_slot"])
+    assert ep.ep_handle_query(h) == (n, 0)
+    # dispatch: one copy per (token, rank)
+    r_x, r_src, _ = oracle.dispatch_bf16(inp.x, ref["row_of_slot"], n)
+    recv = torch.full((n + GUARD, H), SENT16, dtype=torch.int16, device="cuda")
+    src = torch.full((n + GUARD,), -5, dtype=torch.int32, device="cuda")
+    ep.ep_dispatch(h, _dev(inp.x.view(np.int16)), ep.EP_DTYPE_BF16, recv, n + GUARD, recv_src_token=src)
+    torch.cuda.synchronize()
+    g = recv.cpu().numpy().view(np.uint16)
+    np.testing.assert_array_equal(g[:n], r_x)
+    assert (g[n:] == SENT16).all()
+    np.testing.assert_array_equal(src.cpu().numpy()[:n], r_src)
+    # receive-side top-k per row
+    ri = torch.full((n + 1, K), -9, dtype=torch.int64, device="cuda")
+    rw = torch.full((n + 1, K), -1.0, dtype=torch.float32, device="cuda")
+    ep.ep_nonexpand_recv_topk(h, _dev(inp.topk_idx), E, ri, recv_topk_weights=rw,
+                              topk_weights=_dev(inp.topk_weights), recv_capacity=n + 1)
+    torch.cuda.synchronize()
+    r_ri, r_rw = oracle.nonexpand_recv_topk(inp.topk_idx, inp.topk_weights, ref["row_of_slot"], E, R, n)
+    np.testing.assert_array_equal(ri.cpu().numpy()[:n], r_ri)
+    np.testing.assert_array_equal(rw.cpu().numpy()[:n].view(np.uint32), r_rw.view(np.uint32))
+    assert (ri.cpu().numpy()[n:] == -9).all()
+    # unweighted combine: one expert-side row per rank
+    y = gi.normal_bf16(np.random.SeedSequence(41), n, H)
+    out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    ep.ep_combine(h, _dev(y.view(np.int16)) if n else torch.empty((1, H), dtype=torch.int16, device="cuda"), out,
+                  y_rows=n)
+    torch.cuda.synchronize()
+    assert_combine(out.cpu().numpy().view(np.uint16), oracle.combine(y, ref["row_of_slot"], None))
+    h.destroy()
+
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("decode", None), ("prefill", 2048), ("skewed", 3000)])
+def test_nonexpand_workloads(ep, name, T):
+    nonexpand_path(ep, gi.make(name, 15, T=T, with_y=False))
+
+
+@pytest.mark.parametrize("w", [
+    _workload(300, 128, 512, 8, 64),                                  # R > 32
+    _workload(40000, 64, 64, 8, 4, routing="zipf", drop_p=0.05),      # multi-block layout path
+    _workload(50, 128, 8, 2, 2, drop_p=1.0),                          # nothing routed
+])
+def test_nonexpand_edges(ep, w):
+    nonexpand_path(ep, gi.make(w, 16, with_y=False))
+
+
+def test_nonexpand_duplicate_experts_and_invalid_ids(ep):
+    rng = np.random.default_rng(17)
+    idx = rng.integers(0, 12, size=(200, 4)).astype(np.int64)
+    idx[rng.random((200, 4)) < 0.1] = -1
+    inp = gi.Inputs(w=_workload(200, 128, 12, 4, 3), seed=0, x=gi.normal_bf16(np.random.SeedSequence(18), 200, 128),
+                    topk_idx=idx, topk_weights=rng.random((200, 4)).astype(np.float32), y=None, num_valid=0)
+    nonexpand_path(ep, inp)
+    bad = idx.copy()
+    bad[7, 2] = 99
+    ref = oracle.layout_nonexpand(bad, 12, 3)
+    o = [torch.empty(12, dtype=torch.int32, device="cuda"), torch.empty(3, dtype=torch.int32, device="cuda"),
+         torch.empty(200, 3, dtype=torch.uint8, device="cuda"), torch.empty(4, dtype=torch.int32, device="cuda")]
+    h = ep.ep_layout_nonexpand(_dev(bad), 12, 3, *o)
+    assert ep.ep_handle_query(h)[1] == ep.EP_ERR_INVALID_EXPERT
+    np.testing.assert_array_equal(o[3].cpu().numpy(), ref["rank_offsets"])
+    h.destroy()
