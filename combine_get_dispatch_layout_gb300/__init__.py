@@ -23,7 +23,7 @@ EP_SCALE_FP32, EP_SCALE_POW2, EP_SCALE_UE8M0 = 0, 1, 2
 class DispatchConfig(ctypes.Structure):
     """ep_dispatch_config_t (include/ep.h)."""
     _fields_ = [("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int), ("scale_mode", ctypes.c_int),
-                ("scales_col_major", ctypes.c_int), ("scales_ld", ctypes.c_int64)]
+                ("scales_col_major", ctypes.c_int), ("scales_ld", ctypes.c_int64), ("overlap_layout", ctypes.c_int)]
 
 # Exported symbols declared in include/ep.h.
 EXPORTS = ("ep_layout", "ep_layout_aligned", "ep_layout_strided", "ep_layout_nonexpand",
@@ -208,10 +208,12 @@ def ep_dispatch(handle: Handle, x, out_dtype: int, recv_x, recv_capacity: int, r
 def ep_dispatch_ex(handle: Handle, x, recv_x, recv_capacity: int, out_dtype: int = EP_DTYPE_FP8_E4M3,
                    in_dtype: int = EP_DTYPE_BF16, scale_mode: int = EP_SCALE_FP32, x_scales=None, recv_scales=None,
                    scales_col_major: bool = False, scales_ld: int = 0, recv_src_token=None, recv_weights=None,
-                   topk_weights=None, H: int | None = None, stream=None) -> None:
-    """ep_dispatch with fp8 scale modes, column-major scales and fp8 input pass-through."""
+                   topk_weights=None, H: int | None = None, overlap_layout: bool = False, stream=None) -> None:
+    """ep_dispatch with fp8 scale modes, column-major scales, fp8 input pass-through and
+    overlap with the layout that precedes it on the stream."""
     H = int(x.shape[-1]) if H is None else int(H)
-    cfg = DispatchConfig(in_dtype, out_dtype, scale_mode, 1 if scales_col_major else 0, int(scales_ld))
+    cfg = DispatchConfig(in_dtype, out_dtype, scale_mode, 1 if scales_col_major else 0, int(scales_ld),
+                         1 if overlap_layout else 0)
     st = lib().ep_dispatch_ex(handle.ptr, _ptr(x), _ptr(x_scales), H, ctypes.byref(cfg), _ptr(topk_weights),
                               _ptr(recv_x), _ptr(recv_scales), _ptr(recv_src_token), _ptr(recv_weights),
                               int(recv_capacity), _stream(stream))

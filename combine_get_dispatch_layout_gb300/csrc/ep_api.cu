@@ -357,6 +357,7 @@ ep_status_t ep_dispatch_ex(ep_handle_t handle, const void* x, const void* x_scal
     a.scale_col_major = cfg.scales_col_major ? 1 : 0;
     a.scale_ld = cfg.scales_ld;
     a.x_scales = x_scales;
+    a.overlap_layout = cfg.overlap_layout ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t err = fp8_in ? ep::launch_dispatch_fp8_passthrough(a, s)
                       : fp8  ? ep::launch_dispatch_fp8(a, s)

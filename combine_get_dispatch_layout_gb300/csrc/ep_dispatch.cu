@@ -34,6 +34,10 @@ __device__ __forceinline__ int4 ld_stream(const int4* p) {
     return v;
 }
 
+// Wait for the preceding grid (the layout that wrote row_of_slot) when this
+// kernel was launched as its programmatic dependent; a no-op otherwise.
+__device__ __forceinline__ void wait_for_layout() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Row of each slot of token t, lane k holds slot k (K <= 32); -1 if unused.
 __device__ __forceinline__ int slot_row(const int32_t* row_of_slot, int t, int K, int lane) {
     return lane < K ? __ldg(row_of_slot + static_cast<int64_t>(t) * K + lane) : -1;
@@ -54,8 +58,6 @@ dispatch_bf16_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
     const int t = static_cast<int>(item / num_segments);
     const int seg = static_cast<int>(item - static_cast<int64_t>(t) * num_segments);
     const int H16 = a.H / 8;                          // 16-byte vectors per row
-    const int row = slot_row(a.row_of_slot, t, a.K, lane);
-    if (seg == 0) write_side_outputs(a, t, lane, row);
 
     const int4* src = reinterpret_cast<const int4*>(a.x) + static_cast<int64_t>(t) * H16;
     int4* dst = reinterpret_cast<int4*>(a.recv_x);
@@ -66,6 +68,10 @@ dispatch_bf16_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
         const int j = j0 + u * 32;
         if (j < H16) v[u] = ld_stream(src + j);
     }
+    // x is ready before the layout starts; the slot map only after it ends
+    wait_for_layout();
+    const int row = slot_row(a.row_of_slot, t, a.K, lane);
+    if (seg == 0) write_side_outputs(a, t, lane, row);
     for (int k = 0; k < a.K; ++k) {
         const int r = __shfl_sync(kFullMask, row, k);
         if (r < 0) continue;
@@ -119,8 +125,6 @@ dispatch_fp8_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
     const int seg = static_cast<int>(item - static_cast<int64_t>(t) * num_segments);
     const int H16 = a.H / 8;                          // 8-channel groups per row
     const int nb = a.H / 128;                         // scale blocks per row
-    const int row = slot_row(a.row_of_slot, t, a.K, lane);
-    if (seg == 0) write_side_outputs(a, t, lane, row);
 
     const int4* src = reinterpret_cast<const int4*>(a.x) + static_cast<int64_t>(t) * H16;
     uint2 q[kFp8Unroll];
@@ -156,6 +160,9 @@ dispatch_fp8_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
             q[u] = make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
         }
     }
+    wait_for_layout();
+    const int row = slot_row(a.row_of_slot, t, a.K, lane);
+    if (seg == 0) write_side_outputs(a, t, lane, row);
     uint2* dst = reinterpret_cast<uint2*>(a.recv_x);   // 8 codes per lane
     for (int k = 0; k < a.K; ++k) {
         const int r = __shfl_sync(kFullMask, row, k);
@@ -195,7 +202,6 @@ dispatch_fp8_passthrough_kernel(DispatchArgs a, int64_t num_items, int num_segme
     const int seg = static_cast<int>(item - static_cast<int64_t>(t) * num_segments);
     const int V = a.H / 16;                           // 16-byte vectors of codes per row
     const int nb = a.H / 128;
-    const int row = slot_row(a.row_of_slot, t, a.K, lane);
     const int4* src = reinterpret_cast<const int4*>(a.x) + static_cast<int64_t>(t) * V;
     int4* dst = reinterpret_cast<int4*>(a.recv_x);
     const int j0 = seg * (32 * kBf16Unroll) + lane;
@@ -206,6 +212,8 @@ dispatch_fp8_passthrough_kernel(DispatchArgs a, int64_t num_items, int num_segme
         if (j < V) v[u] = ld_stream(src + j);
     }
     const bool ue = a.scale_mode == EP_SCALE_UE8M0;
+    wait_for_layout();
+    const int row = slot_row(a.row_of_slot, t, a.K, lane);
     if (seg == 0) write_side_outputs(a, t, lane, row);
     for (int k = 0; k < a.K; ++k) {
         const int r = __shfl_sync(kFullMask, row, k);
@@ -255,6 +263,23 @@ fill_pad_rows_kernel(const int32_t* counts, const int32_t* offsets, int E, int m
     }
 }
 
+// Launch, as a programmatic dependent of the preceding grid when asked: its
+// blocks may then start (and load x) while the layout is still running.
+template <typename... Params, typename... Args>
+cudaError_t launch_dispatch_kernel(bool overlap, void (*kernel)(Params...), unsigned blocks, cudaStream_t stream,
+                                   Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(kWarpsPerBlock * 32);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = overlap ? &attr : nullptr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch_bf16(const DispatchArgs& a, cudaStream_t stream) {
@@ -264,8 +289,8 @@ cudaError_t launch_dispatch_bf16(const DispatchArgs& a, cudaStream_t stream) {
     const int64_t items = static_cast<int64_t>(a.T) * segs;
     if (items == 0) return cudaSuccess;
     const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    dispatch_bf16_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a, items, segs);
-    return cudaGetLastError();
+    return launch_dispatch_kernel(a.overlap_layout != 0, dispatch_bf16_kernel, static_cast<unsigned>(blocks), stream,
+                                  a, items, segs);
 }
 
 cudaError_t launch_fill_pad_rows(const int32_t* counts, const int32_t* offsets, int E, int64_t row_bytes,
@@ -286,11 +311,10 @@ cudaError_t launch_dispatch_fp8_passthrough(const DispatchArgs& a, cudaStream_t 
     const int64_t items = static_cast<int64_t>(a.T) * segs;
     if (items == 0) return cudaSuccess;
     const unsigned g = static_cast<unsigned>((items + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    const bool ov = a.overlap_layout != 0;
     if (a.scale_col_major)
-        dispatch_fp8_passthrough_kernel<true><<<g, kWarpsPerBlock * 32, 0, stream>>>(a, items, segs);
-    else
-        dispatch_fp8_passthrough_kernel<false><<<g, kWarpsPerBlock * 32, 0, stream>>>(a, items, segs);
-    return cudaGetLastError();
+        return launch_dispatch_kernel(ov, dispatch_fp8_passthrough_kernel<true>, g, stream, a, items, segs);
+    return launch_dispatch_kernel(ov, dispatch_fp8_passthrough_kernel<false>, g, stream, a, items, segs);
 }
 
 cudaError_t launch_dispatch_fp8(const DispatchArgs& a, cudaStream_t stream) {
@@ -301,19 +325,15 @@ cudaError_t launch_dispatch_fp8(const DispatchArgs& a, cudaStream_t stream) {
     if (items == 0) return cudaSuccess;
     const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
     const unsigned g = static_cast<unsigned>(blocks);
-    const int tpb = kWarpsPerBlock * 32;
-    const bool col = a.scale_col_major != 0;
-    if (a.scale_mode == EP_SCALE_POW2) {
-        if (col) dispatch_fp8_kernel<EP_SCALE_POW2, true><<<g, tpb, 0, stream>>>(a, items, segs);
-        else dispatch_fp8_kernel<EP_SCALE_POW2, false><<<g, tpb, 0, stream>>>(a, items, segs);
-    } else if (a.scale_mode == EP_SCALE_UE8M0) {
-        if (col) dispatch_fp8_kernel<EP_SCALE_UE8M0, true><<<g, tpb, 0, stream>>>(a, items, segs);
-        else dispatch_fp8_kernel<EP_SCALE_UE8M0, false><<<g, tpb, 0, stream>>>(a, items, segs);
-    } else {
-        if (col) dispatch_fp8_kernel<EP_SCALE_FP32, true><<<g, tpb, 0, stream>>>(a, items, segs);
-        else dispatch_fp8_kernel<EP_SCALE_FP32, false><<<g, tpb, 0, stream>>>(a, items, segs);
-    }
-    return cudaGetLastError();
+    const bool col = a.scale_col_major != 0, ov = a.overlap_layout != 0;
+    if (a.scale_mode == EP_SCALE_POW2)
+        return col ? launch_dispatch_kernel(ov, dispatch_fp8_kernel<EP_SCALE_POW2, true>, g, stream, a, items, segs)
+                   : launch_dispatch_kernel(ov, dispatch_fp8_kernel<EP_SCALE_POW2, false>, g, stream, a, items, segs);
+    if (a.scale_mode == EP_SCALE_UE8M0)
+        return col ? launch_dispatch_kernel(ov, dispatch_fp8_kernel<EP_SCALE_UE8M0, true>, g, stream, a, items, segs)
+                   : launch_dispatch_kernel(ov, dispatch_fp8_kernel<EP_SCALE_UE8M0, false>, g, stream, a, items, segs);
+    return col ? launch_dispatch_kernel(ov, dispatch_fp8_kernel<EP_SCALE_FP32, true>, g, stream, a, items, segs)
+               : launch_dispatch_kernel(ov, dispatch_fp8_kernel<EP_SCALE_FP32, false>, g, stream, a, items, segs);
 }
 
 }  // namespace ep

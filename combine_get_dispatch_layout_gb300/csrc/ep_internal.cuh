@@ -75,6 +75,7 @@ struct DispatchArgs {
     int scale_col_major;       // 0: scales [rows, H/128]; 1: [H/128, scale_ld]
     int64_t scale_ld;
     const void* x_scales;      // fp8 input: [T, H/128] fp32 (uint8 in UE8M0 mode)
+    int overlap_layout;        // launch as the preceding layout's programmatic dependent
 };
 
 cudaError_t launch_dispatch_bf16(const DispatchArgs& a, cudaStream_t stream);

@@ -239,6 +239,7 @@ layout_scan_kernel(LayoutPlan p, LayoutArgs a) {
 
 __global__ void __launch_bounds__(256)
 layout_assign_kernel(LayoutPlan p, LayoutArgs a) {
+    asm volatile("griddepcontrol.launch_dependents;");
     extern __shared__ int smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int* offs = smem;                                  // [E] exclusive expert offsets
@@ -350,6 +351,9 @@ __device__ __forceinline__ unsigned rank_of(unsigned e, const LayoutPlan& p) {
 // holds the token rank masks (R <= 32) and later the offsets and CTA bases.
 __global__ void __launch_bounds__(1024, 1)
 layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
+    // a dispatch launched as this grid's dependent may start on idle SMs now;
+    // it reads the slot map only after this grid has finished
+    asm volatile("griddepcontrol.launch_dependents;");
     extern __shared__ int smem[];
     __shared__ int s_over;
     cg::cluster_group cluster = cg::this_cluster();

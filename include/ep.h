@@ -82,6 +82,12 @@ typedef struct {
     int scale_mode;        /* ep_scale_mode_t for fp8 output (and the x_scales type)      */
     int scales_col_major;  /* 0: recv_scales [cap, H/128]; 1: [H/128, scales_ld]          */
     int64_t scales_ld;     /* rows of the column-major scale matrix (>= recv_capacity)    */
+    int overlap_layout;    /* 1: the caller enqueues this dispatch directly after the
+                              ep_layout* call that built the handle, on the same stream,
+                              with x complete before that layout was enqueued; the
+                              dispatch then starts on the SMs the layout leaves idle and
+                              loads x while the layout runs (programmatic dependent
+                              launch). 0: ordinary stream order.                      */
 } ep_dispatch_config_t;
 
 /* Opaque routing handle: owns the slot -> row map [T*K] int32, the layout

@@ -985,3 +985,31 @@ def test_nonexpand_duplicate_experts_and_invalid_ids(ep):
     assert ep.ep_handle_query(h)[1] == ep.EP_ERR_INVALID_EXPERT
     np.testing.assert_array_equal(o[3].cpu().numpy(), ref["rank_offsets"])
     h.destroy()
+
+
+@pytest.mark.parametrize("name,fp8", [("prefill", False), ("fp8", True), ("decode", False)])
+def test_dispatch_overlapping_the_layout(ep, name, fp8):
+    """Dispatch launched as the layout's programmatic dependent gives the same bytes."""
+    inp = gi.make(name, 19, with_y=False)
+    w = inp.w
+    ref = oracle.layout(inp.topk_idx, w.E, w.R)
+    n = int(ref["expert_offsets"][-1])
+    idx, x = _dev(inp.topk_idx), _dev(inp.x.view(np.int16))
+    o = [torch.empty(w.E, dtype=torch.int32, device="cuda"), torch.empty(w.R, dtype=torch.int32, device="cuda"),
+         torch.empty(w.T, w.R, dtype=torch.uint8, device="cuda"), torch.empty(w.E + 1, dtype=torch.int32, device="cuda")]
+    h = ep.ep_layout(idx, w.E, w.R, *o)
+    recv = torch.full((n, w.H), SENT8 if fp8 else SENT16, dtype=torch.uint8 if fp8 else torch.int16, device="cuda")
+    sc = torch.full((n, w.H // 128), -1.0, dtype=torch.float32, device="cuda") if fp8 else None
+    for _ in range(3):   # repeated layout -> dispatch pairs on one stream
+        ep.ep_layout(idx, w.E, w.R, *o, handle=h)
+        ep.ep_dispatch_ex(h, x, recv, n, out_dtype=ep.EP_DTYPE_FP8_E4M3 if fp8 else ep.EP_DTYPE_BF16,
+                          recv_scales=sc, overlap_layout=True)
+    torch.cuda.synchronize()
+    if fp8:
+        r_q, r_s, _, _ = oracle.dispatch_e4m3(inp.x, ref["row_of_slot"], n)
+        np.testing.assert_array_equal(recv.cpu().numpy(), r_q)
+        np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint32), r_s.view(np.uint32))
+    else:
+        r_x, _, _ = oracle.dispatch_bf16(inp.x, ref["row_of_slot"], n)
+        np.testing.assert_array_equal(recv.cpu().numpy().view(np.uint16), r_x)
+    h.destroy()
