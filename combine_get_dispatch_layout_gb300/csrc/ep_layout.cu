@@ -412,6 +412,7 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
             if (key >= 0) {
                 loc = mine[key] + __popc(peers & lt);
                 if (small_r) {
+                    // (a butterfly OR over each token's lane group measured slower)
                     const int tl = static_cast<int>((s0 + (j0 + j) * 32 + lane) / p.K) - t0;
                     atomicOr(my_mask + tl, 1u << rank_of(static_cast<unsigned>(key), p));
                 }
@@ -477,6 +478,7 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
     // ---- phase 2: per-warp bases inside the CTA; push this CTA's totals,
     // rank counts and error flag into every CTA of the cluster
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // all CTAs have started
+    int* own_tot = all_tot + cta * E;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int run = 0;
         for (int w0 = 0; w0 < W; w0 += 8) {   // W is a multiple of 8
@@ -489,16 +491,30 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
                 run += c[i];
             }
         }
-#pragma unroll
-        for (int c = 0; c < kMaxClusterCtas; ++c)
-            if (c < C) *cluster.map_shared_rank(all_tot + cta * E + e, c) = run;
+        own_tot[e] = run;
     }
-    for (int i = threadIdx.x; i < R + 1; i += blockDim.x) {
-        const int v = i < R ? rank_acc[i] : all_bad[cta];
-#pragma unroll
-        for (int c = 0; c < kMaxClusterCtas; ++c)
-            if (c < C && c != cta)
-                *cluster.map_shared_rank(i < R ? all_rank + cta * R + i : all_bad + cta, c) = v;
+    __syncthreads();
+    // push this CTA's row of totals into every peer: one remote store per
+    // (piece, peer), 16-byte pieces when E % 4 == 0
+    if (E % 4 == 0) {
+        const int pieces = E / 4;
+        for (int i = threadIdx.x; i < pieces * C; i += blockDim.x) {
+            const int c = i / pieces, q = i - c * pieces;
+            if (c == cta) continue;
+            const int4 v = reinterpret_cast<const int4*>(own_tot)[q];
+            *reinterpret_cast<int4*>(cluster.map_shared_rank(own_tot + 4 * q, c)) = v;
+        }
+    } else {
+        for (int i = threadIdx.x; i < E * C; i += blockDim.x) {
+            const int c = i / E, e = i - c * E;
+            if (c != cta) *cluster.map_shared_rank(own_tot + e, c) = own_tot[e];
+        }
+    }
+    for (int i = threadIdx.x; i < (R + 1) * C; i += blockDim.x) {
+        const int c = i / (R + 1), k = i - c * (R + 1);
+        if (c == cta) continue;
+        if (k < R) *cluster.map_shared_rank(all_rank + cta * R + k, c) = rank_acc[k];
+        else *cluster.map_shared_rank(all_bad + cta, c) = all_bad[cta];
     }
     // Every push lands before any CTA passes this barrier (release/acquire at
     // cluster scope), and nothing touches another CTA's shared memory after
@@ -524,14 +540,16 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
             if (a.h_counts) a.h_counts[e] = total;
         }
     }
-    if (cta == 0)
+    // CTA 0 writes the expert offsets below; the last CTA takes the rank
+    // totals and the error word so that no CTA carries both
+    if (cta == C - 1)
         for (int r = threadIdx.x; r < R; r += blockDim.x) {
             int total = 0;
             for (int c = 0; c < C; ++c) total += all_rank[c * R + r];
             a.num_tokens_per_rank[r] = total;
         }
     __syncthreads();
-    if (cta == 0 && threadIdx.x == 0) {
+    if (cta == C - 1 && threadIdx.x == 0) {
         int bad = 0;
         for (int c = 0; c < C; ++c) bad |= all_bad[c];
         a.meta[kMetaError] = bad ? EP_ERR_INVALID_EXPERT : (s_over ? EP_ERR_CAPACITY : 0);
