@@ -92,3 +92,75 @@ def test_product_never_touches_the_oracle():
         if f.endswith((".py", ".c", ".h")):
             src = open(os.path.join(ROOT, "oracle", f)).read()
             assert "combine_get_dispatch_layout_gb300" not in src and "libep" not in src
+
+
+def _handle_ptr():
+    return ctypes.byref(ctypes.c_void_p(None))
+
+
+@pytest.mark.parametrize("align", [0, -3, 1025])
+def test_layout_aligned_rejects_bad_alignment(L, align):
+    assert L.ep_layout_aligned(16, 4, 2, 8, 2, align, 32, 32, 32, 32, None, None, _handle_ptr(), None) == 1
+
+
+def test_layout_aligned_rejects_rows_past_int32(L):
+    # T*K = 2^31 - 8 is allowed alone, but T*K + E*(A-1) >= 2^31
+    assert L.ep_layout_aligned(16, (1 << 28) - 1, 8, 4096, 1, 1024, 32, 32, 32, 32, None, None, _handle_ptr(),
+                               None) == 1
+
+
+@pytest.mark.parametrize("cap", [0, -1])
+def test_layout_strided_rejects_bad_capacity(L, cap):
+    assert L.ep_layout_strided(16, 4, 2, 8, 2, cap, 32, 32, 32, 32, None, None, _handle_ptr(), None) == 1
+
+
+def test_layout_strided_rejects_rows_past_int32(L):
+    assert L.ep_layout_strided(16, 4, 2, 4096, 2, 1 << 20, 32, 32, 32, 32, None, None, _handle_ptr(), None) == 1
+
+
+def test_layout_nonexpand_rejects_bad_args(L):
+    assert L.ep_layout_nonexpand(16, 4, 2, 6, 4, 32, 32, 32, 32, None, None, _handle_ptr(), None) == 1  # E % R
+    assert L.ep_layout_nonexpand(16, 4, 2, 8, 2, 32, 32, 32, 32, None, None, None, None) == 1           # no handle
+
+
+def test_new_calls_reject_null_handle(L):
+    import combine_get_dispatch_layout_gb300 as ep
+    cfg = ep.DispatchConfig()
+    assert L.ep_dispatch_ex(None, 16, None, 128, ctypes.byref(cfg), None, 16, None, None, None, 8, None) == 1
+    assert L.ep_combine_backward(None, 16, 16, 8, 128, None, 16, 8, None, None) == 1
+    assert L.ep_dispatch_backward(None, 16, 8, 128, None, 16, None, None) == 1
+    assert L.ep_nonexpand_recv_topk(None, 16, None, 8, 16, None, 8, None) == 1
+    assert L.ep_handle_layout_kernels(None) == -1
+
+
+@pytest.mark.parametrize("args", [
+    (16, None, 4, 0, 8),        # K = 0
+    (16, None, 4, 33, 8),       # K > 32
+    (16, None, 4, 2, 0),        # E = 0
+    (16, None, -1, 2, 8),       # T < 0
+    (None, None, 4, 2, 8),      # topk_idx missing
+    (12, None, 4, 2, 8),        # topk_idx not 8-byte aligned
+])
+def test_topk_to_routing_map_rejects_bad_args(L, args):
+    idx, w, T, K, E = args
+    assert L.ep_topk_to_routing_map(idx, w, T, K, E, 64, None, None, None) == 1
+
+
+def test_topk_to_routing_map_probs_need_weights(L):
+    assert L.ep_topk_to_routing_map(16, None, 4, 2, 8, 64, 64, None, None) == 1
+
+
+@pytest.mark.parametrize("args", [(64, 4, 8, 0), (64, 4, 0, 2), (None, 4, 8, 2), (64, -1, 8, 2)])
+def test_routing_map_to_topk_rejects_bad_args(L, args):
+    rm, T, E, K = args
+    assert L.ep_routing_map_to_topk(rm, None, T, E, K, 16, None, None, None) == 1
+
+
+def test_dispatch_config_struct_matches_header():
+    """The binding's ep_dispatch_config_t mirror has the header's field order and size."""
+    import combine_get_dispatch_layout_gb300 as ep
+    src = open(os.path.join(ROOT, "include", "ep.h")).read()
+    body = src[src.index("typedef struct {", src.index("ep_scale_mode_t;")):src.index("} ep_dispatch_config_t;")]
+    fields = re.findall(r"^\s*(?:int|int64_t)\s+(\w+);", body, flags=re.M)
+    assert fields == [f for f, _ in ep.DispatchConfig._fields_]
+    assert ctypes.sizeof(ep.DispatchConfig) == 32
