@@ -1013,3 +1013,36 @@ def test_dispatch_overlapping_the_layout(ep, name, fp8):
         r_x, _, _ = oracle.dispatch_bf16(inp.x, ref["row_of_slot"], n)
         np.testing.assert_array_equal(recv.cpu().numpy().view(np.uint16), r_x)
     h.destroy()
+
+
+def test_fp8_quotients_near_e4m3_midpoints(ep):
+    """Inputs whose x / scale lands within a few fp32 ulps of an e4m3 rounding
+    midpoint (where a reciprocal-multiply could round differently from the
+    IEEE quotient) still give the oracle's bytes."""
+    rng = np.random.default_rng(23)
+    xs_all = gi.bf16_bits_to_f32(np.arange(0x3c00, 0x7f00, dtype=np.uint16))   # positive normals
+    blocks = []
+    for amax_bits in rng.integers(0x3f80, 0x4700, 400).astype(np.uint16):
+        amax = gi.bf16_bits_to_f32(np.array([amax_bits], np.uint16))[0]
+        s = np.float32(amax) / np.float32(448.0)
+        xs = xs_all[xs_all <= amax]
+        q = (xs / s).astype(np.float32)
+        m = (q.view(np.uint32) & 0xFFFFF).astype(np.int64) - 0x80000
+        pick = xs[(np.abs(m) <= 8) & (q >= 2.0 ** -6)]
+        for i in range(0, len(pick), 127):
+            chunk = pick[i:i + 127]
+            sign = np.where(rng.random(len(chunk)) < 0.5, -1.0, 1.0).astype(np.float32)
+            blk = np.zeros(128, np.float32)
+            blk[:len(chunk)] = chunk * sign
+            blk[127] = amax
+            blocks.append(blk)
+    assert len(blocks) >= 8, "the search should find near-midpoint quotients"
+    nb = (len(blocks) + 7) // 8 * 8
+    allb = np.zeros((nb, 128), np.float32)
+    allb[:len(blocks)] = np.stack(blocks)
+    H = 1024
+    x = gi.f32_to_bf16_bits(allb.reshape(nb // 8, H))
+    T = x.shape[0]
+    inp = gi.Inputs(w=_workload(T, H, 1, 1, 1), seed=0, x=x, topk_idx=np.zeros((T, 1), np.int64),
+                    topk_weights=np.ones((T, 1), np.float32), y=None, num_valid=T)
+    full_path(ep, inp, fp8=True)
