@@ -88,6 +88,12 @@ def _lib():
             L.orc_f32_to_e4m3.restype = ctypes.c_uint8
             L.orc_e4m3_to_f32.argtypes = [ctypes.c_uint8]
             L.orc_e4m3_to_f32.restype = ctypes.c_float
+            L.orc_f32_to_e5m2_array.argtypes = [P, i64, P]
+            L.orc_e5m2_sweep.argtypes = [ctypes.c_uint32, ctypes.c_uint32, P]
+            L.orc_e5m2_to_f32.argtypes = [ctypes.c_uint8]
+            L.orc_e5m2_to_f32.restype = ctypes.c_float
+            L.orc_quant_row_e5m2.argtypes = [P, i32, i32, P, P, P]
+            L.orc_quant_row_e5m2.restype = None
             _LIB = L
     return _LIB
 
@@ -266,6 +272,31 @@ def dispatch_e4m3_pow2(x: np.ndarray, row_of_slot: np.ndarray, num_rows: int, ue
     return rq, rs
 
 
+def quant_row_e5m2(xrow: np.ndarray, scale_mode: int = 0):
+    """(codes [H] u8, scales [H/128]): fp32 scales for scale_mode 0 (amax/57344)
+    and 1 (its power-of-two ceiling), u8 exponent bytes for scale_mode 2."""
+    xrow = _c(xrow, np.uint16)
+    H = xrow.shape[0]
+    q = np.zeros(H, np.uint8)
+    s = np.zeros(H // 128, np.uint8 if scale_mode == 2 else np.float32)
+    if scale_mode == 2:
+        _lib().orc_quant_row_e5m2(_p(xrow), H, 2, _p(q), None, _p(s))
+    else:
+        _lib().orc_quant_row_e5m2(_p(xrow), H, scale_mode, _p(q), _p(s), None)
+    return q, s
+
+
+def dispatch_e5m2(x: np.ndarray, row_of_slot: np.ndarray, num_rows: int, scale_mode: int = 0):
+    """e5m2 quantise-permute: (codes [rows, H], scales [rows, H/128])."""
+    x = _c(x, np.uint16)
+    T, H = x.shape
+    q = np.zeros((T, H), np.uint8)
+    s = np.zeros((T, H // 128), np.uint8 if scale_mode == 2 else np.float32)
+    for t in range(T):
+        q[t], s[t] = quant_row_e5m2(x[t], scale_mode)
+    return dispatch_rows(q, row_of_slot, num_rows), dispatch_rows(s, row_of_slot, num_rows)
+
+
 def dispatch_rows(src: np.ndarray, row_of_slot: np.ndarray, num_rows: int, fill: int = 0) -> np.ndarray:
     """Byte permute of rows of any dtype: out[row_of_slot[t,k]] = src[t]."""
     src = np.ascontiguousarray(src)
@@ -382,4 +413,23 @@ def e4m3_sweep(lo: int, hi: int) -> np.ndarray:
 def e4m3_to_f32(q: np.ndarray) -> np.ndarray:
     L = _lib()
     return np.array([L.orc_e4m3_to_f32(int(v)) for v in np.asarray(q).ravel()],
+                    np.float32).reshape(np.shape(q))
+
+
+def f32_to_e5m2(a: np.ndarray) -> np.ndarray:
+    a = _c(a, np.float32)
+    out = np.zeros(a.shape, np.uint8)
+    _lib().orc_f32_to_e5m2_array(_p(a), a.size, _p(out))
+    return out
+
+
+def e5m2_sweep(lo: int, hi: int) -> np.ndarray:
+    out = np.zeros(hi - lo, np.uint8)
+    _lib().orc_e5m2_sweep(lo, hi, _p(out))
+    return out
+
+
+def e5m2_to_f32(q: np.ndarray) -> np.ndarray:
+    L = _lib()
+    return np.array([L.orc_e5m2_to_f32(int(v)) for v in np.asarray(q).ravel()],
                     np.float32).reshape(np.shape(q))

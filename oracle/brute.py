@@ -112,11 +112,33 @@ def e4m3_values() -> tuple[np.ndarray, np.ndarray]:
 
 def e4m3_encode(v: np.ndarray) -> np.ndarray:
     """Nearest finite code (ties to the even code), saturating; -0 keeps its sign."""
-    codes, vals = e4m3_values()
+    return _nearest_code(v, *e4m3_values(), 448.0)
+
+
+def e5m2_values() -> tuple[np.ndarray, np.ndarray]:
+    """(codes, values) of the 248 finite OCP E5M2 codes, decoded from their bits
+    (exponent field 31 holds the infinities and NaNs)."""
+    codes, vals = [], []
+    for c in range(256):
+        s, f, m = c >> 7, (c >> 2) & 31, c & 3
+        if f == 31:
+            continue
+        v = m * 2.0 ** -16 if f == 0 else (1 + m / 4) * 2.0 ** (f - 15)
+        codes.append(c)
+        vals.append(-v if s else v)
+    return np.array(codes, np.uint8), np.array(vals, np.float64)
+
+
+def e5m2_encode(v: np.ndarray) -> np.ndarray:
+    """Nearest finite e5m2 code (ties to the even code), saturating at 57344."""
+    return _nearest_code(v, *e5m2_values(), 57344.0)
+
+
+def _nearest_code(v, codes, vals, vmax) -> np.ndarray:
     v = np.asarray(v, np.float64).ravel()
     out = np.empty(v.shape, np.uint8)
     for i, x in enumerate(v):
-        xs = min(max(x, -448.0), 448.0)
+        xs = min(max(x, -vmax), vmax)
         d = np.abs(vals - xs)
         best = d.min()
         cand = codes[d == best]

@@ -106,6 +106,51 @@ float orc_e4m3_to_f32(uint8_t q) {
     return (float)(s ? -v : v);
 }
 
+/* OCP FP8 E5M2: 1 sign, 5 exponent (bias 15), 2 mantissa bits, laid out
+ * like an IEEE format: exponent field 31 holds infinity (mantissa 0) and NaN,
+ * so the largest finite is S.11110.11 = 1.75 * 2^15 = 57344.
+ * Normal values (exponent field 1..30): 2^(e-15) * (1 + m/4).
+ * Subnormals (exponent field 0): m * 2^-16.
+ * Encoding rounds to nearest, ties to even, and saturates anything beyond
+ * 57344 to +-57344 (satfinite, as for e4m3). Zero keeps its sign.
+ * nccl_ep.cc (ncclTypeSize, ncclEpDispatch) accepts it beside e4m3 as a
+ * one-byte fp8 token type. */
+uint8_t orc_f32_to_e5m2(float f) {
+    if (isnan(f)) return 0x7F;
+    uint8_t sign = signbit(f) ? 0x80 : 0x00;
+    double a = fabs((double)f);
+    if (a >= 57344.0) return (uint8_t)(sign | 0x7B);
+    if (a < ldexp(1.0, -14)) {
+        /* subnormal range: steps of 2^-16, half to even; 4 steps is 2^-14,
+         * the smallest normal, whose code is 0x04 */
+        double m = rint(a * 65536.0);
+        return (uint8_t)(sign | (uint8_t)m);
+    }
+    int ex;
+    (void)frexp(a, &ex);
+    int E = ex - 1;                    /* a in [2^E, 2^(E+1)) */
+    double m = rint(ldexp(a, 2 - E));  /* 4..8 mantissa steps of 2^(E-2) */
+    if (m >= 8.0) { m = 4.0; E += 1; }
+    int code = ((E + 15) << 2) | ((int)m - 4);
+    if (code > 0x7B) code = 0x7B;
+    return (uint8_t)(sign | code);
+}
+
+/* E5M2 byte -> value. */
+float orc_e5m2_to_f32(uint8_t q) {
+    int s = q >> 7, field = (q >> 2) & 0x1F, m = q & 3;
+    double v;
+    if (field == 0x1F) {
+        if (m != 0) return NAN;
+        v = INFINITY;
+    } else if (field == 0) {
+        v = ldexp((double)m, -16);
+    } else {
+        v = ldexp(1.0 + m / 4.0, field - 15);
+    }
+    return (float)(s ? -v : v);
+}
+
 /* ---------------------------------------------------------------- layout */
 
 /* Routing layout from topk_idx [T, K] (int64, -1 = unused slot).
@@ -426,6 +471,56 @@ void orc_quant_row_e4m3_pow2(const uint16_t* xrow, int H, int ue8m0, uint8_t* qr
         }
         for (int i = 0; i < 128; ++i)
             qrow[b * 128 + i] = orc_f32_to_e4m3(orc_bf16_to_f32(xrow[b * 128 + i]) / scale);
+    }
+}
+
+/* Quantise one row to e5m2 with one scale per 128 channels, the e4m3 recipe
+ * with e5m2's largest finite value in place of 448:
+ *   s = amax / 57344 (fp32 division);
+ *   scale_mode 0: scale = s, stored as fp32;
+ *   scale_mode 1: scale = smallest power of two >= s, stored as fp32;
+ *   scale_mode 2: that power raised to at least 2^-127, stored as its biased
+ *                 exponent byte in sbytes[b];
+ *   q = e5m2_rne_satfinite(x / scale).
+ * An all-zero block gives zero codes and scale 0 (byte 0). */
+void orc_quant_row_e5m2(const uint16_t* xrow, int H, int scale_mode, uint8_t* qrow, float* srow,
+                        uint8_t* sbytes) {
+    for (int b = 0; b < H / 128; ++b) {
+        float amax = 0.0f;
+        for (int i = 0; i < 128; ++i) {
+            float v = fabsf(orc_bf16_to_f32(xrow[b * 128 + i]));
+            if (v > amax) amax = v;
+        }
+        if (amax == 0.0f) {
+            if (scale_mode == 2) sbytes[b] = 0; else srow[b] = 0.0f;
+            for (int i = 0; i < 128; ++i) qrow[b * 128 + i] = 0x00;
+            continue;
+        }
+        float scale = amax / 57344.0f;
+        if (scale_mode != 0) scale = orc_pow2_ceil(scale);
+        if (scale_mode == 2) {
+            if (scale < ldexpf(1.0f, -127)) scale = ldexpf(1.0f, -127);
+            int ex;
+            (void)frexpf(scale, &ex);          /* scale = 2^(ex-1) */
+            sbytes[b] = (uint8_t)(ex - 1 + 127);
+        } else {
+            srow[b] = scale;
+        }
+        for (int i = 0; i < 128; ++i)
+            qrow[b * 128 + i] = orc_f32_to_e5m2(orc_bf16_to_f32(xrow[b * 128 + i]) / scale);
+    }
+}
+
+void orc_f32_to_e5m2_array(const float* in, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_e5m2(in[i]);
+}
+
+/* Sweep fp32 bit patterns [lo, hi) through the e5m2 encoder (no input array). */
+void orc_e5m2_sweep(uint32_t lo, uint32_t hi, uint8_t* out) {
+    for (uint32_t u = lo; u < hi; ++u) {
+        float f;
+        memcpy(&f, &u, sizeof f);
+        out[u - lo] = orc_f32_to_e5m2(f);
     }
 }
 

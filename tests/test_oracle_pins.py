@@ -482,6 +482,127 @@ def test_fp8_pow2_closed_forms():
             np.testing.assert_array_equal(qu[b*128:(b+1)*128], want_u)
 
 
+# ------------------------------------------------------------------ e5m2
+
+def _torch_e5m2_bits(f32):
+    t = torch.from_numpy(np.ascontiguousarray(f32, np.float32)).clamp(-57344.0, 57344.0)
+    return t.to(torch.float8_e5m2).view(torch.uint8).numpy()
+
+
+def _e5m2_rounding_patterns():
+    """All sign/exponent/top-2-mantissa combinations with low bits at and
+    around e5m2's rounding midpoint (bit 20) and its subnormal midpoints."""
+    hi = np.arange(1 << 11, dtype=np.uint32) << np.uint32(21)
+    lows = np.array([0, 1, 0xFFFFF, 0x100000, 0x100001, 0x1FFFFF, 0x80000, 0x180000, 0x7FFFF, 0x40000],
+                    np.uint32)
+    f = (hi[:, None] | lows[None, :]).ravel().view(np.float32)
+    return f[np.isfinite(f)]
+
+
+def test_e5m2_encoder_vs_torch():
+    rng = np.random.default_rng(21)
+    f = np.concatenate([_e5m2_rounding_patterns(),
+                        rng.integers(0, 2**32, 2_000_000, dtype=np.uint64).astype(np.uint32).view(np.float32),
+                        (rng.standard_normal(500_000) * 3e4).astype(np.float32),
+                        (rng.standard_normal(500_000) * 1e-4).astype(np.float32)])
+    f = f[np.isfinite(f)]
+    np.testing.assert_array_equal(oracle.f32_to_e5m2(f), _torch_e5m2_bits(f))
+
+
+def test_e5m2_encoder_vs_brute_search():
+    rng = np.random.default_rng(22)
+    codes, vals = brute.e5m2_values()
+    sv = np.sort(vals)
+    mids = (sv[1:] + sv[:-1]) / 2
+    f = np.concatenate([vals, mids, mids * (1 + 2**-20), mids * (1 - 2**-20),
+                        [60000.0, 61440.0, -1e30, 57344.0 * (1 + 2**-20), -0.0, 2.0**-17, 2.0**-18],
+                        rng.standard_normal(3000) * 4000]).astype(np.float32)
+    np.testing.assert_array_equal(oracle.f32_to_e5m2(f), brute.e5m2_encode(f))
+
+
+def test_e5m2_decode_all_codes():
+    codes, vals = brute.e5m2_values()
+    np.testing.assert_array_equal(oracle.e5m2_to_f32(codes).astype(np.float64), vals)
+    np.testing.assert_array_equal(oracle.f32_to_e5m2(vals.astype(np.float32)), codes)
+    allc = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(allc).view(torch.float8_e5m2).float().numpy()
+    got = oracle.e5m2_to_f32(allc)
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    np.testing.assert_array_equal(got[ok], want[ok])
+
+
+def _hand_values(tokens, n):
+    x = np.zeros(n, np.float32)
+    for kv in tokens:
+        i, v = kv.split(":")
+        x[int(i)] = float.fromhex(v) if "p" in v else float(v)
+    return x
+
+
+def _hand_codes(tokens, n):
+    q = np.zeros(n, np.uint8)
+    for kv in tokens:
+        i, v = kv.split(":")
+        q[int(i)] = int(v, 16)
+    return q
+
+
+def test_fp8_e5m2_golden(golden):
+    g = golden("fp8_e5m2_hand.txt")
+    x = _hand_values(g["x"], 256)
+    xb = gi.f32_to_bf16_bits(x)
+    assert (gi.bf16_bits_to_f32(xb) == x).all(), "fixture values must be bf16-exact"
+    for mode, skey, qkey in [(0, "scale_fp32_bits", "q_fp32"), (1, "scale_pow2_bits", "q_pow2")]:
+        q, s = oracle.quant_row_e5m2(xb, mode)
+        np.testing.assert_array_equal(s.view(np.uint32), _ints(g[skey]).astype(np.uint32))
+        np.testing.assert_array_equal(q, _hand_codes(g[qkey], 256))
+    q, sb = oracle.quant_row_e5m2(xb, 2)
+    np.testing.assert_array_equal(sb, _ints(g["ue8m0"]))
+    np.testing.assert_array_equal(q, _hand_codes(g["q_pow2"], 256))
+
+
+def test_e5m2_quant_closed_forms():
+    """Block max -> +-57344 with fp32 scales; dequantisation within half an
+    e5m2 step; power-of-two scales minimal, their codes torch's exact cast."""
+    rng = np.random.default_rng(23)
+    H = 1024
+    xf = (rng.standard_normal((48, H)) * 3).astype(np.float32)
+    xf[0, :128] = 0.0
+    xf[1, 128:256] = 1e-39                     # bf16 subnormals
+    xf[2, 256:384] = np.float32(2.0 ** -133)   # the smallest bf16 subnormal
+    xf[3, 384:512] = 3e38
+    xf[4, ::3] *= 1e5
+    xb = gi.f32_to_bf16_bits(xf)
+    xv = gi.bf16_bits_to_f32(xb).reshape(48, H // 128, 128).astype(np.float64)
+    for t in range(48):
+        q, s = oracle.quant_row_e5m2(xb[t], 0)
+        qp, sp = oracle.quant_row_e5m2(xb[t], 1)
+        qu, su = oracle.quant_row_e5m2(xb[t], 2)
+        for b in range(H // 128):
+            blk = xv[t, b]
+            qb, qpb, qub = (a[b * 128:(b + 1) * 128] for a in (q, qp, qu))
+            amax = np.abs(blk).max()
+            if amax == 0:
+                assert s[b] == 0 and sp[b] == 0 and su[b] == 0
+                assert not qb.any() and not qpb.any() and not qub.any()
+                continue
+            i = int(np.argmax(np.abs(blk)))
+            assert qb[i] & 0x7F == 0x7B                     # the block max saturates the format
+            dq = oracle.e5m2_to_f32(qb).astype(np.float64) * np.float64(s[b])
+            # half a step: 2^-3 relative for normals; half the subnormal step
+            # 2^-16 times the scale; plus fp32 rounding of x / s near 57344
+            bound = 2.0 ** -3 * np.abs(blk) + 2.0 ** -17 * float(s[b]) + 2.0 ** -20 * amax
+            assert (np.abs(dq - blk) <= bound).all()
+            s0 = np.float64(np.float32(amax) / np.float32(57344.0))
+            m, _ = np.frexp(np.float64(sp[b]))
+            assert m == 0.5 and sp[b] >= s0 and sp[b] / 2 < s0
+            np.testing.assert_array_equal(qpb, _torch_e5m2_bits((blk / np.float64(sp[b])).astype(np.float32)))
+            ue = max(float(sp[b]), 2.0 ** -127)
+            assert su[b] == int(np.log2(ue)) + 127
+            np.testing.assert_array_equal(qub, _torch_e5m2_bits((blk / ue).astype(np.float32)))
+
+
 def test_dispatch_rows_moves_any_row_type():
     idx = _random_routing(np.random.default_rng(6), 30, 3, 8, 0.2, True, 0.0)
     L = oracle.layout(idx, 8, 2)
