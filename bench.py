@@ -323,6 +323,8 @@ def gpu_arm(args, rank, world, local):
                                                     scales_col_major=True, scales_ld=n8, stream=stream))
     ms_pass = time_variant(lambda: ep.ep_dispatch_ex(h8, codes_in, q, n8, in_dtype=ep.EP_DTYPE_FP8_E4M3,
                                                      x_scales=scales_in, recv_scales=sc, H=H, stream=stream))
+    ms_e5m2 = time_variant(lambda: ep.ep_dispatch_ex(h8, x8, q, n8, out_dtype=ep.EP_DTYPE_FP8_E5M2,
+                                                     recv_scales=sc, stream=stream))
     b_ue8 = 2 * T * H + n8 * H + n8 * nb + 4 * T * K
     b_pass = T * H + 4 * T * nb + n8 * H + 4 * n8 * nb + 4 * T * K
     del codes_in, scales_in, sc_u
@@ -518,6 +520,9 @@ def gpu_arm(args, rank, world, local):
             "dispatch_fp8_ue8m0_colmajor": {"us": round(ms_ue8 * 1e3, 2), "bytes": b_ue8,
                                             "gbs": round(b_ue8 / (ms_ue8 * 1e-3) / 1e9, 1),
                                             "frac_of_measured": round(b_ue8 / (ms_ue8 * 1e-3) / 1e9 / peak, 4)},
+            "dispatch_fp8_e5m2": {"us": round(ms_e5m2 * 1e3, 2), "bytes": b_fp8,
+                                  "gbs": round(b_fp8 / (ms_e5m2 * 1e-3) / 1e9, 1),
+                                  "frac_of_measured": round(b_fp8 / (ms_e5m2 * 1e-3) / 1e9 / peak, 4)},
             "dispatch_fp8_passthrough": {"us": round(ms_pass * 1e3, 2), "bytes": b_pass,
                                          "gbs": round(b_pass / (ms_pass * 1e-3) / 1e9, 1),
                                          "frac_of_measured": round(b_pass / (ms_pass * 1e-3) / 1e9 / peak, 4)},

@@ -16,7 +16,7 @@ import torch
 from .build import LIB as _LIB_PATH, build
 
 EP_OK, EP_ERR_INVALID_ARG, EP_ERR_INVALID_EXPERT, EP_ERR_CAPACITY, EP_ERR_CUDA, EP_ERR_ALLOC = range(6)
-EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3 = 0, 1
+EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3, EP_DTYPE_FP8_E5M2 = 0, 1, 2
 EP_SCALE_FP32, EP_SCALE_POW2, EP_SCALE_UE8M0 = 0, 1, 2
 
 

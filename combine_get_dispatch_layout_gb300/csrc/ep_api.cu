@@ -315,13 +315,16 @@ ep_status_t ep_dispatch_ex(ep_handle_t handle, const void* x, const void* x_scal
     if (!handle) return EP_ERR_INVALID_ARG;
     ep_dispatch_config_t cfg{};
     if (config) cfg = *config;
-    if (cfg.in_dtype != EP_DTYPE_BF16 && cfg.in_dtype != EP_DTYPE_FP8_E4M3) return EP_ERR_INVALID_ARG;
-    if (cfg.out_dtype != EP_DTYPE_BF16 && cfg.out_dtype != EP_DTYPE_FP8_E4M3) return EP_ERR_INVALID_ARG;
-    if (cfg.in_dtype == EP_DTYPE_FP8_E4M3 && cfg.out_dtype != EP_DTYPE_FP8_E4M3) return EP_ERR_INVALID_ARG;
+    const auto known = [](int d) {
+        return d == EP_DTYPE_BF16 || d == EP_DTYPE_FP8_E4M3 || d == EP_DTYPE_FP8_E5M2;
+    };
+    if (!known(cfg.in_dtype) || !known(cfg.out_dtype)) return EP_ERR_INVALID_ARG;
+    // fp8 input is moved unchanged, so it needs the same output type
+    if (cfg.in_dtype != EP_DTYPE_BF16 && cfg.out_dtype != cfg.in_dtype) return EP_ERR_INVALID_ARG;
     if (cfg.scale_mode != EP_SCALE_FP32 && cfg.scale_mode != EP_SCALE_POW2 && cfg.scale_mode != EP_SCALE_UE8M0)
         return EP_ERR_INVALID_ARG;
-    const bool fp8 = cfg.out_dtype == EP_DTYPE_FP8_E4M3;
-    const bool fp8_in = cfg.in_dtype == EP_DTYPE_FP8_E4M3;
+    const bool fp8 = cfg.out_dtype != EP_DTYPE_BF16;
+    const bool fp8_in = cfg.in_dtype != EP_DTYPE_BF16;
     if (H < 8 || H % 8 != 0 || recv_capacity < 0) return EP_ERR_INVALID_ARG;
     if (fp8 && H % 128 != 0) return EP_ERR_INVALID_ARG;
     const size_t scale_bytes = cfg.scale_mode == EP_SCALE_UE8M0 ? 1 : 4;
@@ -354,6 +357,7 @@ ep_status_t ep_dispatch_ex(ep_handle_t handle, const void* x, const void* x_scal
     a.K = handle->K;
     a.H = H;
     a.scale_mode = cfg.scale_mode;
+    a.fp8_format = cfg.out_dtype;
     a.scale_col_major = cfg.scales_col_major ? 1 : 0;
     a.scale_ld = cfg.scales_ld;
     a.x_scales = x_scales;

@@ -1,12 +1,15 @@
 // Dispatch: stable expert-major permute of token rows into the receive buffer,
-// optionally quantised to e4m3 with one fp32 scale per 128 channels.
+// optionally quantised to fp8 (e4m3 or e5m2) with one scale per 128 channels.
 //
 // What is computed follows nccl_ep.cc, ncclEpDispatch (tokens are bf16 rows;
 // the fp8 path writes fp32 scales shaped [rows, hidden/128]) and the DeepEP
 // API docs, "dispatch()" (do_expand: every (token, expert) pair gets its own
 // received row). Readings where the pages are silent: scale = amax / 448 with
 // IEEE division, q = e4m3(x / scale) rounded to nearest-even and saturated to
-// +-448, and an all-zero block gives scale 0 and zero bytes.
+// +-448, and an all-zero block gives scale 0 and zero bytes. nccl_ep.cc
+// (ncclTypeSize, ncclEpDispatch) also takes e5m2 as a one-byte fp8 token
+// type; its quantiser here is the same rule with e5m2's largest finite value,
+// 57344, in place of 448.
 //
 // GPU design: the work item is (token, column segment), one warp per item.
 // The warp reads its slice of the token row once with 16-byte loads and
@@ -88,11 +91,22 @@ dispatch_bf16_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
     }
 }
 
-// Two fp32 values -> two e4m3 codes (RNE, satfinite); `lo` goes to the low byte.
-__device__ __forceinline__ unsigned short e4m3x2(float lo, float hi) {
+// Two fp32 values -> two codes of the fp8 format kFmt (EP_DTYPE_FP8_E4M3 or
+// EP_DTYPE_FP8_E5M2; RNE, satfinite); `lo` goes to the low byte.
+template <int kFmt>
+__device__ __forceinline__ unsigned short fp8x2(float lo, float hi) {
     unsigned short d;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    if (kFmt == EP_DTYPE_FP8_E5M2)
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
     return d;
+}
+
+// Largest finite value of the fp8 format; a block's amax maps onto it.
+template <int kFmt>
+__host__ __device__ constexpr float fp8_max() {
+    return kFmt == EP_DTYPE_FP8_E5M2 ? 57344.0f : 448.0f;
 }
 
 __device__ __forceinline__ float bf16_lo(unsigned u) { return __uint_as_float(u << 16); }
@@ -116,10 +130,10 @@ __device__ __forceinline__ int64_t scale_index(const DispatchArgs& a, int64_t r,
     return kColMajor ? static_cast<int64_t>(b) * a.scale_ld + r : r * nb + b;
 }
 
-// kMode: EP_SCALE_FP32 (scale = amax/448), EP_SCALE_POW2 (smallest power of
-// two >= amax/448, stored as fp32) or EP_SCALE_UE8M0 (that power, at least
-// 2^-127, stored as its biased exponent byte).
-template <int kMode, bool kColMajor>
+// kMode: EP_SCALE_FP32 (scale = amax/F), EP_SCALE_POW2 (smallest power of
+// two >= amax/F, stored as fp32) or EP_SCALE_UE8M0 (that power, at least
+// 2^-127, stored as its biased exponent byte); F = fp8_max<kFmt>().
+template <int kMode, bool kColMajor, int kFmt>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 dispatch_fp8_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
     const int lane = threadIdx.x & 31;
@@ -155,13 +169,13 @@ dispatch_fp8_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
             scale[u] = 0.0f;
             q[u] = make_uint4(0u, 0u, 0u, 0u);
         } else {
-            float s = __fdiv_rn(m, 448.0f);
+            float s = __fdiv_rn(m, fp8_max<kFmt>());
             if (kMode != EP_SCALE_FP32) s = pow2_ceil(s);
             if (kMode == EP_SCALE_UE8M0) s = fmaxf(s, __uint_as_float(0x00400000u));   // 2^-127
             scale[u] = s;
             unsigned w[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) w[i] = e4m3x2(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
+            for (int i = 0; i < 8; ++i) w[i] = fp8x2<kFmt>(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
             q[u] = make_uint4(w[0] | (w[1] << 16), w[2] | (w[3] << 16), w[4] | (w[5] << 16), w[6] | (w[7] << 16));
         }
     }
@@ -194,7 +208,7 @@ dispatch_fp8_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
 }
 
 // fp8 input pass-through: one warp per (token, column segment) copies the
-// token's e4m3 codes to each of its K rows with 16-byte vectors; the warp of
+// token's fp8 codes (e4m3 or e5m2: bytes either way) to each of its K rows with 16-byte vectors; the warp of
 // segment 0 also copies the token's scale row (fp32, or bytes in UE8M0 mode)
 // into every receive row's scales, in the requested layout.
 template <bool kColMajor>
@@ -322,23 +336,34 @@ cudaError_t launch_dispatch_fp8_passthrough(const DispatchArgs& a, cudaStream_t 
     return launch_dispatch_kernel(ov, dispatch_fp8_passthrough_kernel<false>, g, stream, a, items, segs);
 }
 
+namespace {
+
+template <int kMode, int kFmt>
+cudaError_t launch_fp8_variant(const DispatchArgs& a, unsigned g, cudaStream_t stream, int64_t items, int segs) {
+    const bool ov = a.overlap_layout != 0;
+    if (a.scale_col_major)
+        return launch_dispatch_kernel(ov, dispatch_fp8_kernel<kMode, true, kFmt>, g, stream, a, items, segs);
+    return launch_dispatch_kernel(ov, dispatch_fp8_kernel<kMode, false, kFmt>, g, stream, a, items, segs);
+}
+
+template <int kFmt>
+cudaError_t launch_fp8_format(const DispatchArgs& a, unsigned g, cudaStream_t stream, int64_t items, int segs) {
+    if (a.scale_mode == EP_SCALE_POW2) return launch_fp8_variant<EP_SCALE_POW2, kFmt>(a, g, stream, items, segs);
+    if (a.scale_mode == EP_SCALE_UE8M0) return launch_fp8_variant<EP_SCALE_UE8M0, kFmt>(a, g, stream, items, segs);
+    return launch_fp8_variant<EP_SCALE_FP32, kFmt>(a, g, stream, items, segs);
+}
+
+}  // namespace
+
 cudaError_t launch_dispatch_fp8(const DispatchArgs& a, cudaStream_t stream) {
     const int G = a.H / 16;                           // 16-channel groups per row
     const int per_item = 32 * kFp8Unroll;
     const int segs = (G + per_item - 1) / per_item;
     const int64_t items = static_cast<int64_t>(a.T) * segs;
     if (items == 0) return cudaSuccess;
-    const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    const unsigned g = static_cast<unsigned>(blocks);
-    const bool col = a.scale_col_major != 0, ov = a.overlap_layout != 0;
-    if (a.scale_mode == EP_SCALE_POW2)
-        return col ? launch_dispatch_kernel(ov, dispatch_fp8_kernel<EP_SCALE_POW2, true>, g, stream, a, items, segs)
-                   : launch_dispatch_kernel(ov, dispatch_fp8_kernel<EP_SCALE_POW2, false>, g, stream, a, items, segs);
-    if (a.scale_mode == EP_SCALE_UE8M0)
-        return col ? launch_dispatch_kernel(ov, dispatch_fp8_kernel<EP_SCALE_UE8M0, true>, g, stream, a, items, segs)
-                   : launch_dispatch_kernel(ov, dispatch_fp8_kernel<EP_SCALE_UE8M0, false>, g, stream, a, items, segs);
-    return col ? launch_dispatch_kernel(ov, dispatch_fp8_kernel<EP_SCALE_FP32, true>, g, stream, a, items, segs)
-               : launch_dispatch_kernel(ov, dispatch_fp8_kernel<EP_SCALE_FP32, false>, g, stream, a, items, segs);
+    const unsigned g = static_cast<unsigned>((items + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    if (a.fp8_format == EP_DTYPE_FP8_E5M2) return launch_fp8_format<EP_DTYPE_FP8_E5M2>(a, g, stream, items, segs);
+    return launch_fp8_format<EP_DTYPE_FP8_E4M3>(a, g, stream, items, segs);
 }
 
 }  // namespace ep

@@ -72,6 +72,7 @@ struct DispatchArgs {
     int64_t recv_capacity;
     int T, K, H;
     int scale_mode;            // EP_SCALE_FP32 / EP_SCALE_POW2 / EP_SCALE_UE8M0
+    int fp8_format;            // EP_DTYPE_FP8_E4M3 / EP_DTYPE_FP8_E5M2 (fp8 output)
     int scale_col_major;       // 0: scales [rows, H/128]; 1: [H/128, scale_ld]
     int64_t scale_ld;
     const void* x_scales;      // fp8 input: [T, H/128] fp32 (uint8 in UE8M0 mode)

@@ -63,22 +63,25 @@ typedef enum {
 
 typedef enum {
     EP_DTYPE_BF16 = 0,         /* receive rows are the bf16 token rows        */
-    EP_DTYPE_FP8_E4M3 = 1      /* receive rows are e4m3 bytes + fp32 scales   */
+    EP_DTYPE_FP8_E4M3 = 1,     /* receive rows are e4m3 bytes + fp32 scales   */
+    EP_DTYPE_FP8_E5M2 = 2      /* receive rows are e5m2 bytes + fp32 scales   */
 } ep_dtype_t;
 
-/* How fp8 block scales are formed and stored (one per 128 channels). */
+/* How fp8 block scales are formed and stored (one per 128 channels). F is the
+ * largest finite value of the output format: 448 for e4m3, 57344 for e5m2. */
 typedef enum {
-    EP_SCALE_FP32 = 0,  /* scale = amax / 448 (IEEE fp32 division), stored as fp32        */
-    EP_SCALE_POW2 = 1,  /* smallest power of two >= amax / 448, stored as fp32          */
+    EP_SCALE_FP32 = 0,  /* scale = amax / F (IEEE fp32 division), stored as fp32          */
+    EP_SCALE_POW2 = 1,  /* smallest power of two >= amax / F, stored as fp32            */
     EP_SCALE_UE8M0 = 2  /* that power (at least 2^-127) stored as its biased exponent
                            byte b, value 2^(b - 127)                                    */
 } ep_scale_mode_t;
 
 /* Options of ep_dispatch_ex; an all-zero struct means bf16 in, bf16 out. */
 typedef struct {
-    int in_dtype;          /* EP_DTYPE_BF16: x is bf16 [T, H]; EP_DTYPE_FP8_E4M3: x is e4m3
-                              codes [T, H] with x_scales, moved unchanged (needs fp8 out) */
-    int out_dtype;         /* EP_DTYPE_BF16 or EP_DTYPE_FP8_E4M3                          */
+    int in_dtype;          /* EP_DTYPE_BF16: x is bf16 [T, H]; EP_DTYPE_FP8_E4M3 or _E5M2:
+                              x is fp8 codes [T, H] with x_scales, moved unchanged
+                              (needs out_dtype == in_dtype)                          */
+    int out_dtype;         /* EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3 or EP_DTYPE_FP8_E5M2      */
     int scale_mode;        /* ep_scale_mode_t for fp8 output (and the x_scales type)      */
     int scales_col_major;  /* 0: recv_scales [cap, H/128]; 1: [H/128, scales_ld]          */
     int64_t scales_ld;     /* rows of the column-major scale matrix (>= recv_capacity)    */
@@ -241,6 +244,12 @@ EP_API ep_status_t ep_nonexpand_recv_topk(ep_handle_t handle, const int64_t* top
  *                      (uint8 [cap, H]), recv_scales[n, b] = scale
  *                      (fp32 [cap, H/128] row-major). An all-zero block has
  *                      scale 0 and zero bytes.
+ *   EP_DTYPE_FP8_E5M2: the same with scale = amax / 57344 and e5m2 codes
+ *                      (OCP E5M2: bias 15, 2 mantissa bits, largest finite
+ *                      57344; satfinite RNE). nccl_ep.cc (ncclTypeSize,
+ *                      ncclEpDispatch) lists e5m2 beside e4m3 as a one-byte
+ *                      fp8 token type; the scale rule is e4m3's with the
+ *                      format's largest finite value in place of 448.
  *   recv_src_token[n] = t          (optional, int32 [cap], NULL = skip)
  *   recv_weights[n] = topk_weights[t, k]  (optional, fp32 [cap]; needs
  *                                  topk_weights; NULL = skip)
@@ -267,16 +276,18 @@ EP_API ep_status_t ep_dispatch(ep_handle_t handle, const void* x, int H, ep_dtyp
  * "dispatch()": use_ue8m0), a column-major scale layout (DeepEP
  * "dispatch()": use_tma_aligned_col_major_sf), and fp8 input pass-through
  * (DeepEP "dispatch()": x as an (fp8 data, scales) tuple; nccl_ep.cc: fp8
- * tokens with their scales in the high-throughput path).
+ * tokens with their scales in the high-throughput path), for e4m3 and e5m2
+ * (nccl_ep.cc, ncclEpDispatch: fp8 input is either type).
  *
  * With in_dtype = EP_DTYPE_BF16 and fp8 output, each 128-channel block of
- * token t gets s = amax / 448 and, by scale_mode: FP32 -> scale = s;
+ * token t gets s = amax / F (F = 448 for e4m3, 57344 for e5m2 output) and,
+ * by scale_mode: FP32 -> scale = s;
  * POW2 -> the smallest power of two >= s; UE8M0 -> that power raised to at
- * least 2^-127 and stored as its exponent byte. Codes are
- * e4m3_rne_satfinite(x / scale). An all-zero block has zero codes and scale 0
- * (UE8M0 byte 0). With in_dtype = EP_DTYPE_FP8_E4M3, x holds codes [T, H]
- * (bytes) and x_scales [T, H/128] (fp32, or bytes in UE8M0 mode); both are
- * copied to every slot's row. recv_scales is fp32 (bytes in UE8M0 mode),
+ * least 2^-127 and stored as its exponent byte. Codes are the output
+ * format's rne_satfinite(x / scale). An all-zero block has zero codes and
+ * scale 0 (UE8M0 byte 0). With fp8 in_dtype (out_dtype must match), x holds
+ * codes [T, H] (bytes) and x_scales [T, H/128] (fp32, or bytes in UE8M0
+ * mode); both are copied to every slot's row. recv_scales is fp32 (bytes in UE8M0 mode),
  * [cap, H/128] row-major or, with scales_col_major, element (row n, block b)
  * at n + b * scales_ld. Other arguments and errors as ep_dispatch; config may
  * be NULL (bf16 in and out).

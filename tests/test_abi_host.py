@@ -164,3 +164,13 @@ def test_dispatch_config_struct_matches_header():
     fields = re.findall(r"^\s*(?:int|int64_t)\s+(\w+);", body, flags=re.M)
     assert fields == [f for f, _ in ep.DispatchConfig._fields_]
     assert ctypes.sizeof(ep.DispatchConfig) == 32
+
+
+def test_enum_constants_match_header():
+    """Every enumerator the header defines has the same value in the binding."""
+    import combine_get_dispatch_layout_gb300 as ep
+    src = open(os.path.join(ROOT, "include", "ep.h")).read()
+    enums = dict((k, int(v)) for k, v in re.findall(r"^\s*(EP_[A-Z0-9_]+)\s*=\s*(\d+)\s*,?", src, flags=re.M))
+    assert {"EP_DTYPE_FP8_E5M2", "EP_SCALE_UE8M0", "EP_ERR_ALLOC"} <= set(enums)
+    for name, value in enums.items():
+        assert getattr(ep, name) == value, name

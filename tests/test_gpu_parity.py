@@ -296,13 +296,14 @@ def test_fp8_special_blocks(ep):
     full_path(ep, inp, fp8=True)
 
 
-def test_fp8_encoder_sweep_all_bf16(ep):
-    """Every finite bf16 pattern through the quantiser under several block scales."""
+def _sweep_inputs(amaxes):
+    """Blocks holding every finite bf16 pattern of magnitude <= amax, with amax
+    itself as the block's last element, for each amax."""
     pats = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
     f = gi.bf16_bits_to_f32(pats)
     pats = pats[np.isfinite(f)]
     rows = []
-    for amax in [448.0, 1.0, 3.0, 1e-3, 7.5e7, 2.0 ** -120]:
+    for amax in amaxes:
         vals = gi.bf16_bits_to_f32(pats)
         vals = vals[np.abs(vals) <= amax]
         per = 127
@@ -319,9 +320,13 @@ def test_fp8_encoder_sweep_all_bf16(ep):
     pad = np.zeros((nb * 8 - len(allb), 128), np.float32)
     x = gi.f32_to_bf16_bits(np.concatenate([allb, pad]).reshape(nb, H))
     idx = np.zeros((nb, 1), np.int64)
-    inp = gi.Inputs(w=_workload(nb, H, 1, 1, 1), seed=0, x=x, topk_idx=idx,
-                    topk_weights=np.ones((nb, 1), np.float32), y=None, num_valid=nb)
-    full_path(ep, inp, fp8=True)
+    return gi.Inputs(w=_workload(nb, H, 1, 1, 1), seed=0, x=x, topk_idx=idx,
+                     topk_weights=np.ones((nb, 1), np.float32), y=None, num_valid=nb)
+
+
+def test_fp8_encoder_sweep_all_bf16(ep):
+    """Every finite bf16 pattern through the quantiser under several block scales."""
+    full_path(ep, _sweep_inputs([448.0, 1.0, 3.0, 1e-3, 7.5e7, 2.0 ** -120]), fp8=True)
 
 
 def test_invalid_expert_ids(ep):
@@ -700,14 +705,16 @@ def _layout_dev(ep, inp, A=1):
     return ep.ep_layout_aligned(_dev(inp.topk_idx), w.E, w.R, A, *o)
 
 
-def fp8_variant(ep, inp, mode, col_major=False, A=1):
+def fp8_variant(ep, inp, mode, col_major=False, A=1, fmt=1):
     w = inp.w
     ref = oracle.layout_aligned(inp.topk_idx, w.E, w.R, A)
     n = int(ref["expert_offsets"][-1])
     nb = w.H // 128
     ue = mode == ep.EP_SCALE_UE8M0
     h = _layout_dev(ep, inp, A)
-    if mode == ep.EP_SCALE_FP32:
+    if fmt == ep.EP_DTYPE_FP8_E5M2:
+        r_q, r_s = oracle.dispatch_e5m2(inp.x, ref["row_of_slot"], n, scale_mode=mode)
+    elif mode == ep.EP_SCALE_FP32:
         r_q, r_s, _, _ = oracle.dispatch_e4m3(inp.x, ref["row_of_slot"], n)
     else:
         r_q, r_s = oracle.dispatch_e4m3_pow2(inp.x, ref["row_of_slot"], n, ue8m0=ue)
@@ -722,7 +729,7 @@ def fp8_variant(ep, inp, mode, col_major=False, A=1):
     sent = 0xEE if ue else -1.0
     q = torch.full((max(n, 1), w.H), SENT8, dtype=torch.uint8, device="cuda")
     sc = torch.full((nb * ld,) if col_major else (max(n, 1), nb), sent, dtype=sdt, device="cuda")
-    ep.ep_dispatch_ex(h, _dev(inp.x.view(np.int16)), q, n, scale_mode=mode, recv_scales=sc,
+    ep.ep_dispatch_ex(h, _dev(inp.x.view(np.int16)), q, n, out_dtype=fmt, scale_mode=mode, recv_scales=sc,
                       scales_col_major=col_major, scales_ld=ld if col_major else 0)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(q.cpu().numpy()[:n], r_q)
@@ -797,6 +804,94 @@ def test_fp8_input_passthrough(ep, ue):
     np.testing.assert_array_equal(sc.cpu().numpy(), oracle.dispatch_rows(scales, ref["row_of_slot"], n))
     _, r_src, _ = oracle.dispatch_bf16(inp.x, ref["row_of_slot"], n)
     np.testing.assert_array_equal(src.cpu().numpy(), r_src)
+    h.destroy()
+
+
+# ------------------------------------------------------------------ e5m2
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("decode", None), ("fp8", 1001), ("skewed", 2000)])
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_e5m2_quantise_permute(ep, name, T, mode):
+    fp8_variant(ep, gi.make(name, 31, T=T, with_y=False), mode, fmt=ep.EP_DTYPE_FP8_E5M2)
+
+
+def test_e5m2_full_size(ep):
+    """The fp8 prefill workload (T=8192, H=7168, top-8 of 256) quantised to e5m2."""
+    fp8_variant(ep, gi.make("fp8", 0, with_y=False), 0, fmt=ep.EP_DTYPE_FP8_E5M2)
+
+
+@pytest.mark.parametrize("mode,col,A", [(0, True, 1), (2, True, 1), (1, False, 32), (0, True, 32)])
+def test_e5m2_col_major_and_aligned(ep, mode, col, A):
+    fp8_variant(ep, gi.make("skewed", 32, T=1500, with_y=False), mode, col_major=col, A=A,
+                fmt=ep.EP_DTYPE_FP8_E5M2)
+
+
+def test_e5m2_special_blocks(ep):
+    rng = np.random.default_rng(33)
+    T, H = 40, 1024
+    xf = (rng.standard_normal((T, H)) * 2).astype(np.float32)
+    xf[0, :128] = 0.0
+    xf[1, 128:256] = 1e-39
+    xf[2, 256:384] = 2.0 ** -130
+    xf[3, 384:512] = 3e38
+    xf[4, :] = np.float32(2.0 ** -133)
+    xf[5, ::2] *= 1e4
+    xf[6, 512:640] = -0.0
+    x = gi.f32_to_bf16_bits(xf)
+    idx = np.argsort(rng.random((T, 16)), axis=1)[:, :3].astype(np.int64)
+    inp = gi.Inputs(w=_workload(T, H, 16, 3, 4), seed=0, x=x, topk_idx=idx,
+                    topk_weights=np.full((T, 3), 1 / 3, np.float32), y=None, num_valid=3 * T)
+    for mode in (0, 1, 2):
+        fp8_variant(ep, inp, mode, fmt=ep.EP_DTYPE_FP8_E5M2)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_e5m2_encoder_sweep_all_bf16(ep, mode):
+    """Every finite bf16 pattern through the e5m2 quantiser under several block scales."""
+    inp = _sweep_inputs([57344.0, 448.0, 1.0, 3.0, 1e-3, 7.5e7, 2.0 ** -120])
+    fp8_variant(ep, inp, mode, fmt=ep.EP_DTYPE_FP8_E5M2)
+
+
+@pytest.mark.parametrize("ue", [False, True])
+def test_e5m2_input_passthrough(ep, ue):
+    inp = gi.make("fp8", 34, T=500, with_y=False)
+    w = inp.w
+    nb = w.H // 128
+    codes = np.zeros((w.T, w.H), np.uint8)
+    scales = np.zeros((w.T, nb), np.uint8 if ue else np.float32)
+    for t in range(w.T):
+        codes[t], scales[t] = oracle.quant_row_e5m2(inp.x[t], 2 if ue else 0)
+    ref = oracle.layout(inp.topk_idx, w.E, w.R)
+    n = int(ref["expert_offsets"][-1])
+    h = _layout_dev(ep, inp)
+    q = torch.full((n, w.H), SENT8, dtype=torch.uint8, device="cuda")
+    sc = torch.full((n, nb), 0xEE if ue else -1.0, dtype=torch.uint8 if ue else torch.float32, device="cuda")
+    ep.ep_dispatch_ex(h, _dev(codes), q, n, in_dtype=ep.EP_DTYPE_FP8_E5M2, out_dtype=ep.EP_DTYPE_FP8_E5M2,
+                      scale_mode=ep.EP_SCALE_UE8M0 if ue else ep.EP_SCALE_FP32,
+                      x_scales=_dev(scales), recv_scales=sc, H=w.H)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(q.cpu().numpy(), oracle.dispatch_rows(codes, ref["row_of_slot"], n))
+    np.testing.assert_array_equal(sc.cpu().numpy(), oracle.dispatch_rows(scales, ref["row_of_slot"], n))
+    h.destroy()
+
+
+@pytest.mark.parametrize("in_dt,out_dt", [(1, 2), (2, 1), (2, 0), (1, 0), (0, 3), (3, 3)])
+def test_dispatch_ex_rejects_fp8_type_mismatch(ep, in_dt, out_dt):
+    """fp8 input is moved unchanged, so in and out types must agree; unknown
+    types are rejected; nothing is written."""
+    inp = gi.make("tiny", 35, with_y=False)
+    w = inp.w
+    h = _layout_dev(ep, inp)
+    n = w.T * w.K
+    q = torch.full((n, w.H), SENT8, dtype=torch.uint8, device="cuda")
+    sc = torch.zeros((n, w.H // 128), dtype=torch.float32, device="cuda")
+    xs = torch.ones((w.T, w.H // 128), dtype=torch.float32, device="cuda")
+    x = torch.zeros((w.T, w.H), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ep.EPError) as e:
+        ep.ep_dispatch_ex(h, x, q, n, in_dtype=in_dt, out_dtype=out_dt, x_scales=xs, recv_scales=sc, H=w.H)
+    assert e.value.status == ep.EP_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert (q == SENT8).all()
     h.destroy()
 
 
