@@ -24,6 +24,7 @@ struct ep_handle {
     ep::LayoutPlan plan{};
     cudaStream_t layout_stream = nullptr;
     bool error_latched = false;
+    bool meta_known = false;    // host_meta holds the last layout's state words
     int layout_kernels = 0;     // kernels the last ep_layout enqueued
     // capacities of the device block
     int64_t cap_slots = 0, cap_chunk_cells = 0, cap_rank_cells = 0, cap_experts = 0;
@@ -103,12 +104,17 @@ ep_status_t ensure_block(ep_handle* h, int64_t slots, int64_t chunk_cells, int64
     return EP_OK;
 }
 
-// Read the state words written by the last layout (synchronises its stream).
+// Read the state words written by the last layout. Only layouts write them,
+// so the first read after a layout synchronises its stream and later reads
+// use the host copy until the next layout on this handle.
 ep_status_t read_meta(ep_handle* h, int64_t* rows, int32_t* err) {
-    if (cudaMemcpyAsync(h->host_meta, h->meta, sizeof(int32_t) * ep::kMetaWords, cudaMemcpyDeviceToHost,
-                        h->layout_stream) != cudaSuccess)
-        return EP_ERR_CUDA;
-    if (cudaStreamSynchronize(h->layout_stream) != cudaSuccess) return EP_ERR_CUDA;
+    if (!h->meta_known) {
+        if (cudaMemcpyAsync(h->host_meta, h->meta, sizeof(int32_t) * ep::kMetaWords, cudaMemcpyDeviceToHost,
+                            h->layout_stream) != cudaSuccess)
+            return EP_ERR_CUDA;
+        if (cudaStreamSynchronize(h->layout_stream) != cudaSuccess) return EP_ERR_CUDA;
+        h->meta_known = true;
+    }
     if (rows) *rows = h->host_meta[ep::kMetaRows];
     if (err) *err = h->host_meta[ep::kMetaError];
     // an invalid expert id blocks later calls; a strided overflow only drops slots
@@ -180,6 +186,7 @@ ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int
         ep_status_t st = current_device_is(h);
         if (st != EP_OK) return st;
     }
+    h->meta_known = false;   // this layout rewrites the state words
 
     // a non-expand layout runs the expert layout over derived rank keys: the
     // key space is the R ranks (one "expert" per rank)

@@ -31,6 +31,12 @@
  *  - All device work is enqueued on `stream` (a cudaStream_t; NULL = the
  *    legacy default stream) and is asynchronous, except where a call says it
  *    synchronises.
+ *  - N (the receive rows of the last layout) and the device error word are
+ *    read from the device at most once per layout: the first call that needs
+ *    them (ep_handle_query, or a dispatch / combine whose buffer is smaller
+ *    than the most rows the routing can need) synchronises the layout's
+ *    stream; later calls use the host copy until the next layout on the
+ *    handle.
  *  - Arguments are checked on the host first. A failed check returns
  *    EP_ERR_INVALID_ARG and enqueues nothing.
  *  - Row buffers (x, recv_x, y, out) must be 16-byte aligned.
@@ -260,7 +266,7 @@ EP_API ep_status_t ep_nonexpand_recv_topk(ep_handle_t handle, const int64_t* top
  * Rows >= N (the padded total after an aligned layout) are not written.
  * recv_capacity is the number of rows the receive buffers hold. If it is
  * below the most the routing can need (T*K, plus E*(A-1) when aligned) the
- * call reads N from the device (one stream synchronise) and returns
+ * call needs N (read once per layout, see above) and returns
  * EP_ERR_CAPACITY, enqueuing nothing, when N > recv_capacity.
  * Returns EP_ERR_INVALID_EXPERT if the handle is known to have seen an
  * invalid expert id.
@@ -305,8 +311,8 @@ EP_API ep_status_t ep_dispatch_ex(ep_handle_t handle, const void* x, const void*
  * accumulated in fp32 with fused multiply-adds in ascending k from +0, and
  * rounded once. topk_weights is fp32 [T, K] (device) or NULL for all-ones.
  * y is bf16 [y_rows, H] (device), out is bf16 [T, H] (device), H % 8 == 0.
- * A token with no valid slot gets +0. If y_rows < T*K the call reads N
- * (one stream synchronise) and returns EP_ERR_CAPACITY when N > y_rows.
+ * A token with no valid slot gets +0. If y_rows < T*K the call needs N
+ * (read once per layout) and returns EP_ERR_CAPACITY when N > y_rows.
  */
 EP_API ep_status_t ep_combine(ep_handle_t handle, const void* y, int64_t y_rows, int H,
                        const float* topk_weights, void* out, void* stream);
@@ -324,8 +330,8 @@ EP_API ep_status_t ep_combine(ep_handle_t handle, const void* y, int64_t y_rows,
  * (needed only for grad_topk_weights); topk_weights fp32 [T, K] or NULL (all
  * ones); grad_y bf16 [grad_y_capacity, H] or NULL; grad_topk_weights fp32
  * [T, K] or NULL. After an aligned layout the pad rows of grad_y are zeroed.
- * Buffers smaller than the most rows the routing can need trigger one stream
- * synchronise and EP_ERR_CAPACITY if they hold fewer than N rows.
+ * Buffers smaller than the most rows the routing can need need N (read once
+ * per layout) and give EP_ERR_CAPACITY if they hold fewer than N rows.
  */
 EP_API ep_status_t ep_combine_backward(ep_handle_t handle, const void* grad_out, const void* y, int64_t y_rows,
                                        int H, const float* topk_weights, void* grad_y,
@@ -376,7 +382,8 @@ EP_API ep_status_t ep_routing_map_to_topk(const uint8_t* routing_map, const floa
  * last layout call: N (receive rows: valid slots, the padded total after
  * ep_layout_aligned, E * capacity after ep_layout_strided) and the device
  * error word (0, EP_ERR_INVALID_EXPERT, or EP_ERR_CAPACITY when a strided
- * layout dropped slots). Synchronises the layout stream. Returns the error
+ * layout dropped slots). Synchronises the layout stream on the first read
+ * after a layout; later queries return the host copy. Returns the error
  * word's code if it is set (outputs still filled). Either output pointer may
  * be NULL.
  */

@@ -378,6 +378,48 @@ def test_capacity_errors(ep):
     run.h.destroy()
 
 
+def test_cached_row_count_follows_each_layout(ep):
+    """N is read from the device once per layout; a new layout on the same
+    handle must not be checked against the previous layout's N."""
+    rng = np.random.default_rng(41)
+    T, K, E, R, H = 300, 4, 16, 4, 64
+    idx_a = np.argsort(rng.random((T, E)), axis=1)[:, :K].astype(np.int64)
+    idx_a[rng.random((T, K)) < 0.5] = -1
+    idx_b = np.argsort(rng.random((T, E)), axis=1)[:, :K].astype(np.int64)
+    idx_b[rng.random((T, K)) < 0.1] = -1
+    n_a, n_b = int((idx_a >= 0).sum()), int((idx_b >= 0).sum())
+    assert n_a < n_b
+    x = _dev(gi.normal_bf16(np.random.SeedSequence(42), T, H).view(np.int16), torch.bfloat16)
+    run = Run(ep, idx_a, E, R)
+    assert ep.ep_handle_query(run.h)[0] == n_a           # reads and caches N of layout A
+    recv_a = torch.zeros((n_a, H), dtype=torch.bfloat16, device="cuda")
+    ep.ep_dispatch(run.h, x, ep.EP_DTYPE_BF16, recv_a, n_a)
+    run_b = Run(ep, idx_b, E, R, handle=run.h)           # layout B on the same handle
+    with pytest.raises(ep.EPError) as e:
+        ep.ep_dispatch(run_b.h, x, ep.EP_DTYPE_BF16, recv_a, n_a)
+    assert e.value.status == ep.EP_ERR_CAPACITY
+    recv_b = torch.full((n_b, H), -7.0, dtype=torch.bfloat16, device="cuda")
+    ep.ep_dispatch(run_b.h, x, ep.EP_DTYPE_BF16, recv_b, n_b)   # N of B, from the cache now
+    out = torch.zeros((T, H), dtype=torch.bfloat16, device="cuda")
+    ep.ep_combine(run_b.h, recv_b, out)
+    torch.cuda.synchronize()
+    ref = oracle.layout(idx_b, E, R)
+    x_bits = x.view(torch.int16).cpu().numpy().view(np.uint16)
+    r_x, _, _ = oracle.dispatch_bf16(x_bits, ref["row_of_slot"], n_b)
+    np.testing.assert_array_equal(recv_b.view(torch.int16).cpu().numpy().view(np.uint16), r_x)
+    np.testing.assert_array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16),
+                                  oracle.combine(r_x, ref["row_of_slot"], None))
+    # a layout with an invalid id after a clean one: the error is not hidden
+    # by the clean layout's cached words
+    idx_c = idx_b.copy()
+    idx_c[7, 2] = E + 3
+    run_c = Run(ep, idx_c, E, R, handle=run.h)
+    with pytest.raises(ep.EPError) as e:
+        ep.ep_dispatch(run_c.h, x, ep.EP_DTYPE_BF16, recv_b, n_b)
+    assert e.value.status == ep.EP_ERR_INVALID_EXPERT
+    run.h.destroy()
+
+
 def test_handle_reuse_grow_and_shrink(ep):
     h = None
     for (T, K, E, R, seed) in [(64, 2, 8, 2, 0), (5000, 8, 256, 8, 1), (10, 3, 6, 3, 2), (20000, 6, 64, 4, 3)]:
