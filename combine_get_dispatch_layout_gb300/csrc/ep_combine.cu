@@ -10,12 +10,15 @@
 //
 // GPU design: the work item is (token, column segment), one warp per item.
 // The warp compacts the token's used slots (ballot + popc) into shared memory
-// in ascending k, then for its 16-byte column vector issues the loads of 4
-// slots at once before accumulating them in k order. Items are small (256
-// channels) and blocks are 2 warps, so many warps per SM keep the gather's
-// bytes in flight and the last wave is short; a sweep of vectors per lane
-// (1, 2, 4), slots per load group (4, 8) and warps per block (1 to 8) on the
-// prefill shape picked this point.
+// in ascending k, then for its 16-byte column vector issues the loads of a
+// group of slots at once before accumulating them in k order. Items are small
+// (256 channels) and blocks are 2 warps, so many warps per SM keep the
+// gather's bytes in flight and the last wave is short; a sweep of vectors per
+// lane (1, 2, 4), slots per load group (3 to 8) and warps per block (1 to 8)
+// picked this point. The group is K split into the fewest round trips of at
+// most 6 slots, in equal parts: 4 + 4 for top-8, one trip of 6 for top-6
+// (groups of 4 there cost 5% on a 4 + 2 split; groups of 8 for top-8 cost 2%
+// in occupancy).
 #include <cuda_bf16.h>
 
 #include "ep_internal.cuh"
@@ -26,7 +29,7 @@ namespace {
 
 constexpr int kWarpsPerBlock = 2;   // small blocks: fine-grained scheduling
 constexpr int kUnroll = 1;      // 16-byte column vectors per lane per item
-constexpr int kGroup = 4;       // slots whose loads are issued together
+constexpr int kMaxGroup = 6;    // most slots whose loads are issued together
 
 __device__ __forceinline__ int4 ld_stream(const int4* p) {
     int4 v;
@@ -51,6 +54,7 @@ __device__ __forceinline__ unsigned pack_bf16x2(float lo, float hi) {
     return static_cast<unsigned>(l) | (static_cast<unsigned>(h) << 16);
 }
 
+template <int kGroup>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 combine_kernel(CombineArgs a, int64_t num_items, int num_segments) {
     __shared__ int s_row[kWarpsPerBlock][32];
@@ -132,7 +136,11 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
     const int64_t items = static_cast<int64_t>(a.T) * segs;
     if (items == 0) return cudaSuccess;
     const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    combine_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a, items, segs);
+    const int trips = (a.K + kMaxGroup - 1) / kMaxGroup;
+    const int group = (a.K + trips - 1) / trips;      // 1..6
+    const unsigned g = static_cast<unsigned>(blocks);
+    if (group <= 4) combine_kernel<4><<<g, kWarpsPerBlock * 32, 0, stream>>>(a, items, segs);
+    else combine_kernel<kMaxGroup><<<g, kWarpsPerBlock * 32, 0, stream>>>(a, items, segs);
     return cudaGetLastError();
 }
 
