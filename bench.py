@@ -270,6 +270,18 @@ def gpu_arm(args, rank, world, local):
     stream.synchronize()
     per = np.array([[split[i][j].elapsed_time(split[i][j + 1]) for j in range(3)] for i in range(reps_split)])
     ms_layout, ms_dispatch, ms_combine = (float(per[:, j].mean()) for j in range(3))
+
+    # layout + dispatch end to end (the dispatch as the layout's programmatic
+    # dependent), events only at the pair boundaries
+    ev_ld = [torch.cuda.Event(enable_timing=True) for _ in range(reps_split + 1)]
+    for i in range(-3, reps_split):
+        if i >= 0:
+            ev_ld[i].record(stream)
+        ep.ep_layout(idx, E, R, cnt, ntr, itr, off, handle=handle, stream=stream)
+        ep.ep_dispatch_ex(handle, x, recv, N, out_dtype=ep.EP_DTYPE_BF16, overlap_layout=True, stream=stream)
+    ev_ld[reps_split].record(stream)
+    stream.synchronize()
+    ms_lay_dis = float(np.mean([ev_ld[i].elapsed_time(ev_ld[i + 1]) for i in range(reps_split)]))
     b_lay = bytes_layout(T, K, E, R)
     b_dis = bytes_dispatch_bf16(T, K, H, N)
     b_com = bytes_combine(T, K, H, N)
@@ -459,6 +471,8 @@ def gpu_arm(args, rank, world, local):
     h_d.destroy()
     del d_y, d_recv
 
+    others = other_configs(torch, ep, dev, stream, args, rank, peak, reps_b)
+
     # end to end through the public API with pinned host buffers
     e2e = e2e_measure(torch, ep, dev, inp, args, stream)
     e2e["ms_per_step"], _ = aggregate_over_ranks(e2e["ms_per_step"], 0, device=dev)
@@ -509,6 +523,9 @@ def gpu_arm(args, rank, world, local):
                         "gbs": round(b_com / (ms_combine * 1e-3) / 1e9, 1),
                         "frac_of_measured": round(b_com / (ms_combine * 1e-3) / 1e9 / peak, 4),
                         "frac_of_8tbs": round(b_com / (ms_combine * 1e-3) / 8e12, 4)},
+            "layout_plus_dispatch_bf16": {"us": round(ms_lay_dis * 1e3, 2), "bytes": b_lay + b_dis,
+                                          "gbs": round((b_lay + b_dis) / (ms_lay_dis * 1e-3) / 1e9, 1),
+                                          "note": "dispatch launched as the layout's programmatic dependent"},
             "dispatch_bf16_aligned128": {"rows_padded": n_pad, "layout_us": round(ms_lay_a * 1e3, 2),
                                          "us": round(ms_dis_a * 1e3, 2), "bytes": b_dis_a,
                                          "gbs": round(b_dis_a / (ms_dis_a * 1e-3) / 1e9, 1),
@@ -539,6 +556,7 @@ def gpu_arm(args, rank, world, local):
                                "layout_strided_us": round(ms_d[0] * 1e3, 2),
                                "dispatch_us": round(ms_d[1] * 1e3, 2), "combine_us": round(ms_d[2] * 1e3, 2),
                                "tokens_per_s": round(wd.T / (sum(ms_d) * 1e-3), 1)},
+            **others,
             "combine_backward": {"us": round(ms_cbw * 1e3, 2), "bytes": b_cbw,
                                  "gbs": round(b_cbw / (ms_cbw * 1e-3) / 1e9, 1),
                                  "frac_of_measured": round(b_cbw / (ms_cbw * 1e-3) / 1e9 / peak, 4)},
@@ -565,6 +583,93 @@ def gpu_arm(args, rank, world, local):
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def other_configs(torch, ep, dev, stream, args, rank, peak, reps):
+    """The skewed workload's step (T=16384, H=4096, E=64, top-6 with drops)
+    and the decode step with L2 flushed before every iteration."""
+    out = {}
+
+    def split_loop(calls, flush=None):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(reps)]
+        for i in range(-3, reps):
+            if flush is not None:
+                with torch.cuda.stream(stream):
+                    flush.fill_(i)
+            for j, call in enumerate(calls):
+                if i >= 0:
+                    ev[i][j].record(stream)
+                call()
+            if i >= 0:
+                ev[i][len(calls)].record(stream)
+        stream.synchronize()
+        return [float(np.mean([e[j].elapsed_time(e[j + 1]) for e in ev])) for j in range(len(calls))]
+
+    def tensors(inp, rows):
+        w = inp.w
+        with torch.cuda.stream(stream):
+            t = {"idx": torch.from_numpy(inp.topk_idx).to(dev),
+                 "x": torch.from_numpy(inp.x.view(np.int16)).to(dev),
+                 "w": torch.from_numpy(inp.topk_weights).to(dev),
+                 "recv": torch.empty(rows, w.H, dtype=torch.int16, device=dev),
+                 "out": torch.empty(w.T, w.H, dtype=torch.int16, device=dev),
+                 "cnt": torch.empty(w.E, dtype=torch.int32, device=dev),
+                 "ntr": torch.empty(w.R, dtype=torch.int32, device=dev),
+                 "itr": torch.empty(w.T, w.R, dtype=torch.uint8, device=dev),
+                 "off": torch.empty(w.E + 1, dtype=torch.int32, device=dev)}
+        return t
+
+    # skewed: Zipf expert popularity, 5% dropped slots; y stands in for the
+    # expert outputs. The receive and expert-output buffers hold T*K rows, the
+    # most the routing can need, so no call waits for the layout's row count
+    sk = gi.make("skewed", seed=args.seed + rank)
+    ws, Ns = sk.w, sk.num_valid
+    cap = ws.T * ws.K
+    t = tensors(sk, cap)
+    with torch.cuda.stream(stream):
+        y = torch.zeros(cap, ws.H, dtype=torch.int16, device=dev)
+        y[:Ns] = torch.from_numpy(sk.y.view(np.int16)).to(dev)
+    h = ep.ep_layout(t["idx"], ws.E, ws.R, t["cnt"], t["ntr"], t["itr"], t["off"], stream=stream)
+    ms = split_loop([
+        lambda: ep.ep_layout(t["idx"], ws.E, ws.R, t["cnt"], t["ntr"], t["itr"], t["off"], handle=h, stream=stream),
+        lambda: ep.ep_dispatch(h, t["x"], ep.EP_DTYPE_BF16, t["recv"], cap, stream=stream),
+        lambda: ep.ep_combine(h, y, t["out"], topk_weights=t["w"], stream=stream)])
+    h.destroy()
+    bd, bc = bytes_dispatch_bf16(ws.T, ws.K, ws.H, Ns), bytes_combine(ws.T, ws.K, ws.H, Ns)
+    out["skewed_step"] = {
+        "workload": f"skewed: T={ws.T} H={ws.H} E={ws.E} K={ws.K} R={ws.R}, Zipf(1.2) experts, "
+                    f"5% dropped slots, N={Ns}",
+        "layout_us": round(ms[0] * 1e3, 2),
+        "dispatch_us": round(ms[1] * 1e3, 2), "dispatch_gbs": round(bd / (ms[1] * 1e-3) / 1e9, 1),
+        "dispatch_frac_of_measured": round(bd / (ms[1] * 1e-3) / 1e9 / peak, 4),
+        "combine_us": round(ms[2] * 1e3, 2), "combine_gbs": round(bc / (ms[2] * 1e-3) / 1e9, 1),
+        "combine_frac_of_measured": round(bc / (ms[2] * 1e-3) / 1e9 / peak, 4),
+        "tokens_per_s": round(ws.T / (sum(ms) * 1e-3), 1)}
+    del t, y
+
+    # decode through the strided layout [E, cap, H], L2 flushed first: a
+    # buffer twice the L2 size is written before every iteration (untimed)
+    dec = gi.make("decode", seed=args.seed + rank)
+    wd, cap = dec.w, dec.w.T
+    t = tensors(dec, wd.E * cap)
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or (128 << 20)
+    with torch.cuda.stream(stream):
+        y = torch.randn(wd.E * cap, wd.H, device=dev).to(torch.bfloat16).view(torch.int16)
+        flush = torch.empty(2 * l2 // 4, dtype=torch.int32, device=dev)
+    h = ep.ep_layout_strided(t["idx"], wd.E, wd.R, cap, t["cnt"], t["ntr"], t["itr"], t["off"], stream=stream)
+    ms = split_loop([
+        lambda: ep.ep_layout_strided(t["idx"], wd.E, wd.R, cap, t["cnt"], t["ntr"], t["itr"], t["off"],
+                                     handle=h, stream=stream),
+        lambda: ep.ep_dispatch(h, t["x"], ep.EP_DTYPE_BF16, t["recv"], wd.E * cap, stream=stream),
+        lambda: ep.ep_combine(h, y, t["out"], topk_weights=t["w"], stream=stream)], flush=flush)
+    h.destroy()
+    out["decode_ll_step_l2_flushed"] = {
+        "workload": f"decode T={wd.T} H={wd.H} E={wd.E} K={wd.K} R={wd.R}, strided layout cap={cap}, "
+                    f"L2 flushed ({2 * l2 >> 20} MiB written) before each iteration",
+        "layout_strided_us": round(ms[0] * 1e3, 2), "dispatch_us": round(ms[1] * 1e3, 2),
+        "combine_us": round(ms[2] * 1e3, 2), "tokens_per_s": round(wd.T / (sum(ms) * 1e-3), 1)}
+    del t, y, flush
+    return out
 
 
 def e2e_measure(torch, ep, dev, inp, args, stream):
