@@ -57,6 +57,10 @@ __device__ __forceinline__ unsigned pack_bf16x2(float lo, float hi) {
 template <int kGroup>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 combine_kernel(CombineArgs a, int64_t num_items, int num_segments) {
+    // launched as the preceding kernel's programmatic dependent: nothing is
+    // read or written before that kernel has finished
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     __shared__ int s_row[kWarpsPerBlock][32];
     __shared__ float s_w[kWarpsPerBlock][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -138,10 +142,20 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
     const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
     const int trips = (a.K + kMaxGroup - 1) / kMaxGroup;
     const int group = (a.K + trips - 1) / trips;      // 1..6
-    const unsigned g = static_cast<unsigned>(blocks);
-    if (group <= 4) combine_kernel<4><<<g, kWarpsPerBlock * 32, 0, stream>>>(a, items, segs);
-    else combine_kernel<kMaxGroup><<<g, kWarpsPerBlock * 32, 0, stream>>>(a, items, segs);
-    return cudaGetLastError();
+    // a programmatic dependent of whatever kernel precedes it on the stream:
+    // its blocks may be scheduled while that kernel's last wave runs, and wait
+    // for it to finish before touching memory
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kWarpsPerBlock * 32);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (group <= 4) return cudaLaunchKernelEx(&cfg, combine_kernel<4>, a, items, segs);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<kMaxGroup>, a, items, segs);
 }
 
 }  // namespace ep

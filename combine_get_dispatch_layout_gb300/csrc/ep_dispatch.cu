@@ -42,8 +42,16 @@ __device__ __forceinline__ int4 ld_stream(const int4* p) {
 }
 
 // Wait for the preceding grid (the layout that wrote row_of_slot) when this
-// kernel was launched as its programmatic dependent; a no-op otherwise.
-__device__ __forceinline__ void wait_for_layout() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// kernel was launched as its programmatic dependent; a no-op otherwise. Then
+// let a kernel launched as this grid's dependent (a combine) be scheduled on
+// SMs that this grid's last wave leaves free: it waits for this grid to
+// finish before its first memory access. Triggering only after the wait keeps
+// the chain's guarantee: when a kernel starts, all work before its immediate
+// predecessor is complete.
+__device__ __forceinline__ void wait_for_layout() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+}
 
 // Row of each slot of token t, lane k holds slot k (K <= 32); -1 if unused.
 __device__ __forceinline__ int slot_row(const int32_t* row_of_slot, int t, int K, int lane) {

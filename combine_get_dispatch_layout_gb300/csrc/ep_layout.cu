@@ -351,8 +351,11 @@ __device__ __forceinline__ unsigned rank_of(unsigned e, const LayoutPlan& p) {
 // holds the token rank masks (R <= 32) and later the offsets and CTA bases.
 __global__ void __launch_bounds__(1024, 1)
 layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
-    // a dispatch launched as this grid's dependent may start on idle SMs now;
-    // it reads the slot map only after this grid has finished
+    // launched as the preceding kernel's programmatic dependent: wait for it
+    // (and so for all earlier work) before touching memory; only then may a
+    // dispatch launched as this grid's dependent start on idle SMs (it reads
+    // the slot map only after this grid has finished)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     extern __shared__ int smem[];
     __shared__ int s_over;
@@ -708,13 +711,17 @@ cudaError_t launch_layout(const LayoutPlan& plan, const LayoutArgs& a, cudaStrea
             cfg.blockDim = dim3(p.cl_warps * 32);
             cfg.dynamicSmemBytes = p.smem_cluster;
             cfg.stream = stream;
-            cudaLaunchAttribute attr;
-            attr.id = cudaLaunchAttributeClusterDimension;
-            attr.val.clusterDim.x = ctas;
-            attr.val.clusterDim.y = 1;
-            attr.val.clusterDim.z = 1;
-            cfg.attrs = &attr;
-            cfg.numAttrs = 1;
+            cudaLaunchAttribute attr[2];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = ctas;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            // may be scheduled while the preceding kernel drains; it waits for
+            // that kernel before its first memory access
+            attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[1].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 2;
             if (kernels) *kernels = 1;
             return cudaLaunchKernelEx(&cfg, layout_cluster_kernel, p, a);
         }
