@@ -369,6 +369,13 @@ ep_status_t ep_dispatch_ex(ep_handle_t handle, const void* x, const void* x_scal
     a.scale_ld = cfg.scales_ld;
     a.x_scales = x_scales;
     a.overlap_layout = cfg.overlap_layout ? 1 : 0;
+    if (a.overlap_layout && handle->T > 0) {
+        // the L2 prefetch of x during the layout is for device memory only
+        cudaPointerAttributes attr{};
+        if (cudaPointerGetAttributes(&attr, x) == cudaSuccess && attr.type == cudaMemoryTypeDevice)
+            a.prefetch_x = 1;
+        cudaGetLastError();
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t err = fp8_in ? ep::launch_dispatch_fp8_passthrough(a, s)
                       : fp8  ? ep::launch_dispatch_fp8(a, s)

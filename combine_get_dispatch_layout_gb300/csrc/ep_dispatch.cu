@@ -53,6 +53,36 @@ __device__ __forceinline__ void wait_for_layout() {
     asm volatile("griddepcontrol.launch_dependents;");
 }
 
+constexpr int kPrefetchCtas = 512;                   // blocks that issue the x prefetch
+constexpr int64_t kPrefetchWindow = int64_t{96} << 20;   // bytes of x prefetched past theirs
+
+// HBM is idle while the layout runs. In a dispatch launched as the layout's
+// programmatic dependent, the first kPrefetchCtas blocks (resident from the
+// layout's start) ask the L2 to fetch up to kPrefetchWindow bytes of x past
+// the rows they read themselves: one bulk L2 prefetch each, holding no
+// registers or shared memory. Later blocks then find their rows in L2 (the
+// receive stores are evict-first, so the prefetched lines survive until
+// read), which takes those bytes off the dispatch's critical path. A hint
+// only: results do not depend on it. On the prefill shape it shortened the
+// step by ~5 us; windows of 64 to 128 MB and 256 to 1024 blocks were within
+// 1 us of each other, and an evict-last cache policy was slower (and kept x
+// in L2 past the dispatch).
+__device__ __forceinline__ void prefetch_x_during_layout(const DispatchArgs& a, int num_segments,
+                                                         int64_t row_bytes) {
+    if (!a.prefetch_x || blockIdx.x >= kPrefetchCtas || threadIdx.x != 0) return;
+    // tokens the prefetching blocks read themselves (row_bytes % 16 == 0)
+    const int64_t own = (static_cast<int64_t>(kPrefetchCtas) * kWarpsPerBlock + num_segments - 1) / num_segments;
+    const int64_t lo0 = own * row_bytes;
+    const int64_t end = min(static_cast<int64_t>(a.T) * row_bytes, lo0 + kPrefetchWindow);
+    if (end <= lo0) return;
+    const int64_t per = ((end - lo0 + kPrefetchCtas - 1) / kPrefetchCtas + 15) / 16 * 16;
+    const int64_t lo = lo0 + static_cast<int64_t>(blockIdx.x) * per;
+    const int64_t hi = min(lo + per, end);
+    if (lo >= hi) return;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                 :: "l"(static_cast<const char*>(a.x) + lo), "r"(static_cast<unsigned>(hi - lo)) : "memory");
+}
+
 // Row of each slot of token t, lane k holds slot k (K <= 32); -1 if unused.
 __device__ __forceinline__ int slot_row(const int32_t* row_of_slot, int t, int K, int lane) {
     return lane < K ? __ldg(row_of_slot + static_cast<int64_t>(t) * K + lane) : -1;
@@ -84,6 +114,7 @@ dispatch_bf16_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
         if (j < H16) v[u] = ld_stream(src + j);
     }
     // x is ready before the layout starts; the slot map only after it ends
+    prefetch_x_during_layout(a, num_segments, static_cast<int64_t>(a.H) * 2);
     wait_for_layout();
     const int row = slot_row(a.row_of_slot, t, a.K, lane);
     if (seg == 0) write_side_outputs(a, t, lane, row);
@@ -187,6 +218,7 @@ dispatch_fp8_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
             q[u] = make_uint4(w[0] | (w[1] << 16), w[2] | (w[3] << 16), w[4] | (w[5] << 16), w[6] | (w[7] << 16));
         }
     }
+    prefetch_x_during_layout(a, num_segments, static_cast<int64_t>(a.H) * 2);
     wait_for_layout();
     const int row = slot_row(a.row_of_slot, t, a.K, lane);
     if (seg == 0) write_side_outputs(a, t, lane, row);
@@ -239,6 +271,7 @@ dispatch_fp8_passthrough_kernel(DispatchArgs a, int64_t num_items, int num_segme
         if (j < V) v[u] = ld_stream(src + j);
     }
     const bool ue = a.scale_mode == EP_SCALE_UE8M0;
+    prefetch_x_during_layout(a, num_segments, a.H);
     wait_for_layout();
     const int row = slot_row(a.row_of_slot, t, a.K, lane);
     if (seg == 0) write_side_outputs(a, t, lane, row);

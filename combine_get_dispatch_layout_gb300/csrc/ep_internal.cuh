@@ -77,6 +77,7 @@ struct DispatchArgs {
     int64_t scale_ld;
     const void* x_scales;      // fp8 input: [T, H/128] fp32 (uint8 in UE8M0 mode)
     int overlap_layout;        // launch as the preceding layout's programmatic dependent
+    int prefetch_x;            // overlap_layout with x in device memory: prefetch x into L2
 };
 
 cudaError_t launch_dispatch_bf16(const DispatchArgs& a, cudaStream_t stream);

@@ -102,7 +102,9 @@ typedef struct {
                               with x complete before that layout was enqueued; the
                               dispatch then starts on the SMs the layout leaves idle and
                               loads x while the layout runs (programmatic dependent
-                              launch). 0: ordinary stream order.                      */
+                              launch); if x is device memory its first blocks also
+                              prefetch later rows of x into L2 meanwhile.
+                              0: ordinary stream order.                               */
 } ep_dispatch_config_t;
 
 /* Opaque routing handle: owns the slot -> row map [T*K] int32, the layout
