@@ -25,6 +25,8 @@ struct ep_handle {
     cudaStream_t layout_stream = nullptr;
     bool error_latched = false;
     bool meta_known = false;    // host_meta holds the last layout's state words
+    bool captured = false;      // a layout was enqueued under stream capture: graph
+                                // replays rerun it unseen, so nothing is cached
     int layout_kernels = 0;     // kernels the last ep_layout enqueued
     // capacities of the device block
     int64_t cap_slots = 0, cap_chunk_cells = 0, cap_rank_cells = 0, cap_experts = 0;
@@ -63,12 +65,16 @@ void release_block(ep_handle* h) {
     h->cap_slots = h->cap_chunk_cells = h->cap_rank_cells = h->cap_experts = h->cap_keys = 0;
 }
 
-// (Re)allocate the device block for at least the given sizes; zeroes the state words.
+bool capturing(cudaStream_t s);
+
+// (Re)allocate the device block for at least the given sizes; zeroes the state
+// words. Growing allocates and synchronises, which a stream capture forbids.
 ep_status_t ensure_block(ep_handle* h, int64_t slots, int64_t chunk_cells, int64_t rank_cells,
                          int64_t experts, int64_t keys, cudaStream_t stream) {
     if (h->dev_block && slots <= h->cap_slots && chunk_cells <= h->cap_chunk_cells &&
         rank_cells <= h->cap_rank_cells && experts <= h->cap_experts && keys <= h->cap_keys)
         return EP_OK;
+    if (capturing(stream)) return EP_ERR_INVALID_ARG;
     if (h->dev_block) {
         // work already enqueued may still read the old block
         if (cudaDeviceSynchronize() != cudaSuccess) return EP_ERR_CUDA;
@@ -104,11 +110,19 @@ ep_status_t ensure_block(ep_handle* h, int64_t slots, int64_t chunk_cells, int64
     return EP_OK;
 }
 
+bool capturing(cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    return cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone;
+}
+
 // Read the state words written by the last layout. Only layouts write them,
 // so the first read after a layout synchronises its stream and later reads
-// use the host copy until the next layout on this handle.
+// use the host copy until the next layout on this handle (always re-read
+// for a handle whose layout a graph may replay). Not possible while the
+// layout's stream is being captured.
 ep_status_t read_meta(ep_handle* h, int64_t* rows, int32_t* err) {
-    if (!h->meta_known) {
+    if (!h->meta_known || h->captured) {
+        if (capturing(h->layout_stream)) return EP_ERR_INVALID_ARG;
         if (cudaMemcpyAsync(h->host_meta, h->meta, sizeof(int32_t) * ep::kMetaWords, cudaMemcpyDeviceToHost,
                             h->layout_stream) != cudaSuccess)
             return EP_ERR_CUDA;
@@ -118,7 +132,7 @@ ep_status_t read_meta(ep_handle* h, int64_t* rows, int32_t* err) {
     if (rows) *rows = h->host_meta[ep::kMetaRows];
     if (err) *err = h->host_meta[ep::kMetaError];
     // an invalid expert id blocks later calls; a strided overflow only drops slots
-    if (h->host_meta[ep::kMetaError] == EP_ERR_INVALID_EXPERT) h->error_latched = true;
+    h->error_latched = h->host_meta[ep::kMetaError] == EP_ERR_INVALID_EXPERT;
     return EP_OK;
 }
 
@@ -131,11 +145,14 @@ int64_t max_rows_of(int T, int K, int E, int align, int stride = 0) {
 
 // Rows that a consumer buffer must hold: skip the device read when the
 // buffer holds the most a routing can produce.
-ep_status_t check_rows(ep_handle* h, int64_t capacity) {
-    if (h->error_latched) return EP_ERR_INVALID_EXPERT;
+ep_status_t check_rows(ep_handle* h, int64_t capacity, cudaStream_t stream) {
+    // (a replayed layout may have cleared a latched error: graph handles
+    // report it through ep_handle_query only)
+    if (h->error_latched && !h->captured) return EP_ERR_INVALID_EXPERT;
     const int64_t max_rows = max_rows_of(h->T, h->K, h->E, h->align, h->stride);
     if (capacity >= max_rows) return EP_OK;
     if (h->stride > 0) return EP_ERR_CAPACITY;   // a strided buffer must span E * stride rows
+    if (capturing(stream)) return EP_ERR_INVALID_ARG;   // N cannot be read inside a capture
     int64_t n = 0;
     int32_t err = 0;
     ep_status_t st = read_meta(h, &n, &err);
@@ -171,6 +188,7 @@ ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int
     ep_handle* h = *handle;
     bool created = false;
     if (h == nullptr) {
+        if (capturing(s)) return EP_ERR_INVALID_ARG;   // creating a handle allocates
         h = new (std::nothrow) ep_handle();
         if (!h) return EP_ERR_ALLOC;
         created = true;
@@ -187,6 +205,7 @@ ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int
         if (st != EP_OK) return st;
     }
     h->meta_known = false;   // this layout rewrites the state words
+    if (capturing(static_cast<cudaStream_t>(stream))) h->captured = true;
 
     // a non-expand layout runs the expert layout over derived rank keys: the
     // key space is the R ranks (one "expert" per rank)
@@ -307,7 +326,7 @@ ep_status_t ep_nonexpand_recv_topk(ep_handle_t handle, const int64_t* topk_idx, 
         return EP_ERR_INVALID_ARG;
     ep_status_t st = current_device_is(handle);
     if (st != EP_OK) return st;
-    st = check_rows(handle, recv_capacity);
+    st = check_rows(handle, recv_capacity, static_cast<cudaStream_t>(stream));
     if (st != EP_OK) return st;
     return ep::launch_nonexpand_recv_topk(topk_idx, topk_weights, handle->row_of_slot, T, K, E, R, recv_topk_idx,
                                           recv_topk_weights, static_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -348,7 +367,7 @@ ep_status_t ep_dispatch_ex(ep_handle_t handle, const void* x, const void* x_scal
         return EP_ERR_INVALID_ARG;
     ep_status_t st = current_device_is(handle);
     if (st != EP_OK) return st;
-    st = check_rows(handle, recv_capacity);
+    st = check_rows(handle, recv_capacity, static_cast<cudaStream_t>(stream));
     if (st != EP_OK) return st;
 
     ep::DispatchArgs a{};
@@ -416,7 +435,7 @@ ep_status_t ep_combine(ep_handle_t handle, const void* y, int64_t y_rows, int H,
     if (!aligned(y, 16) || !aligned(out, 16) || !aligned(topk_weights, 4)) return EP_ERR_INVALID_ARG;
     ep_status_t st = current_device_is(handle);
     if (st != EP_OK) return st;
-    st = check_rows(handle, y_rows);
+    st = check_rows(handle, y_rows, static_cast<cudaStream_t>(stream));
     if (st != EP_OK) return st;
 
     ep::CombineArgs a{};
@@ -446,11 +465,11 @@ ep_status_t ep_combine_backward(ep_handle_t handle, const void* grad_out, const 
     ep_status_t st = current_device_is(handle);
     if (st != EP_OK) return st;
     if (grad_y) {
-        st = check_rows(handle, grad_y_capacity);
+        st = check_rows(handle, grad_y_capacity, static_cast<cudaStream_t>(stream));
         if (st != EP_OK) return st;
     }
     if (grad_topk_weights) {
-        st = check_rows(handle, y_rows);
+        st = check_rows(handle, y_rows, static_cast<cudaStream_t>(stream));
         if (st != EP_OK) return st;
     }
     ep::CombineBackwardArgs a{};

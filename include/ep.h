@@ -43,6 +43,17 @@
  *    than the most rows the routing can need) synchronises the layout's
  *    stream; later calls use the host copy until the next layout on the
  *    handle.
+ *  - Stream capture (CUDA graphs): ep_layout*, ep_dispatch*, ep_combine* and
+ *    the backward calls can be captured when the handle already exists with
+ *    room for the routing and every buffer holds the most rows the routing
+ *    can need (T*K, plus E*(A-1) when aligned). Inside a capture, a call
+ *    that would allocate (creating or growing a handle) or need N from the
+ *    device (a smaller buffer, ep_handle_query) returns EP_ERR_INVALID_ARG
+ *    and enqueues nothing. A replay reruns the captured layout unseen by the
+ *    host, so a handle whose layout was captured keeps no host copy of N or
+ *    of the error word: ep_handle_query re-reads them after every replay,
+ *    and dispatch / combine on it report an invalid expert id only through
+ *    that query.
  *  - Arguments are checked on the host first. A failed check returns
  *    EP_ERR_INVALID_ARG and enqueues nothing.
  *  - Row buffers (x, recv_x, y, out) must be 16-byte aligned.

@@ -1183,3 +1183,116 @@ def test_fp8_quotients_near_e4m3_midpoints(ep):
     inp = gi.Inputs(w=_workload(T, H, 1, 1, 1), seed=0, x=x, topk_idx=np.zeros((T, 1), np.int64),
                     topk_weights=np.ones((T, 1), np.float32), y=None, num_valid=T)
     full_path(ep, inp, fp8=True)
+
+
+# ------------------------------------------------------------------ CUDA graphs
+
+@pytest.mark.parametrize("name,fp8", [("decode", False), ("skewed", False), ("tiny", True)])
+def test_graph_capture_replays_the_step(ep, name, fp8):
+    """layout -> dispatch (overlapped) -> combine captured once into a CUDA
+    graph (handle reused, buffers of T*K rows: no allocation, no host wait)
+    and replayed for new routings written into the same input buffers."""
+    inp = gi.make(name, 50, T=600 if name == "skewed" else None)
+    w = inp.w
+    cap = w.T * w.K
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        idx = _dev(inp.topk_idx)
+        x = _dev(inp.x.view(np.int16), torch.bfloat16)
+        wt = _dev(inp.topk_weights)
+        y = torch.zeros(cap, w.H, dtype=torch.bfloat16, device="cuda")
+        o = [torch.empty(w.E, dtype=torch.int32, device="cuda"), torch.empty(w.R, dtype=torch.int32, device="cuda"),
+             torch.empty(w.T, w.R, dtype=torch.uint8, device="cuda"),
+             torch.empty(w.E + 1, dtype=torch.int32, device="cuda")]
+        recv = torch.empty(cap, w.H, dtype=torch.uint8 if fp8 else torch.bfloat16, device="cuda")
+        sc = torch.empty(cap, w.H // 128, dtype=torch.float32, device="cuda") if fp8 else None
+        out = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
+        h = ep.ep_layout(idx, w.E, w.R, *o)          # creates the handle (allocates) before capture
+    s.synchronize()
+
+    def step():
+        ep.ep_layout(idx, w.E, w.R, *o, handle=h)
+        ep.ep_dispatch_ex(h, x, recv, cap, out_dtype=ep.EP_DTYPE_FP8_E4M3 if fp8 else ep.EP_DTYPE_BF16,
+                          recv_scales=sc, overlap_layout=True)
+        ep.ep_combine(h, y, out, topk_weights=wt)
+
+    with torch.cuda.stream(s):
+        step()                                        # warm-up outside the capture
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    rng = np.random.default_rng(51)
+    for rep in range(3):
+        # new routing and weights in the captured buffers, and expert outputs
+        # for the rows this routing produces
+        idx_n = np.argsort(rng.random((w.T, w.E)), axis=1)[:, :w.K].astype(np.int64)
+        idx_n[rng.random((w.T, w.K)) < 0.1 * rep] = -1
+        wt_n = rng.random((w.T, w.K)).astype(np.float32)
+        ref = oracle.layout(idx_n, w.E, w.R)
+        n = int(ref["expert_offsets"][-1])
+        y_n = gi.normal_bf16(np.random.SeedSequence(52 + rep), n, w.H)
+        with torch.cuda.stream(s):
+            idx.copy_(torch.from_numpy(idx_n))
+            wt.copy_(torch.from_numpy(wt_n))
+            y[:n].copy_(torch.from_numpy(y_n.view(np.int16)).view(torch.bfloat16))
+        g.replay()
+        s.synchronize()
+        np.testing.assert_array_equal(o[3].cpu().numpy(), ref["expert_offsets"])
+        np.testing.assert_array_equal(o[2].cpu().numpy(), ref["is_token_in_rank"])
+        np.testing.assert_array_equal(o[1].cpu().numpy(), ref["num_tokens_per_rank"])
+        if fp8:
+            r_q, r_s, _, _ = oracle.dispatch_e4m3(inp.x, ref["row_of_slot"], n)
+            np.testing.assert_array_equal(recv[:n].cpu().numpy(), r_q)
+            np.testing.assert_array_equal(sc[:n].cpu().numpy().view(np.uint32), r_s.view(np.uint32))
+        else:
+            r_x, _, _ = oracle.dispatch_bf16(inp.x, ref["row_of_slot"], n)
+            np.testing.assert_array_equal(_u16(recv[:n]), r_x)
+        np.testing.assert_array_equal(_u16(out), oracle.combine(y_n, ref["row_of_slot"], wt_n))
+        assert ep.ep_handle_query(h)[0] == n
+    del g
+    h.destroy()
+
+
+def test_capture_refuses_host_waits_and_allocation(ep):
+    """Inside a stream capture, calls that would allocate or wait for the
+    device are refused with EP_ERR_INVALID_ARG and enqueue nothing; the rest
+    of the capture is intact and replays correctly."""
+    inp = gi.make("decode", 54)
+    w = inp.w
+    cap = w.T * w.K
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        idx = _dev(inp.topk_idx)
+        x = _dev(inp.x.view(np.int16), torch.bfloat16)
+        o = [torch.empty(w.E, dtype=torch.int32, device="cuda"), torch.empty(w.R, dtype=torch.int32, device="cuda"),
+             torch.empty(w.T, w.R, dtype=torch.uint8, device="cuda"),
+             torch.empty(w.E + 1, dtype=torch.int32, device="cuda")]
+        small = torch.empty(cap - 1, w.H, dtype=torch.bfloat16, device="cuda")
+        full = torch.full((cap, w.H), -3.0, dtype=torch.bfloat16, device="cuda")
+        h = ep.ep_layout(idx, w.E, w.R, *o)
+    s.synchronize()
+    statuses = []
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        ep.ep_layout(idx, w.E, w.R, *o, handle=h)
+        for call in (lambda: ep.ep_dispatch(h, x, ep.EP_DTYPE_BF16, small, cap - 1),
+                     lambda: ep.ep_layout(idx, w.E, w.R, *o),
+                     lambda: ep.ep_handle_query(h)):
+            try:
+                call()
+                statuses.append(ep.EP_OK)
+            except ep.EPError as e:
+                statuses.append(e.status)
+        ep.ep_dispatch(h, x, ep.EP_DTYPE_BF16, full, cap)
+    assert statuses == [ep.EP_ERR_INVALID_ARG] * 3
+    full.fill_(-3.0)
+    g.replay()
+    s.synchronize()
+    ref = oracle.layout(inp.topk_idx, w.E, w.R)
+    n = int(ref["expert_offsets"][-1])
+    r_x, _, _ = oracle.dispatch_bf16(inp.x, ref["row_of_slot"], n)
+    np.testing.assert_array_equal(_u16(full[:n]), r_x)
+    assert ep.ep_handle_query(h)[0] == n
+    del g
+    h.destroy()
