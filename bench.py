@@ -663,6 +663,33 @@ def other_configs(torch, ep, dev, stream, args, rank, peak, reps):
         lambda: ep.ep_dispatch(h, t["x"], ep.EP_DTYPE_BF16, t["recv"], wd.E * cap, stream=stream),
         lambda: ep.ep_combine(h, y, t["out"], topk_weights=t["w"], stream=stream)], flush=flush)
     h.destroy()
+    # the same step captured once into a CUDA graph (kernels chained by
+    # programmatic edges) and replayed: no host launch cost per step, warm L2
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        h = ep.ep_layout_strided(t["idx"], wd.E, wd.R, cap, t["cnt"], t["ntr"], t["itr"], t["off"], stream=stream)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            ep.ep_layout_strided(t["idx"], wd.E, wd.R, cap, t["cnt"], t["ntr"], t["itr"], t["off"], handle=h,
+                                 stream=stream)
+            ep.ep_dispatch_ex(h, t["x"], t["recv"], wd.E * cap, out_dtype=ep.EP_DTYPE_BF16, overlap_layout=True,
+                              stream=stream)
+            ep.ep_combine(h, y, t["out"], topk_weights=t["w"], stream=stream)
+        for _ in range(5):
+            g.replay()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+    stream.synchronize()
+    ms_g = ev0.elapsed_time(ev1) / reps
+    del g
+    h.destroy()
+    out["decode_ll_step_graph"] = {
+        "workload": f"decode T={wd.T} H={wd.H} E={wd.E} K={wd.K} R={wd.R}, strided layout cap={cap}, "
+                    "one CUDA graph per step (layout, overlapped dispatch, combine), warm L2",
+        "step_us": round(ms_g * 1e3, 2), "tokens_per_s": round(wd.T / (ms_g * 1e-3), 1)}
     out["decode_ll_step_l2_flushed"] = {
         "workload": f"decode T={wd.T} H={wd.H} E={wd.E} K={wd.K} R={wd.R}, strided layout cap={cap}, "
                     f"L2 flushed ({2 * l2 >> 20} MiB written) before each iteration",
