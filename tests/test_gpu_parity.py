@@ -1296,3 +1296,60 @@ def test_capture_refuses_host_waits_and_allocation(ep):
     assert ep.ep_handle_query(h)[0] == n
     del g
     h.destroy()
+
+
+@pytest.mark.parametrize("kind", ["bf16", "e4m3", "e5m2", "passthrough"])
+def test_overlapped_dispatch_ragged_shapes(ep, kind):
+    """Overlapped dispatch (programmatic dependent of the layout, with the L2
+    prefetch of x) on a ragged token count and a row that is not a whole
+    number of work items: the prefetch window is clamped to x and every
+    kernel variant gives the oracle's bytes."""
+    H = 4104 if kind == "bf16" else 4224
+    w = _workload(5001, H, 64, 6, 4, routing="zipf", drop_p=0.05)
+    inp = gi.make(w, 55, with_y=False)
+    ref = oracle.layout(inp.topk_idx, w.E, w.R)
+    n = int(ref["expert_offsets"][-1])
+    nb = H // 128
+    h = _layout_dev(ep, inp)
+    idx = _dev(inp.topk_idx)
+    o = [torch.empty(w.E, dtype=torch.int32, device="cuda"), torch.empty(w.R, dtype=torch.int32, device="cuda"),
+         torch.empty(w.T, w.R, dtype=torch.uint8, device="cuda"), torch.empty(w.E + 1, dtype=torch.int32, device="cuda")]
+    if kind == "passthrough":
+        codes = np.zeros((w.T, H), np.uint8)
+        scales = np.zeros((w.T, nb), np.float32)
+        for t in range(w.T):
+            codes[t], scales[t] = oracle.quant_row_e4m3(inp.x[t])
+        x, xs = _dev(codes), _dev(scales)
+    else:
+        x, xs = _dev(inp.x.view(np.int16)), None
+    bf16 = kind == "bf16"
+    cap = w.T * w.K
+    recv = torch.full((cap, H), SENT16 if bf16 else SENT8, dtype=torch.int16 if bf16 else torch.uint8,
+                      device="cuda")
+    sc = None if bf16 else torch.full((cap, nb), -1.0, dtype=torch.float32, device="cuda")
+    fmt = {"bf16": ep.EP_DTYPE_BF16, "e4m3": ep.EP_DTYPE_FP8_E4M3, "e5m2": ep.EP_DTYPE_FP8_E5M2,
+           "passthrough": ep.EP_DTYPE_FP8_E4M3}[kind]
+    for _ in range(2):
+        ep.ep_layout(idx, w.E, w.R, *o, handle=h)
+        ep.ep_dispatch_ex(h, x, recv, cap, out_dtype=fmt,
+                          in_dtype=ep.EP_DTYPE_FP8_E4M3 if kind == "passthrough" else ep.EP_DTYPE_BF16,
+                          x_scales=xs, recv_scales=sc, H=H, overlap_layout=True)
+    torch.cuda.synchronize()
+    got = recv.cpu().numpy()
+    if bf16:
+        r_x, _, _ = oracle.dispatch_bf16(inp.x, ref["row_of_slot"], n)
+        np.testing.assert_array_equal(got[:n].view(np.uint16), r_x)
+        assert (got[n:] == SENT16).all()
+        h.destroy()
+        return
+    if kind == "passthrough":
+        r_q = oracle.dispatch_rows(codes, ref["row_of_slot"], n)
+        r_s = oracle.dispatch_rows(scales, ref["row_of_slot"], n)
+    elif kind == "e5m2":
+        r_q, r_s = oracle.dispatch_e5m2(inp.x, ref["row_of_slot"], n)
+    else:
+        r_q, r_s, _, _ = oracle.dispatch_e4m3(inp.x, ref["row_of_slot"], n)
+    np.testing.assert_array_equal(got[:n], r_q)
+    assert (got[n:] == SENT8).all()
+    np.testing.assert_array_equal(sc.cpu().numpy()[:n].view(np.uint32), r_s.view(np.uint32))
+    h.destroy()
