@@ -36,6 +36,10 @@
 
 #include <cooperative_groups.h>
 
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "ep_internal.cuh"
 
 namespace cg = cooperative_groups;
@@ -639,40 +643,58 @@ LayoutPlan make_layout_plan(int T, int K, int E, int R) {
 
 namespace {
 
-// Largest cluster (16, else 8) that this device can co-schedule for the
-// single-launch kernel with the given block; 0 if none. Cached per device.
-int cluster_ctas_for(int dev, int warps, size_t smem) {
-    static int cached[64][3] = {};   // [dev][0]=ctas+1, [1]=warps, [2]=smem
-    if (cached[dev][0] && cached[dev][1] == warps && cached[dev][2] == static_cast<int>(smem))
-        return cached[dev][0] - 1;
+// Per-device launch state, shared by every handle and host thread.
+struct DeviceLaunchState {
+    bool attrs_set = false;
+    std::map<std::pair<int, size_t>, int> cluster_ctas;   // (warps, smem) -> CTAs, 0 = none
+};
+std::mutex g_launch_mu;
+DeviceLaunchState g_launch_state[64];
+
+// Opt-ins the layout kernels need, set once per device (the current one):
+// dynamic shared memory up to the largest any plan uses, and cluster sizes
+// above the portable 8.
+cudaError_t set_kernel_attributes(DeviceLaunchState& st) {
+    if (st.attrs_set) return cudaSuccess;
+    const int budget = static_cast<int>(kClusterSmemBudget);
+    cudaError_t err = cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(layout_assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(layout_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(layout_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (err == cudaSuccess) st.attrs_set = true;
+    return err;
+}
+
+// Largest cluster (16, else 8) that the device can co-schedule for the
+// single-launch kernel with the given block; 0 if none. Cached.
+int cluster_ctas_for(DeviceLaunchState& st, int warps, size_t smem) {
+    const auto key = std::make_pair(warps, smem);
+    const auto it = st.cluster_ctas.find(key);
+    if (it != st.cluster_ctas.end()) return it->second;
     int found = 0;
-    if (cudaFuncSetAttribute(layout_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-            cudaSuccess &&
-        cudaFuncSetAttribute(layout_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) == cudaSuccess) {
-        for (int c : {16, 8}) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(c);
-            cfg.blockDim = dim3(warps * 32);
-            cfg.dynamicSmemBytes = smem;
-            cudaLaunchAttribute attr;
-            attr.id = cudaLaunchAttributeClusterDimension;
-            attr.val.clusterDim.x = c;
-            attr.val.clusterDim.y = 1;
-            attr.val.clusterDim.z = 1;
-            cfg.attrs = &attr;
-            cfg.numAttrs = 1;
-            int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, layout_cluster_kernel, &cfg) == cudaSuccess && n > 0) {
-                found = c;
-                break;
-            }
+    for (int c : {16, 8}) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(c);
+        cfg.blockDim = dim3(warps * 32);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = c;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, layout_cluster_kernel, &cfg) == cudaSuccess && n > 0) {
+            found = c;
+            break;
         }
     }
     cudaGetLastError();   // a refused probe must not leak into the caller's error state
-    cached[dev][0] = found + 1;
-    cached[dev][1] = warps;
-    cached[dev][2] = static_cast<int>(smem);
+    st.cluster_ctas[key] = found;
     return found;
 }
 
@@ -680,24 +702,23 @@ int cluster_ctas_for(int dev, int warps, size_t smem) {
 
 cudaError_t launch_layout(const LayoutPlan& plan, const LayoutArgs& a, cudaStream_t stream, int* kernels) {
     if (kernels) *kernels = 0;
-    // the shared-memory opt-in is per device
-    static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        err = cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    int ctas = 0;
+    const int64_t slots = static_cast<int64_t>(plan.T) * plan.K;
+    const bool try_cluster = slots <= kClusterMaxSlots && plan.smem_cluster > 0;
+    {
+        std::lock_guard<std::mutex> lock(g_launch_mu);
+        DeviceLaunchState& st = g_launch_state[dev];
+        err = set_kernel_attributes(st);
         if (err != cudaSuccess) return err;
-        err = cudaFuncSetAttribute(layout_assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        if (err != cudaSuccess) return err;
-        attr_set[dev] = true;
+        if (try_cluster && plan.num_blocks > 0) ctas = cluster_ctas_for(st, plan.cl_warps, plan.smem_cluster);
     }
     if (plan.num_blocks == 0) return cudaSuccess;
 
-    const int64_t slots = static_cast<int64_t>(plan.T) * plan.K;
-    if (slots <= kClusterMaxSlots && plan.smem_cluster > 0) {
-        const int ctas = cluster_ctas_for(dev, plan.cl_warps, plan.smem_cluster);
+    if (try_cluster) {
         const int warps = ctas * plan.cl_warps;
         const int ct = warps > 0 ? (plan.T + warps - 1) / warps : 0;
         // each warp's chunk must fit kMaxRounds rounds (and the token-mask area)

@@ -1353,3 +1353,49 @@ def test_overlapped_dispatch_ragged_shapes(ep, kind):
     assert (got[n:] == SENT8).all()
     np.testing.assert_array_equal(sc.cpu().numpy()[:n].view(np.uint32), r_s.view(np.uint32))
     h.destroy()
+
+
+def test_two_host_threads_with_their_own_handles(ep):
+    """Handles used from two host threads at once (one handle per thread,
+    one stream each), alternating shapes so the shared launch-state cache
+    takes new entries while the other thread launches."""
+    import threading
+    cases = [gi.make("decode", 60 + i, with_y=False) for i in range(2)] + \
+            [gi.make("skewed", 62 + i, T=3000, with_y=False) for i in range(2)]
+    refs = [oracle.layout(c.topk_idx, c.w.E, c.w.R) for c in cases]
+    errors = []
+
+    def worker(order):
+        try:
+            s = torch.cuda.Stream()
+            h = None
+            for rep in range(6):
+                for ci in order:
+                    c, ref = cases[ci], refs[ci]
+                    w = c.w
+                    with torch.cuda.stream(s):
+                        idx, x = _dev(c.topk_idx), _dev(c.x.view(np.int16), torch.bfloat16)
+                        o = [torch.empty(w.E, dtype=torch.int32, device="cuda"),
+                             torch.empty(w.R, dtype=torch.int32, device="cuda"),
+                             torch.empty(w.T, w.R, dtype=torch.uint8, device="cuda"),
+                             torch.empty(w.E + 1, dtype=torch.int32, device="cuda")]
+                        recv = torch.empty(w.T * w.K, w.H, dtype=torch.bfloat16, device="cuda")
+                        h = ep.ep_layout(idx, w.E, w.R, *o, handle=h, stream=s)
+                        ep.ep_dispatch(h, x, ep.EP_DTYPE_BF16, recv, w.T * w.K, stream=s)
+                    s.synchronize()
+                    n = int(ref["expert_offsets"][-1])
+                    if not np.array_equal(o[3].cpu().numpy(), ref["expert_offsets"]):
+                        errors.append(("offsets", ci))
+                    r_x, _, _ = oracle.dispatch_bf16(c.x, ref["row_of_slot"], n)
+                    if not np.array_equal(_u16(recv[:n]), r_x):
+                        errors.append(("rows", ci))
+            h.destroy()
+        except Exception as e:   # surfaced below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(o,)) for o in ([0, 2, 1, 3], [3, 1, 2, 0])]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert errors == []
