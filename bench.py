@@ -152,9 +152,10 @@ def smi_id(local: int) -> str:
     return str(local)
 
 
-def read_traffic(kernel: str):
+def read_traffic(kernel: str, T: int):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if
-    the kernel source has not changed since the capture (else None)."""
+    the capture was of this token count and the kernel source has not changed
+    since (else None)."""
     import hashlib
     import re
 
@@ -162,14 +163,14 @@ def read_traffic(kernel: str):
     if not os.path.exists(path):
         return None
     txt = open(path).read()
-    m = re.search(rf"<!-- traffic kernel={kernel} bytes=(\d+) src_sha256=([0-9a-f]+) -->", txt)
-    if not m:
+    m = re.search(rf"<!-- traffic kernel={kernel} T=(\d+) bytes=(\d+) src_sha256=([0-9a-f]+) -->", txt)
+    if not m or int(m.group(1)) != T:
         return None
     src = {"dispatch_bf16": "ep_dispatch.cu", "combine": "ep_combine.cu"}.get(kernel)
     if src is None:
         return None
     h = hashlib.sha256(open(os.path.join(ROOT, "combine_get_dispatch_layout_gb300", "csrc", src), "rb").read())
-    return int(m.group(1)) if h.hexdigest()[:16] == m.group(2) else None
+    return int(m.group(2)) if h.hexdigest()[:16] == m.group(3) else None
 
 
 def aggregate_over_ranks(local_ms: float, local_bytes: int, device=None):
@@ -598,7 +599,7 @@ def gpu_arm(args, rank, world, local):
         },
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": read_traffic(dominant)},
+                     "traffic": read_traffic(dominant, T)},
         "e2e": {"value": round(job_bytes / (e2e["ms_per_step"] * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e["ms_per_step"], 4), "steps": e2e["steps"], "how": e2e["how"]},

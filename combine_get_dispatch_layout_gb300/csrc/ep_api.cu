@@ -11,6 +11,8 @@
 #include <cstring>
 #include <new>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "ep_internal.cuh"
 
 struct ep_handle {
@@ -44,6 +46,16 @@ struct ep_handle {
 };
 
 namespace {
+
+// A named NVTX range around each public call, so that profilers (ncu
+// --nvtx-include, Nsight Systems) can attribute its kernels to it; with no
+// tool attached a push is a pointer check.
+struct ApiRange {
+    explicit ApiRange(const char* name) { nvtxRangePushA(name); }
+    ~ApiRange() { nvtxRangePop(); }
+    ApiRange(const ApiRange&) = delete;
+    ApiRange& operator=(const ApiRange&) = delete;
+};
 
 int default_alloc(void** p, size_t bytes) { return cudaMalloc(p, bytes) == cudaSuccess ? 0 : 1; }
 int default_free(void* p) { return cudaFree(p) == cudaSuccess ? 0 : 1; }
@@ -281,6 +293,7 @@ ep_status_t ep_layout(const int64_t* topk_idx, int T, int K, int E, int R,
                       uint8_t* is_token_in_rank, int32_t* expert_offsets,
                       ep_alloc_fn alloc_fn, ep_free_fn free_fn,
                       ep_handle_t* handle, void* stream) {
+    ApiRange range("ep_layout");
     return layout_impl(topk_idx, T, K, E, R, 1, 0, false, num_tokens_per_expert, num_tokens_per_rank, is_token_in_rank,
                        expert_offsets, alloc_fn, free_fn, handle, stream);
 }
@@ -290,6 +303,7 @@ ep_status_t ep_layout_aligned(const int64_t* topk_idx, int T, int K, int E, int 
                               uint8_t* is_token_in_rank, int32_t* expert_offsets,
                               ep_alloc_fn alloc_fn, ep_free_fn free_fn,
                               ep_handle_t* handle, void* stream) {
+    ApiRange range("ep_layout_aligned");
     return layout_impl(topk_idx, T, K, E, R, expert_alignment, 0, false, num_tokens_per_expert, num_tokens_per_rank,
                        is_token_in_rank, expert_offsets, alloc_fn, free_fn, handle, stream);
 }
@@ -299,6 +313,7 @@ ep_status_t ep_layout_strided(const int64_t* topk_idx, int T, int K, int E, int 
                               uint8_t* is_token_in_rank, int32_t* expert_offsets,
                               ep_alloc_fn alloc_fn, ep_free_fn free_fn,
                               ep_handle_t* handle, void* stream) {
+    ApiRange range("ep_layout_strided");
     if (expert_capacity < 1) return EP_ERR_INVALID_ARG;
     return layout_impl(topk_idx, T, K, E, R, 1, expert_capacity, false, num_tokens_per_expert, num_tokens_per_rank,
                        is_token_in_rank, expert_offsets, alloc_fn, free_fn, handle, stream);
@@ -309,6 +324,7 @@ ep_status_t ep_layout_nonexpand(const int64_t* topk_idx, int T, int K, int E, in
                                 uint8_t* is_token_in_rank, int32_t* rank_offsets,
                                 ep_alloc_fn alloc_fn, ep_free_fn free_fn,
                                 ep_handle_t* handle, void* stream) {
+    ApiRange range("ep_layout_nonexpand");
     return layout_impl(topk_idx, T, K, E, R, 1, 0, true, num_tokens_per_expert, num_tokens_per_rank,
                        is_token_in_rank, rank_offsets, alloc_fn, free_fn, handle, stream);
 }
@@ -316,6 +332,7 @@ ep_status_t ep_layout_nonexpand(const int64_t* topk_idx, int T, int K, int E, in
 ep_status_t ep_nonexpand_recv_topk(ep_handle_t handle, const int64_t* topk_idx, const float* topk_weights, int E,
                                    int64_t* recv_topk_idx, float* recv_topk_weights, int64_t recv_capacity,
                                    void* stream) {
+    ApiRange range("ep_nonexpand_recv_topk");
     if (!handle) return EP_ERR_INVALID_ARG;
     const int T = handle->T, K = handle->K, R = handle->R;
     if (E < 1 || E > EP_MAX_EXPERTS || E % R != 0 || recv_capacity < 0) return EP_ERR_INVALID_ARG;
@@ -338,6 +355,7 @@ ep_status_t ep_dispatch_ex(ep_handle_t handle, const void* x, const void* x_scal
                            const ep_dispatch_config_t* config, const float* topk_weights,
                            void* recv_x, void* recv_scales, int32_t* recv_src_token,
                            float* recv_weights, int64_t recv_capacity, void* stream) {
+    ApiRange range("ep_dispatch_ex");
     if (!handle) return EP_ERR_INVALID_ARG;
     ep_dispatch_config_t cfg{};
     if (config) cfg = *config;
@@ -419,6 +437,7 @@ ep_status_t ep_dispatch(ep_handle_t handle, const void* x, int H, ep_dtype_t out
                         const float* topk_weights,
                         void* recv_x, float* recv_scales, int32_t* recv_src_token,
                         float* recv_weights, int64_t recv_capacity, void* stream) {
+    ApiRange range("ep_dispatch");
     ep_dispatch_config_t cfg{};
     cfg.in_dtype = EP_DTYPE_BF16;
     cfg.out_dtype = out_dtype;
@@ -428,6 +447,7 @@ ep_status_t ep_dispatch(ep_handle_t handle, const void* x, int H, ep_dtype_t out
 
 ep_status_t ep_combine(ep_handle_t handle, const void* y, int64_t y_rows, int H,
                        const float* topk_weights, void* out, void* stream) {
+    ApiRange range("ep_combine");
     if (!handle) return EP_ERR_INVALID_ARG;
     if (H < 8 || H % 8 != 0 || y_rows < 0) return EP_ERR_INVALID_ARG;
     if (handle->T > 0 && !out) return EP_ERR_INVALID_ARG;
@@ -454,6 +474,7 @@ ep_status_t ep_combine(ep_handle_t handle, const void* y, int64_t y_rows, int H,
 ep_status_t ep_combine_backward(ep_handle_t handle, const void* grad_out, const void* y, int64_t y_rows, int H,
                                 const float* topk_weights, void* grad_y, int64_t grad_y_capacity,
                                 float* grad_topk_weights, void* stream) {
+    ApiRange range("ep_combine_backward");
     if (!handle) return EP_ERR_INVALID_ARG;
     if (H < 8 || H % 8 != 0 || y_rows < 0 || grad_y_capacity < 0) return EP_ERR_INVALID_ARG;
     if (handle->T > 0 && !grad_out) return EP_ERR_INVALID_ARG;
@@ -494,6 +515,7 @@ ep_status_t ep_combine_backward(ep_handle_t handle, const void* grad_out, const 
 ep_status_t ep_dispatch_backward(ep_handle_t handle, const void* grad_recv, int64_t grad_rows, int H,
                                  const float* grad_recv_weights, void* grad_x, float* grad_topk_weights,
                                  void* stream) {
+    ApiRange range("ep_dispatch_backward");
     if (!handle) return EP_ERR_INVALID_ARG;
     if (grad_topk_weights && !grad_recv_weights) return EP_ERR_INVALID_ARG;
     if (!aligned(grad_recv_weights, 4) || !aligned(grad_topk_weights, 4)) return EP_ERR_INVALID_ARG;
@@ -508,6 +530,7 @@ ep_status_t ep_dispatch_backward(ep_handle_t handle, const void* grad_recv, int6
 
 ep_status_t ep_topk_to_routing_map(const int64_t* topk_idx, const float* topk_weights, int T, int K, int E,
                                    uint8_t* routing_map, float* probs, int32_t* device_error, void* stream) {
+    ApiRange range("ep_topk_to_routing_map");
     if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS) return EP_ERR_INVALID_ARG;
     if (T > 0 && (!topk_idx || !routing_map)) return EP_ERR_INVALID_ARG;
     if (probs && !topk_weights) return EP_ERR_INVALID_ARG;
@@ -522,6 +545,7 @@ ep_status_t ep_topk_to_routing_map(const int64_t* topk_idx, const float* topk_we
 
 ep_status_t ep_routing_map_to_topk(const uint8_t* routing_map, const float* probs, int T, int E, int K,
                                    int64_t* topk_idx, float* topk_weights, int32_t* device_error, void* stream) {
+    ApiRange range("ep_routing_map_to_topk");
     if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS) return EP_ERR_INVALID_ARG;
     if (T > 0 && (!topk_idx || !routing_map)) return EP_ERR_INVALID_ARG;
     if (!aligned(topk_idx, 8) || !aligned(topk_weights, 4) || !aligned(probs, 4) || !aligned(device_error, 4))
@@ -534,6 +558,7 @@ ep_status_t ep_routing_map_to_topk(const uint8_t* routing_map, const float* prob
 }
 
 ep_status_t ep_handle_query(ep_handle_t handle, int64_t* num_recv_rows, int32_t* device_error) {
+    ApiRange range("ep_handle_query");
     if (!handle) return EP_ERR_INVALID_ARG;
     ep_status_t st = current_device_is(handle);
     if (st != EP_OK) return st;
