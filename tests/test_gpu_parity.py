@@ -216,6 +216,8 @@ def _workload(T, H, E, K, R, **kw):
     _workload(500, 128, 256, 8, 32, drop_p=0.1),         # R = 32: every rank bit in use
     _workload(21504, 64, 64, 6, 4, routing="zipf"),      # K = 6: largest single-cluster chunk
     _workload(21505, 64, 64, 6, 4, routing="zipf"),      # one token more: multi-block path
+    _workload(8000, 128, 4096, 8, 1024, drop_p=0.02),    # maximum E and R, 64k slots (multi-block)
+    _workload(9000, 128, 2048, 32, 256, drop_p=0.02),    # maximum top-k above 2^18 slots
 ])
 def test_edge_shapes(ep, w):
     inp = gi.make(w, 11)
