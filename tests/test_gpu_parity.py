@@ -974,6 +974,50 @@ def test_routing_map_conversions(ep, name, T):
     full_path(ep, inp2, fp8=(w.H % 128 == 0))
 
 
+@pytest.mark.parametrize("E,K,T,offset", [
+    (12, 3, 700, 0),       # E % 8 != 0: scalar kernels
+    (256, 8, 1000, 1),     # map and probs at odd offsets: scalar kernels
+    (4096, 32, 300, 0),    # 16 blocks of 256 experts per token
+    (40, 6, 999, 0),       # a partial block
+    (64, 4, 513, 0),
+])
+def test_routing_map_vector_and_scalar_forms(ep, E, K, T, offset):
+    """Both conversion directions against the oracle: random top-k with
+    duplicate experts and dropped slots; random dense maps with any non-zero
+    byte meaning routed, some rows holding more than K experts."""
+    rng = np.random.default_rng(E * 100 + K)
+    idx = rng.integers(-1, E, (T, K)).astype(np.int64)
+    wts = rng.random((T, K)).astype(np.float32)
+    r_map, r_probs, _ = oracle.topk_to_routing_map(idx, wts, E)
+    mbuf = torch.full((T * E + 64,), SENT8, dtype=torch.uint8, device="cuda")
+    pbuf = torch.full((T * E + 16,), -1.0, dtype=torch.float32, device="cuda")
+    rm = mbuf[offset:offset + T * E].view(T, E)
+    pr = pbuf[offset:offset + T * E].view(T, E)
+    err = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    ep.ep_topk_to_routing_map(_dev(idx), E, rm, topk_weights=_dev(wts), probs=pr, device_error=err)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(rm.cpu().numpy(), r_map)
+    np.testing.assert_array_equal(pr.cpu().numpy().view(np.uint32), r_probs.view(np.uint32))
+    assert err.item() == 0
+    assert (mbuf[:offset] == SENT8).all() and (mbuf[offset + T * E:] == SENT8).all()
+
+    dense = (rng.random((T, E)) < min(1.0, 1.5 * K / E)) * rng.integers(1, 256, (T, E))
+    dense = dense.astype(np.uint8)
+    probs = rng.random((T, E)).astype(np.float32)
+    r_idx, r_w, st = oracle.routing_map_to_topk(dense, probs, K)
+    rm.copy_(torch.from_numpy(dense))
+    pr.copy_(torch.from_numpy(probs))
+    out_i = torch.full((T, K), -9, dtype=torch.int64, device="cuda")
+    out_w = torch.full((T, K), -1.0, dtype=torch.float32, device="cuda")
+    ep.ep_routing_map_to_topk(rm, K, out_i, probs=pr, topk_weights=out_w, device_error=err)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out_i.cpu().numpy(), r_idx)
+    np.testing.assert_array_equal(out_w.cpu().numpy().view(np.uint32), r_w.view(np.uint32))
+    over = ((dense != 0).sum(axis=1) > K).any()
+    assert err.item() == (ep.EP_ERR_CAPACITY if over else 0)
+    assert (st != oracle.OK) == over          # the oracle flags the same inputs
+
+
 def test_routing_map_errors(ep):
     idx = torch.tensor([[0, 9], [1, -3]], dtype=torch.int64, device="cuda")
     rm = torch.empty((2, 8), dtype=torch.uint8, device="cuda")
