@@ -414,22 +414,23 @@ ep_status_t ep_dispatch_ex(ep_handle_t handle, const void* x, const void* x_scal
         cudaGetLastError();
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (handle->align > 1) {
+        // the dispatch grid also zeroes the pad rows (at most align - 1 per expert)
+        a.pad_counts = handle->counts;
+        a.pad_offsets = handle->offsets;
+        a.pad_experts = handle->E;
+        a.pad_max = handle->align - 1;
+        if (fp8) {
+            a.pad_scales.ptr = recv_scales;
+            a.pad_scales.nb = H / 128;
+            a.pad_scales.bytes = static_cast<int>(scale_bytes);
+            a.pad_scales.col_major = a.scale_col_major;
+            a.pad_scales.ld = cfg.scales_ld;
+        }
+    }
     cudaError_t err = fp8_in ? ep::launch_dispatch_fp8_passthrough(a, s)
                       : fp8  ? ep::launch_dispatch_fp8(a, s)
                              : ep::launch_dispatch_bf16(a, s);
-    if (err == cudaSuccess && handle->align > 1 && handle->T > 0) {
-        ep::PadScales ps;
-        if (fp8) {
-            ps.ptr = recv_scales;
-            ps.nb = H / 128;
-            ps.bytes = static_cast<int>(scale_bytes);
-            ps.col_major = a.scale_col_major;
-            ps.ld = cfg.scales_ld;
-        }
-        err = ep::launch_fill_pad_rows(handle->counts, handle->offsets, handle->E,
-                                       fp8 ? static_cast<int64_t>(H) : static_cast<int64_t>(H) * 2, recv_x, ps,
-                                       recv_src_token, recv_weights, s, handle->align - 1);
-    }
     return err == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
 

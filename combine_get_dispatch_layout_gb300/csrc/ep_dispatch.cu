@@ -53,6 +53,45 @@ __device__ __forceinline__ void wait_for_layout() {
     asm volatile("griddepcontrol.launch_dependents;");
 }
 
+// Zero pad row `item` of an aligned layout (item = expert * max_pad + i, one
+// warp each): row offsets[e] + counts[e] + i if it is below offsets[e + 1].
+__device__ __forceinline__ void zero_pad_row(const int32_t* counts, const int32_t* offsets, int E, int max_pad,
+                                             int64_t item, int64_t row_bytes, char* recv, const PadScales& sc,
+                                             int32_t* src, float* weights, int lane) {
+    const int e = static_cast<int>(item / max_pad);
+    const int i = static_cast<int>(item - static_cast<int64_t>(e) * max_pad);
+    if (e >= E) return;
+    const int64_t row = static_cast<int64_t>(offsets[e]) + counts[e] + i;
+    if (row >= offsets[e + 1]) return;
+    int4* d = reinterpret_cast<int4*>(recv + row * row_bytes);   // row_bytes % 16 == 0
+    for (int64_t j = lane; j < row_bytes / 16; j += 32) d[j] = make_int4(0, 0, 0, 0);
+    if (sc.ptr)
+        for (int b = lane; b < sc.nb; b += 32) {
+            const int64_t si = sc.col_major ? static_cast<int64_t>(b) * sc.ld + row : row * sc.nb + b;
+            if (sc.bytes == 1) static_cast<uint8_t*>(sc.ptr)[si] = 0;
+            else static_cast<float*>(sc.ptr)[si] = 0.0f;
+        }
+    if (lane == 0) {
+        if (src) src[row] = -1;
+        if (weights) weights[row] = 0.0f;
+    }
+}
+
+// The grid's first a.pad_blocks blocks zero the pad rows of an aligned layout
+// and return true; the others return false and dispatch, their block index
+// counted from the end of the pad blocks. Pad rows are disjoint from the rows
+// the dispatch writes, so both share the grid (and HBM) from the first wave;
+// the pad counts come from the layout, hence the same wait.
+__device__ __forceinline__ bool pad_block(const DispatchArgs& a, int64_t row_bytes, int64_t& block) {
+    block = static_cast<int64_t>(blockIdx.x) - a.pad_blocks;
+    if (block >= 0) return false;
+    wait_for_layout();
+    const int64_t item = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+    zero_pad_row(a.pad_counts, a.pad_offsets, a.pad_experts, a.pad_max, item, row_bytes,
+                 static_cast<char*>(a.recv_x), a.pad_scales, a.recv_src_token, a.recv_weights, threadIdx.x & 31);
+    return true;
+}
+
 constexpr int kPrefetchCtas = 512;                   // blocks that issue the x prefetch
 constexpr int64_t kPrefetchWindow = int64_t{96} << 20;   // bytes of x prefetched past theirs
 
@@ -68,15 +107,15 @@ constexpr int64_t kPrefetchWindow = int64_t{96} << 20;   // bytes of x prefetche
 // 1 us of each other, and an evict-last cache policy was slower (and kept x
 // in L2 past the dispatch).
 __device__ __forceinline__ void prefetch_x_during_layout(const DispatchArgs& a, int num_segments,
-                                                         int64_t row_bytes) {
-    if (!a.prefetch_x || blockIdx.x >= kPrefetchCtas || threadIdx.x != 0) return;
+                                                         int64_t row_bytes, int64_t block) {
+    if (!a.prefetch_x || block >= kPrefetchCtas || threadIdx.x != 0) return;
     // tokens the prefetching blocks read themselves (row_bytes % 16 == 0)
     const int64_t own = (static_cast<int64_t>(kPrefetchCtas) * kWarpsPerBlock + num_segments - 1) / num_segments;
     const int64_t lo0 = own * row_bytes;
     const int64_t end = min(static_cast<int64_t>(a.T) * row_bytes, lo0 + kPrefetchWindow);
     if (end <= lo0) return;
     const int64_t per = ((end - lo0 + kPrefetchCtas - 1) / kPrefetchCtas + 15) / 16 * 16;
-    const int64_t lo = lo0 + static_cast<int64_t>(blockIdx.x) * per;
+    const int64_t lo = lo0 + block * per;
     const int64_t hi = min(lo + per, end);
     if (lo >= hi) return;
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
@@ -98,7 +137,9 @@ __device__ __forceinline__ void write_side_outputs(const DispatchArgs& a, int t,
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 dispatch_bf16_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
     const int lane = threadIdx.x & 31;
-    const int64_t item = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+    int64_t block;
+    if (pad_block(a, static_cast<int64_t>(a.H) * 2, block)) return;
+    const int64_t item = block * kWarpsPerBlock + (threadIdx.x >> 5);
     if (item >= num_items) return;
     const int t = static_cast<int>(item / num_segments);
     const int seg = static_cast<int>(item - static_cast<int64_t>(t) * num_segments);
@@ -114,7 +155,7 @@ dispatch_bf16_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
         if (j < H16) v[u] = ld_stream(src + j);
     }
     // x is ready before the layout starts; the slot map only after it ends
-    prefetch_x_during_layout(a, num_segments, static_cast<int64_t>(a.H) * 2);
+    prefetch_x_during_layout(a, num_segments, static_cast<int64_t>(a.H) * 2, block);
     wait_for_layout();
     const int row = slot_row(a.row_of_slot, t, a.K, lane);
     if (seg == 0) write_side_outputs(a, t, lane, row);
@@ -176,7 +217,9 @@ template <int kMode, bool kColMajor, int kFmt>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 dispatch_fp8_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
     const int lane = threadIdx.x & 31;
-    const int64_t item = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+    int64_t block;
+    if (pad_block(a, a.H, block)) return;
+    const int64_t item = block * kWarpsPerBlock + (threadIdx.x >> 5);
     if (item >= num_items) return;
     const int t = static_cast<int>(item / num_segments);
     const int seg = static_cast<int>(item - static_cast<int64_t>(t) * num_segments);
@@ -218,7 +261,7 @@ dispatch_fp8_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
             q[u] = make_uint4(w[0] | (w[1] << 16), w[2] | (w[3] << 16), w[4] | (w[5] << 16), w[6] | (w[7] << 16));
         }
     }
-    prefetch_x_during_layout(a, num_segments, static_cast<int64_t>(a.H) * 2);
+    prefetch_x_during_layout(a, num_segments, static_cast<int64_t>(a.H) * 2, block);
     wait_for_layout();
     const int row = slot_row(a.row_of_slot, t, a.K, lane);
     if (seg == 0) write_side_outputs(a, t, lane, row);
@@ -255,7 +298,9 @@ template <bool kColMajor>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 dispatch_fp8_passthrough_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
     const int lane = threadIdx.x & 31;
-    const int64_t item = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+    int64_t block;
+    if (pad_block(a, a.H, block)) return;
+    const int64_t item = block * kWarpsPerBlock + (threadIdx.x >> 5);
     if (item >= num_items) return;
     const int t = static_cast<int>(item / num_segments);
     const int seg = static_cast<int>(item - static_cast<int64_t>(t) * num_segments);
@@ -271,7 +316,7 @@ dispatch_fp8_passthrough_kernel(DispatchArgs a, int64_t num_items, int num_segme
         if (j < V) v[u] = ld_stream(src + j);
     }
     const bool ue = a.scale_mode == EP_SCALE_UE8M0;
-    prefetch_x_during_layout(a, num_segments, a.H);
+    prefetch_x_during_layout(a, num_segments, a.H, block);
     wait_for_layout();
     const int row = slot_row(a.row_of_slot, t, a.K, lane);
     if (seg == 0) write_side_outputs(a, t, lane, row);
@@ -302,25 +347,8 @@ dispatch_fp8_passthrough_kernel(DispatchArgs a, int64_t num_items, int num_segme
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 fill_pad_rows_kernel(const int32_t* counts, const int32_t* offsets, int E, int max_pad, int64_t row_bytes,
                      char* recv, PadScales sc, int32_t* src, float* weights) {
-    const int lane = threadIdx.x & 31;
     const int64_t item = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
-    const int e = static_cast<int>(item / max_pad);
-    const int i = static_cast<int>(item - static_cast<int64_t>(e) * max_pad);
-    if (e >= E) return;
-    const int64_t row = static_cast<int64_t>(offsets[e]) + counts[e] + i;
-    if (row >= offsets[e + 1]) return;
-    int4* d = reinterpret_cast<int4*>(recv + row * row_bytes);   // row_bytes % 16 == 0
-    for (int64_t j = lane; j < row_bytes / 16; j += 32) d[j] = make_int4(0, 0, 0, 0);
-    if (sc.ptr)
-        for (int b = lane; b < sc.nb; b += 32) {
-            const int64_t si = sc.col_major ? static_cast<int64_t>(b) * sc.ld + row : row * sc.nb + b;
-            if (sc.bytes == 1) static_cast<uint8_t*>(sc.ptr)[si] = 0;
-            else static_cast<float*>(sc.ptr)[si] = 0.0f;
-        }
-    if (lane == 0) {
-        if (src) src[row] = -1;
-        if (weights) weights[row] = 0.0f;
-    }
+    zero_pad_row(counts, offsets, E, max_pad, item, row_bytes, recv, sc, src, weights, threadIdx.x & 31);
 }
 
 // Launch, as a programmatic dependent of the preceding grid when asked: its
@@ -340,15 +368,26 @@ cudaError_t launch_dispatch_kernel(bool overlap, void (*kernel)(Params...), unsi
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// The arguments with pad_blocks set: enough blocks, one warp per (expert,
+// pad row), to zero the pad rows of an aligned layout (0 without padding).
+DispatchArgs with_pad_blocks(const DispatchArgs& a) {
+    DispatchArgs b = a;
+    b.pad_blocks = a.pad_max > 0
+                       ? (static_cast<int64_t>(a.pad_experts) * a.pad_max + kWarpsPerBlock - 1) / kWarpsPerBlock
+                       : 0;
+    return b;
+}
+
 }  // namespace
 
-cudaError_t launch_dispatch_bf16(const DispatchArgs& a, cudaStream_t stream) {
+cudaError_t launch_dispatch_bf16(const DispatchArgs& args, cudaStream_t stream) {
+    const DispatchArgs a = with_pad_blocks(args);
     const int H16 = a.H / 8;
     const int per_item = 32 * kBf16Unroll;
     const int segs = (H16 + per_item - 1) / per_item;
     const int64_t items = static_cast<int64_t>(a.T) * segs;
     if (items == 0) return cudaSuccess;
-    const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock + a.pad_blocks;
     return launch_dispatch_kernel(a.overlap_layout != 0, dispatch_bf16_kernel, static_cast<unsigned>(blocks), stream,
                                   a, items, segs);
 }
@@ -364,13 +403,14 @@ cudaError_t launch_fill_pad_rows(const int32_t* counts, const int32_t* offsets, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_dispatch_fp8_passthrough(const DispatchArgs& a, cudaStream_t stream) {
+cudaError_t launch_dispatch_fp8_passthrough(const DispatchArgs& args, cudaStream_t stream) {
+    const DispatchArgs a = with_pad_blocks(args);
     const int V = a.H / 16;
     const int per_item = 32 * kBf16Unroll;
     const int segs = (V + per_item - 1) / per_item;
     const int64_t items = static_cast<int64_t>(a.T) * segs;
     if (items == 0) return cudaSuccess;
-    const unsigned g = static_cast<unsigned>((items + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    const unsigned g = static_cast<unsigned>((items + kWarpsPerBlock - 1) / kWarpsPerBlock + a.pad_blocks);
     const bool ov = a.overlap_layout != 0;
     if (a.scale_col_major)
         return launch_dispatch_kernel(ov, dispatch_fp8_passthrough_kernel<true>, g, stream, a, items, segs);
@@ -396,13 +436,14 @@ cudaError_t launch_fp8_format(const DispatchArgs& a, unsigned g, cudaStream_t st
 
 }  // namespace
 
-cudaError_t launch_dispatch_fp8(const DispatchArgs& a, cudaStream_t stream) {
+cudaError_t launch_dispatch_fp8(const DispatchArgs& args, cudaStream_t stream) {
+    const DispatchArgs a = with_pad_blocks(args);
     const int G = a.H / 16;                           // 16-channel groups per row
     const int per_item = 32 * kFp8Unroll;
     const int segs = (G + per_item - 1) / per_item;
     const int64_t items = static_cast<int64_t>(a.T) * segs;
     if (items == 0) return cudaSuccess;
-    const unsigned g = static_cast<unsigned>((items + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    const unsigned g = static_cast<unsigned>((items + kWarpsPerBlock - 1) / kWarpsPerBlock + a.pad_blocks);
     if (a.fp8_format == EP_DTYPE_FP8_E5M2) return launch_fp8_format<EP_DTYPE_FP8_E5M2>(a, g, stream, items, segs);
     return launch_fp8_format<EP_DTYPE_FP8_E4M3>(a, g, stream, items, segs);
 }

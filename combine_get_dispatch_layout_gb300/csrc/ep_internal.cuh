@@ -61,6 +61,14 @@ struct LayoutArgs {
 // enqueued (1 on the single-cluster path, 3 on the multi-block path).
 cudaError_t launch_layout(const LayoutPlan& p, const LayoutArgs& a, cudaStream_t stream, int* kernels = nullptr);
 
+// The fp8 scales of pad rows, zeroed with them.
+struct PadScales {
+    void* ptr = nullptr;       // null: no scales
+    int nb = 0;                // blocks per row
+    int bytes = 4;             // 4 (fp32) or 1 (UE8M0)
+    int col_major = 0;
+    int64_t ld = 0;
+};
 struct DispatchArgs {
     const void* x;             // bf16 [T, H]
     const int32_t* row_of_slot;
@@ -78,6 +86,14 @@ struct DispatchArgs {
     const void* x_scales;      // fp8 input: [T, H/128] fp32 (uint8 in UE8M0 mode)
     int overlap_layout;        // launch as the preceding layout's programmatic dependent
     int prefetch_x;            // overlap_layout with x in device memory: prefetch x into L2
+    // aligned layouts: the grid's first pad_blocks blocks zero the pad rows
+    // (one warp per (expert, pad row), at most pad_max pad rows per expert)
+    int64_t pad_blocks;
+    const int32_t* pad_counts;
+    const int32_t* pad_offsets;
+    int pad_experts;
+    int pad_max;
+    PadScales pad_scales;
 };
 
 cudaError_t launch_dispatch_bf16(const DispatchArgs& a, cudaStream_t stream);
@@ -88,14 +104,9 @@ cudaError_t launch_dispatch_fp8_passthrough(const DispatchArgs& a, cudaStream_t 
 // Zero the pad rows of an aligned layout: for each expert e the rows from
 // offsets[e] + counts[e] up to offsets[e+1] (at most max_pad of them) get
 // zero bytes (row_bytes each, a multiple of 16), zero scales (if any, in their
-// layout), source -1 (if src) and weight 0 (if weights).
-struct PadScales {
-    void* ptr = nullptr;       // null: no scales
-    int nb = 0;                // blocks per row
-    int bytes = 4;             // 4 (fp32) or 1 (UE8M0)
-    int col_major = 0;
-    int64_t ld = 0;
-};
+// layout), source -1 (if src) and weight 0 (if weights). The dispatch does
+// this inside its own grid (DispatchArgs::pad_blocks); this launch serves the
+// other producers of receive-shaped rows (the combine backward's grad_y).
 cudaError_t launch_fill_pad_rows(const int32_t* counts, const int32_t* offsets, int E, int64_t row_bytes,
                                  void* recv, const PadScales& scales, int32_t* src, float* weights,
                                  cudaStream_t stream, int max_pad);
