@@ -284,6 +284,35 @@ ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int
     return err == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
 
+// The combine, and for the dispatch backward also the gather of the slot
+// weights (row_weights non-null), in one kernel.
+ep_status_t combine_impl(ep_handle* handle, const void* y, int64_t y_rows, int H, const float* topk_weights,
+                         void* out, const float* row_weights, float* slot_weights, void* stream) {
+    if (!handle) return EP_ERR_INVALID_ARG;
+    if (H < 8 || H % 8 != 0 || y_rows < 0) return EP_ERR_INVALID_ARG;
+    if (handle->T > 0 && !out) return EP_ERR_INVALID_ARG;
+    if (y_rows > 0 && !y) return EP_ERR_INVALID_ARG;
+    if (!aligned(y, 16) || !aligned(out, 16) || !aligned(topk_weights, 4)) return EP_ERR_INVALID_ARG;
+    ep_status_t st = current_device_is(handle);
+    if (st != EP_OK) return st;
+    st = check_rows(handle, y_rows, static_cast<cudaStream_t>(stream));
+    if (st != EP_OK) return st;
+
+    ep::CombineArgs a{};
+    a.y = y;
+    a.row_of_slot = handle->row_of_slot;
+    a.topk_weights = topk_weights;
+    a.out = out;
+    a.y_rows = y_rows;
+    a.T = handle->T;
+    a.K = handle->K;
+    a.H = H;
+    a.row_weights = row_weights;
+    a.slot_weights = slot_weights;
+    cudaError_t err = ep::launch_combine(a, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -449,27 +478,7 @@ ep_status_t ep_dispatch(ep_handle_t handle, const void* x, int H, ep_dtype_t out
 ep_status_t ep_combine(ep_handle_t handle, const void* y, int64_t y_rows, int H,
                        const float* topk_weights, void* out, void* stream) {
     ApiRange range("ep_combine");
-    if (!handle) return EP_ERR_INVALID_ARG;
-    if (H < 8 || H % 8 != 0 || y_rows < 0) return EP_ERR_INVALID_ARG;
-    if (handle->T > 0 && !out) return EP_ERR_INVALID_ARG;
-    if (y_rows > 0 && !y) return EP_ERR_INVALID_ARG;
-    if (!aligned(y, 16) || !aligned(out, 16) || !aligned(topk_weights, 4)) return EP_ERR_INVALID_ARG;
-    ep_status_t st = current_device_is(handle);
-    if (st != EP_OK) return st;
-    st = check_rows(handle, y_rows, static_cast<cudaStream_t>(stream));
-    if (st != EP_OK) return st;
-
-    ep::CombineArgs a{};
-    a.y = y;
-    a.row_of_slot = handle->row_of_slot;
-    a.topk_weights = topk_weights;
-    a.out = out;
-    a.y_rows = y_rows;
-    a.T = handle->T;
-    a.K = handle->K;
-    a.H = H;
-    cudaError_t err = ep::launch_combine(a, static_cast<cudaStream_t>(stream));
-    return err == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+    return combine_impl(handle, y, y_rows, H, topk_weights, out, nullptr, nullptr, stream);
 }
 
 ep_status_t ep_combine_backward(ep_handle_t handle, const void* grad_out, const void* y, int64_t y_rows, int H,
@@ -520,13 +529,9 @@ ep_status_t ep_dispatch_backward(ep_handle_t handle, const void* grad_recv, int6
     if (!handle) return EP_ERR_INVALID_ARG;
     if (grad_topk_weights && !grad_recv_weights) return EP_ERR_INVALID_ARG;
     if (!aligned(grad_recv_weights, 4) || !aligned(grad_topk_weights, 4)) return EP_ERR_INVALID_ARG;
-    ep_status_t st = ep_combine(handle, grad_recv, grad_rows, H, nullptr, grad_x, stream);
-    if (st != EP_OK || !grad_topk_weights) return st;
-    const int64_t slots = static_cast<int64_t>(handle->T) * handle->K;
-    return ep::launch_gather_slot_weights(handle->row_of_slot, grad_recv_weights, grad_topk_weights, slots,
-                                          static_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? EP_OK
-               : EP_ERR_CUDA;
+    // the unweighted combine, which also gathers the weight gradients
+    return combine_impl(handle, grad_recv, grad_rows, H, nullptr, grad_x,
+                        grad_topk_weights ? grad_recv_weights : nullptr, grad_topk_weights, stream);
 }
 
 ep_status_t ep_topk_to_routing_map(const int64_t* topk_idx, const float* topk_weights, int T, int K, int E,

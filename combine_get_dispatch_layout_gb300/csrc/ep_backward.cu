@@ -8,6 +8,9 @@
 //                      grad_w[t,k]      = sum_h grad_out[t,h] * y[row(t,k),h]   (fp32)
 //   dispatch backward: grad_x[t] = bf16(sum_k grad_recv[row(t,k)])     (the unweighted combine)
 //                      grad_topk_weights[t,k] = grad_recv_weights[row(t,k)]  (0 if dropped)
+// The dispatch backward runs as the combine kernel (ep_combine.cu) with null
+// weights, whose warps for each token's first column segment also write the
+// token's weight gradients.
 //
 // GPU design (combine backward): one 4-warp block per token. Each thread owns
 // a stride of 16-byte column vectors; for each vector it loads grad_out once,
@@ -135,29 +138,11 @@ combine_backward_kernel(CombineBackwardArgs a) {
     }
 }
 
-// grad_topk_weights[t, k] = grad_recv_weights[row(t, k)], 0 for dropped slots.
-__global__ void gather_slot_weights_kernel(const int32_t* row_of_slot, const float* row_weights, float* slot_weights,
-                                           int64_t slots) {
-    const int64_t s = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (s >= slots) return;
-    const int32_t r = row_of_slot[s];
-    slot_weights[s] = r >= 0 ? row_weights[r] : 0.0f;
-}
-
 }  // namespace
 
 cudaError_t launch_combine_backward(const CombineBackwardArgs& a, cudaStream_t stream) {
     if (a.T == 0) return cudaSuccess;
     combine_backward_kernel<<<a.T, kBwdThreads, 0, stream>>>(a);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_gather_slot_weights(const int32_t* row_of_slot, const float* row_weights, float* slot_weights,
-                                       int64_t slots, cudaStream_t stream) {
-    if (slots == 0) return cudaSuccess;
-    const int threads = 256;
-    gather_slot_weights_kernel<<<static_cast<unsigned>((slots + threads - 1) / threads), threads, 0, stream>>>(
-        row_of_slot, row_weights, slot_weights, slots);
     return cudaGetLastError();
 }
 

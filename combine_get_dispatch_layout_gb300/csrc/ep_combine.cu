@@ -76,6 +76,8 @@ combine_kernel(CombineArgs a, int64_t num_items, int num_segments) {
         row = __ldg(a.row_of_slot + static_cast<int64_t>(t) * a.K + lane);
         if (a.topk_weights) w = __ldg(a.topk_weights + static_cast<int64_t>(t) * a.K + lane);
     }
+    if (a.slot_weights && seg == 0 && lane < a.K)
+        a.slot_weights[static_cast<int64_t>(t) * a.K + lane] = row >= 0 ? __ldg(a.row_weights + row) : 0.0f;
     const unsigned used = __ballot_sync(kFullMask, row >= 0);
     const int n_used = __popc(used);
     if (row >= 0) {

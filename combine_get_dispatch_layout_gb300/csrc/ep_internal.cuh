@@ -118,6 +118,10 @@ struct CombineArgs {
     void* out;                 // bf16 [T, H]
     int64_t y_rows;
     int T, K, H;
+    // optional (dispatch backward): slot_weights[t, k] = row_weights[row(t, k)],
+    // 0 for an unused slot, written by the warp of each token's first segment
+    const float* row_weights;
+    float* slot_weights;
 };
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
@@ -133,8 +137,7 @@ struct CombineBackwardArgs {
 };
 
 cudaError_t launch_combine_backward(const CombineBackwardArgs& a, cudaStream_t stream);
-cudaError_t launch_gather_slot_weights(const int32_t* row_of_slot, const float* row_weights, float* slot_weights,
-                                       int64_t slots, cudaStream_t stream);
+
 
 cudaError_t launch_topk_to_routing_map(const int64_t* topk_idx, const float* w, int T, int K, int E,
                                        uint8_t* routing_map, float* probs, int32_t* device_error,
