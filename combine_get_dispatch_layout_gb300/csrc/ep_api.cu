@@ -404,7 +404,7 @@ ep_status_t ep_dispatch_ex(ep_handle_t handle, const void* x, const void* x_scal
     if (fp8 && !aligned(recv_scales, scale_bytes)) return EP_ERR_INVALID_ARG;
     if (fp8 && cfg.scales_col_major && cfg.scales_ld < recv_capacity) return EP_ERR_INVALID_ARG;
     if (fp8_in && handle->T > 0 && (!x_scales || !aligned(x_scales, scale_bytes))) return EP_ERR_INVALID_ARG;
-    if (recv_weights && !topk_weights) return EP_ERR_INVALID_ARG;
+    if (recv_weights && !topk_weights && handle->T > 0) return EP_ERR_INVALID_ARG;
     if (handle->T > 0 && !x) return EP_ERR_INVALID_ARG;
     // zero-row receive buffers may be NULL; the capacity check below then
     // guarantees no row is written
@@ -527,7 +527,7 @@ ep_status_t ep_dispatch_backward(ep_handle_t handle, const void* grad_recv, int6
                                  void* stream) {
     ApiRange range("ep_dispatch_backward");
     if (!handle) return EP_ERR_INVALID_ARG;
-    if (grad_topk_weights && !grad_recv_weights) return EP_ERR_INVALID_ARG;
+    if (grad_topk_weights && !grad_recv_weights && grad_rows > 0) return EP_ERR_INVALID_ARG;
     if (!aligned(grad_recv_weights, 4) || !aligned(grad_topk_weights, 4)) return EP_ERR_INVALID_ARG;
     // the unweighted combine, which also gathers the weight gradients
     return combine_impl(handle, grad_recv, grad_rows, H, nullptr, grad_x,
@@ -539,7 +539,7 @@ ep_status_t ep_topk_to_routing_map(const int64_t* topk_idx, const float* topk_we
     ApiRange range("ep_topk_to_routing_map");
     if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS) return EP_ERR_INVALID_ARG;
     if (T > 0 && (!topk_idx || !routing_map)) return EP_ERR_INVALID_ARG;
-    if (probs && !topk_weights) return EP_ERR_INVALID_ARG;
+    if (probs && !topk_weights && T > 0) return EP_ERR_INVALID_ARG;
     if (!aligned(topk_idx, 8) || !aligned(topk_weights, 4) || !aligned(probs, 4) || !aligned(device_error, 4))
         return EP_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -134,7 +134,10 @@ def combine(ep, run, y, weights, H):
 
 
 def assert_combine(got, want):
+    assert got.shape == want.shape
     d = bf16_ulp_dist(got, want)
+    if d.size == 0:
+        return
     assert d.max() <= 1, f"combine off by {d.max()} ulp at {np.argwhere(d > 1)[:5]}"
     # same fp32 fma order on both sides: expect exact equality
     assert (d == 0).all(), f"{int((d > 0).sum())} of {d.size} elements differ by 1 ulp"
@@ -1449,3 +1452,65 @@ def test_two_host_threads_with_their_own_handles(ep):
     for t in threads:
         t.join()
     assert errors == []
+
+
+# ------------------------------------------------------------------ randomised configurations
+
+def _random_config(seed):
+    """A seeded random shape inside the API's limits, with its options."""
+    rng = np.random.default_rng(1000 + seed)
+    R = int(rng.choice([1, 2, 3, 4, 8, 16, 32, 64]))
+    E = R * int(rng.integers(1, max(2, 512 // R) + 1))
+    K = int(rng.integers(1, min(32, E) + 1))
+    T = int(rng.choice([0, 1, 7, int(rng.integers(2, 3000))]))
+    H = int(rng.choice([8, 136, 256, 1024, 1288, 2048, 3072]))
+    w = _workload(T, H, E, K, R, routing=str(rng.choice(["uniform", "zipf"])),
+                  drop_p=float(rng.choice([0.0, 0.05, 0.5])))
+    opts = dict(A=int(rng.choice([1, 1, 2, 8, 64, 128])), mode=int(rng.integers(0, 3)),
+                fmt=int(rng.choice([1, 2])), col=bool(rng.integers(0, 2)))
+    return w, opts
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_configurations(ep, seed):
+    """Random shapes, routings and options through layout, dispatch (bf16, and
+    fp8 when H % 128 == 0) and combine, plus the aligned fp8 variant, all
+    against the oracle."""
+    w, o = _random_config(seed)
+    inp = gi.make(w, 2000 + seed)
+    fp8 = w.H % 128 == 0
+    full_path(ep, inp, fp8=fp8, weights=bool(seed % 4))
+    if fp8 and w.T > 0:
+        fp8_variant(ep, inp, o["mode"], col_major=o["col"], A=o["A"], fmt=o["fmt"])
+
+
+def test_empty_inputs_with_optional_outputs(ep):
+    """Empty arrays arrive as null pointers: T = 0 with weights requested, and
+    a dispatch backward whose receive side has no rows (every slot dropped),
+    are valid calls that write what they must and nothing else."""
+    # T = 0, recv_weights requested, weights tensor empty
+    idx0 = np.zeros((0, 4), np.int64)
+    run0 = Run(ep, idx0, 8, 2)
+    recv = torch.full((GUARD, 64), 3.0, dtype=torch.bfloat16, device="cuda")
+    rw = torch.full((GUARD,), 5.0, dtype=torch.float32, device="cuda")
+    ep.ep_dispatch(run0.h, torch.empty(0, 64, dtype=torch.bfloat16, device="cuda"), ep.EP_DTYPE_BF16, recv, GUARD,
+                   recv_weights=rw, topk_weights=torch.empty(0, 4, dtype=torch.float32, device="cuda"))
+    rm = torch.empty(0, 8, dtype=torch.uint8, device="cuda")
+    ep.ep_topk_to_routing_map(torch.empty(0, 4, dtype=torch.int64, device="cuda"), 8, rm,
+                              topk_weights=torch.empty(0, 4, dtype=torch.float32, device="cuda"),
+                              probs=torch.empty(0, 8, dtype=torch.float32, device="cuda"))
+    torch.cuda.synchronize()
+    assert (recv == 3.0).all() and (rw == 5.0).all()
+    run0.h.destroy()
+    # T > 0, every slot dropped: no receive rows, weight gradients all 0
+    T, K = 50, 3
+    idx = np.full((T, K), -1, np.int64)
+    run = Run(ep, idx, 8, 2)
+    gx = torch.full((T, 64), 7.0, dtype=torch.bfloat16, device="cuda")
+    gtw = torch.full((T, K), 9.0, dtype=torch.float32, device="cuda")
+    ep.ep_dispatch_backward(run.h, torch.empty(0, 64, dtype=torch.bfloat16, device="cuda"), gx,
+                            grad_recv_weights=torch.empty(0, dtype=torch.float32, device="cuda"),
+                            grad_topk_weights=gtw)
+    torch.cuda.synchronize()
+    assert (gx == 0).all() and (gtw == 0).all()
+    run.h.destroy()
