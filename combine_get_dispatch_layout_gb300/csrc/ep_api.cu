@@ -253,6 +253,8 @@ ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int
         if (err == cudaSuccess) err = cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (KE + 1), s);
         if (err == cudaSuccess) err = cudaMemsetAsync(h->meta, 0, sizeof(int32_t) * ep::kMetaWords, s);
         if (err == cudaSuccess) err = cudaMemsetAsync(h->counts, 0, sizeof(int32_t) * (2 * KE + 1), s);
+        if (err == cudaSuccess && stride > 0)
+            err = ep::launch_strided_empty(expert_offsets, h->offsets, h->meta, KE, stride, s);
     } else {
         ep::LayoutArgs a{};
         a.topk_idx = topk_idx;
@@ -279,7 +281,7 @@ ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int
         a.h_offsets = h->offsets;
         if (err == cudaSuccess) err = ep::launch_layout(plan, a, s, &h->layout_kernels);
     }
-    if (T == 0) h->layout_kernels = 0;
+    if (T == 0) h->layout_kernels = stride > 0 ? 1 : 0;
     *handle = h;
     return err == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }

@@ -600,6 +600,23 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
 
 }  // namespace
 
+// A strided layout of no tokens still spans E * stride rows: expert e's rows
+// start at e * stride (the counts are zero, the error word stays clear).
+__global__ void strided_empty_kernel(int32_t* expert_offsets, int32_t* h_offsets, int32_t* meta, int E,
+                                     int stride) {
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e <= E; e += gridDim.x * blockDim.x) {
+        expert_offsets[e] = e * stride;
+        if (h_offsets) h_offsets[e] = e * stride;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) meta[kMetaRows] = E * stride;
+}
+
+cudaError_t launch_strided_empty(int32_t* expert_offsets, int32_t* h_offsets, int32_t* meta, int E, int stride,
+                                 cudaStream_t stream) {
+    strided_empty_kernel<<<(E + 256) / 256, 256, 0, stream>>>(expert_offsets, h_offsets, meta, E, stride);
+    return cudaGetLastError();
+}
+
 LayoutPlan make_layout_plan(int T, int K, int E, int R) {
     LayoutPlan p{};
     p.T = T; p.K = K; p.E = E; p.R = R; p.L = E / R;

@@ -1514,3 +1514,16 @@ def test_empty_inputs_with_optional_outputs(ep):
     torch.cuda.synchronize()
     assert (gx == 0).all() and (gtw == 0).all()
     run.h.destroy()
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_random_configurations_other_paths(ep, seed):
+    """Random shapes through the aligned, backward, strided (capacity drawn
+    at random, sometimes too small) and non-expand paths against the oracle."""
+    w, o = _random_config(100 + seed)
+    inp = gi.make(w, 3000 + seed)
+    rng = np.random.default_rng(4000 + seed)
+    full_path_aligned(ep, inp, o["A"], fp8=(w.H % 128 == 0))
+    backward_path(ep, inp, A=o["A"], weights=bool(seed % 3))
+    strided_path(ep, inp, cap=int(rng.integers(1, max(2, w.T + 2))))
+    nonexpand_path(ep, inp)
