@@ -1527,3 +1527,71 @@ def test_random_configurations_other_paths(ep, seed):
     backward_path(ep, inp, A=o["A"], weights=bool(seed % 3))
     strided_path(ep, inp, cap=int(rng.integers(1, max(2, w.T + 2))))
     nonexpand_path(ep, inp)
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_random_overlapped_dispatch(ep, seed):
+    """Random shapes and alignments with the dispatch launched as the layout's
+    programmatic dependent (x loaded and prefetched during the layout, pad rows
+    zeroed by the dispatch grid): bf16, and fp8 in a random format and scale
+    mode when H % 128 == 0, against the oracle, pad rows included."""
+    w, o = _random_config(200 + seed)
+    if w.T == 0:
+        w = _workload(1 + 37 * seed, w.H, w.E, w.K, w.R, routing=w.routing, drop_p=w.drop_p)
+    inp = gi.make(w, 5000 + seed, with_y=False)
+    T, K, E, R, H, A = w.T, w.K, w.E, w.R, w.H, o["A"]
+    ref = oracle.layout_aligned(inp.topk_idx, E, R, A)
+    n = int(ref["expert_offsets"][-1])
+    cap = T * K + E * (A - 1)
+    idx, x = _dev(inp.topk_idx), _dev(inp.x.view(np.int16))
+    h = _layout_dev(ep, inp, A)
+    outs = [torch.empty(E, dtype=torch.int32, device="cuda"), torch.empty(R, dtype=torch.int32, device="cuda"),
+            torch.empty(T, R, dtype=torch.uint8, device="cuda"), torch.empty(E + 1, dtype=torch.int32, device="cuda")]
+    src = torch.full((cap,), -5, dtype=torch.int32, device="cuda")
+    # bf16
+    recv = torch.full((cap, H), SENT16, dtype=torch.int16, device="cuda")
+    ep.ep_layout_aligned(idx, E, R, A, *outs, handle=h)
+    ep.ep_dispatch_ex(h, x, recv, cap, out_dtype=ep.EP_DTYPE_BF16, recv_src_token=src, H=H, overlap_layout=True)
+    torch.cuda.synchronize()
+    r_x, r_src, _ = oracle.dispatch_bf16(inp.x, ref["row_of_slot"], n)
+    r_src = r_src.copy()
+    oracle.fill_pad_rows(ref, r_x, src=r_src)
+    got = recv.cpu().numpy()
+    np.testing.assert_array_equal(got[:n].view(np.uint16), r_x)
+    assert (got[n:] == SENT16).all()
+    np.testing.assert_array_equal(src.cpu().numpy()[:n], r_src)
+    if H % 128 or n == 0:
+        h.destroy()
+        return
+    # fp8, format / scale mode / scale layout drawn for this seed
+    mode, fmt, col = o["mode"], o["fmt"], o["col"]
+    ue = mode == ep.EP_SCALE_UE8M0
+    nb = H // 128
+    ld = cap + 4
+    q = torch.full((cap, H), SENT8, dtype=torch.uint8, device="cuda")
+    sc = torch.full((nb * ld,) if col else (cap, nb), 0xEE if ue else -1.0,
+                    dtype=torch.uint8 if ue else torch.float32, device="cuda")
+    ep.ep_layout_aligned(idx, E, R, A, *outs, handle=h)
+    ep.ep_dispatch_ex(h, x, q, cap, out_dtype=fmt, scale_mode=mode, recv_scales=sc, scales_col_major=col,
+                      scales_ld=ld if col else 0, H=H, overlap_layout=True)
+    torch.cuda.synchronize()
+    if fmt == ep.EP_DTYPE_FP8_E5M2:
+        r_q, r_s = oracle.dispatch_e5m2(inp.x, ref["row_of_slot"], n, scale_mode=mode)
+    elif mode == ep.EP_SCALE_FP32:
+        r_q, r_s, _, _ = oracle.dispatch_e4m3(inp.x, ref["row_of_slot"], n)
+    else:
+        r_q, r_s = oracle.dispatch_e4m3_pow2(inp.x, ref["row_of_slot"], n, ue8m0=ue)
+    oracle.fill_pad_rows(ref, r_q, scales=None if ue else r_s)
+    if ue:
+        for e in range(E):
+            r_s[ref["expert_offsets"][e] + ref["num_tokens_per_expert"][e]:ref["expert_offsets"][e + 1]] = 0
+    gq = q.cpu().numpy()
+    np.testing.assert_array_equal(gq[:n], r_q)
+    assert (gq[n:] == SENT8).all()
+    g = sc.cpu().numpy()
+    got_s = g.reshape(nb, ld)[:, :n].T if col else g[:n]
+    if ue:
+        np.testing.assert_array_equal(got_s, r_s)
+    else:
+        np.testing.assert_array_equal(got_s.view(np.uint32), r_s.view(np.uint32))
+    h.destroy()
