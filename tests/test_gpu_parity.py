@@ -1595,3 +1595,75 @@ def test_random_overlapped_dispatch(ep, seed):
     else:
         np.testing.assert_array_equal(got_s.view(np.uint32), r_s.view(np.uint32))
     h.destroy()
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_random_routing_map_conversions(ep, seed):
+    """Both conversion directions on random T, E (any value, so both kernel
+    forms), K, duplicate experts, dropped slots and buffer offsets."""
+    rng = np.random.default_rng(6000 + seed)
+    E = int(rng.choice([int(rng.integers(1, 64)), 8 * int(rng.integers(1, 65)), int(rng.integers(1, 4097))]))
+    K = int(rng.integers(1, min(32, E) + 1))
+    T = int(rng.choice([0, 1, int(rng.integers(2, 2000))]))
+    off = int(rng.choice([0, 0, 1, 3]))
+    idx = rng.integers(-1, E, (T, K)).astype(np.int64)
+    wts = rng.random((T, K)).astype(np.float32)
+    r_map, r_probs, _ = oracle.topk_to_routing_map(idx, wts, E)
+    mbuf = torch.full((T * E + 16,), SENT8, dtype=torch.uint8, device="cuda")
+    pbuf = torch.full((T * E + 8,), -1.0, dtype=torch.float32, device="cuda")
+    rm, pr = mbuf[off:off + T * E].view(T, E), pbuf[off:off + T * E].view(T, E)
+    ep.ep_topk_to_routing_map(_dev(idx), E, rm, topk_weights=_dev(wts), probs=pr)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(rm.cpu().numpy(), r_map)
+    np.testing.assert_array_equal(pr.cpu().numpy().view(np.uint32), r_probs.view(np.uint32))
+    assert (mbuf[:off] == SENT8).all() and (mbuf[off + T * E:] == SENT8).all()
+    r_idx, r_w, _ = oracle.routing_map_to_topk(r_map, r_probs, K)
+    out_i = torch.full((T, K), -9, dtype=torch.int64, device="cuda")
+    out_w = torch.full((T, K), -1.0, dtype=torch.float32, device="cuda")
+    ep.ep_routing_map_to_topk(rm, K, out_i, probs=pr, topk_weights=out_w)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out_i.cpu().numpy(), r_idx)
+    np.testing.assert_array_equal(out_w.cpu().numpy().view(np.uint32), r_w.view(np.uint32))
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_fp8_passthrough(ep, seed):
+    """fp8 input pass-through on random shapes, formats, scale modes and
+    layouts and alignments: codes and scale rows moved unchanged, pad rows
+    zeroed."""
+    rng = np.random.default_rng(7000 + seed)
+    w, o = _random_config(300 + seed)
+    H = 128 * int(rng.integers(1, 25))
+    w = _workload(max(1, w.T), H, w.E, w.K, w.R, routing=w.routing, drop_p=w.drop_p)
+    inp = gi.make(w, 8000 + seed, with_y=False)
+    T, K, E, R, A = w.T, w.K, w.E, w.R, o["A"]
+    fmt, ue, col = o["fmt"], bool(rng.integers(0, 2)), o["col"]
+    nb = H // 128
+    codes = rng.integers(0, 256, (T, H)).astype(np.uint8)
+    scales = rng.integers(0, 256, (T, nb)).astype(np.uint8) if ue else rng.random((T, nb)).astype(np.float32)
+    ref = oracle.layout_aligned(inp.topk_idx, E, R, A)
+    n = int(ref["expert_offsets"][-1])
+    cap = T * K + E * (A - 1)
+    ld = cap + 2
+    h = _layout_dev(ep, inp, A)
+    q = torch.full((cap, H), SENT8, dtype=torch.uint8, device="cuda")
+    sc = torch.full((nb * ld,) if col else (cap, nb), 0xEE if ue else -1.0,
+                    dtype=torch.uint8 if ue else torch.float32, device="cuda")
+    ep.ep_dispatch_ex(h, _dev(codes), q, cap, in_dtype=fmt, out_dtype=fmt,
+                      scale_mode=ep.EP_SCALE_UE8M0 if ue else ep.EP_SCALE_FP32, x_scales=_dev(scales),
+                      recv_scales=sc, scales_col_major=col, scales_ld=ld if col else 0, H=H)
+    torch.cuda.synchronize()
+    r_q = oracle.dispatch_rows(codes, ref["row_of_slot"], n)
+    r_s = oracle.dispatch_rows(scales, ref["row_of_slot"], n)
+    oracle.fill_pad_rows(ref, r_q, scales=None if ue else r_s)
+    if ue:
+        for e in range(E):
+            r_s[ref["expert_offsets"][e] + ref["num_tokens_per_expert"][e]:ref["expert_offsets"][e + 1]] = 0
+    gq = q.cpu().numpy()
+    np.testing.assert_array_equal(gq[:n], r_q)
+    assert (gq[n:] == SENT8).all()
+    g = sc.cpu().numpy()
+    got_s = g.reshape(nb, ld)[:, :n].T if col else g[:n]
+    np.testing.assert_array_equal(got_s.view(np.uint8) if ue else got_s.view(np.uint32),
+                                  r_s.view(np.uint8) if ue else r_s.view(np.uint32))
+    h.destroy()
