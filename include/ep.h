@@ -57,6 +57,9 @@
  *  - Arguments are checked on the host first. A failed check returns
  *    EP_ERR_INVALID_ARG and enqueues nothing.
  *  - Row buffers (x, recv_x, y, out) must be 16-byte aligned.
+ *  - An array with no elements may be passed as NULL, and an input is only
+ *    required when something would be read from it (T = 0, or no receive
+ *    rows, needs no token, weight or row data).
  *  - A handle may be used from one host thread at a time.
  */
 #ifndef EP_GB300_EP_H
@@ -165,7 +168,10 @@ typedef int (*ep_free_fn)(void* ptr);
  *                         that reads the handle must be on `stream` or
  *                         finished.
  * Writes every element of the four outputs; needs no zeroed memory.
- * Three kernel launches, no host synchronisation (except on creation/growth).
+ * One kernel (a single thread-block cluster) for routings up to 2^17 slots
+ * whose plan fits its shared memory, else three (count, scan, assign);
+ * ep_handle_layout_kernels says which. No host synchronisation except on
+ * creation or growth.
  */
 EP_API ep_status_t ep_layout(const int64_t* topk_idx, int T, int K, int E, int R,
                       int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
@@ -312,9 +318,9 @@ EP_API ep_status_t ep_dispatch(ep_handle_t handle, const void* x, int H, ep_dtyp
  * format's rne_satfinite(x / scale). An all-zero block has zero codes and
  * scale 0 (UE8M0 byte 0). With fp8 in_dtype (out_dtype must match), x holds
  * codes [T, H] (bytes) and x_scales [T, H/128] (fp32, or bytes in UE8M0
- * mode); both are copied to every slot's row. recv_scales is fp32 (bytes in UE8M0 mode),
- * [cap, H/128] row-major or, with scales_col_major, element (row n, block b)
- * at n + b * scales_ld. Other arguments and errors as ep_dispatch; config may
+ * mode); both are copied to every slot's row. recv_scales is fp32 (bytes in
+ * UE8M0 mode), [cap, H/128] row-major or, with scales_col_major, element
+ * (row n, block b) at n + b * scales_ld. Other arguments and errors as ep_dispatch; config may
  * be NULL (bf16 in and out).
  */
 EP_API ep_status_t ep_dispatch_ex(ep_handle_t handle, const void* x, const void* x_scales, int H,
