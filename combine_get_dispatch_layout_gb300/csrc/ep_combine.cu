@@ -148,6 +148,7 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
     // its blocks may be scheduled while that kernel's last wave runs, and wait
     // for it to finish before touching memory
     cudaLaunchConfig_t cfg = {};
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;   // beyond the grid limit: refuse
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
     cfg.blockDim = dim3(kWarpsPerBlock * 32);
     cfg.stream = stream;

@@ -354,10 +354,11 @@ fill_pad_rows_kernel(const int32_t* counts, const int32_t* offsets, int E, int m
 // Launch, as a programmatic dependent of the preceding grid when asked: its
 // blocks may then start (and load x) while the layout is still running.
 template <typename... Params, typename... Args>
-cudaError_t launch_dispatch_kernel(bool overlap, void (*kernel)(Params...), unsigned blocks, cudaStream_t stream,
+cudaError_t launch_dispatch_kernel(bool overlap, void (*kernel)(Params...), int64_t blocks, cudaStream_t stream,
                                    Args... args) {
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;   // beyond the grid limit: refuse
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(blocks);
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
     cfg.blockDim = dim3(kWarpsPerBlock * 32);
     cfg.stream = stream;
     cudaLaunchAttribute attr;
@@ -388,7 +389,7 @@ cudaError_t launch_dispatch_bf16(const DispatchArgs& args, cudaStream_t stream) 
     const int64_t items = static_cast<int64_t>(a.T) * segs;
     if (items == 0) return cudaSuccess;
     const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock + a.pad_blocks;
-    return launch_dispatch_kernel(a.overlap_layout != 0, dispatch_bf16_kernel, static_cast<unsigned>(blocks), stream,
+    return launch_dispatch_kernel(a.overlap_layout != 0, dispatch_bf16_kernel, blocks, stream,
                                   a, items, segs);
 }
 
@@ -410,7 +411,7 @@ cudaError_t launch_dispatch_fp8_passthrough(const DispatchArgs& args, cudaStream
     const int segs = (V + per_item - 1) / per_item;
     const int64_t items = static_cast<int64_t>(a.T) * segs;
     if (items == 0) return cudaSuccess;
-    const unsigned g = static_cast<unsigned>((items + kWarpsPerBlock - 1) / kWarpsPerBlock + a.pad_blocks);
+    const int64_t g = (items + kWarpsPerBlock - 1) / kWarpsPerBlock + a.pad_blocks;
     const bool ov = a.overlap_layout != 0;
     if (a.scale_col_major)
         return launch_dispatch_kernel(ov, dispatch_fp8_passthrough_kernel<true>, g, stream, a, items, segs);
@@ -420,7 +421,7 @@ cudaError_t launch_dispatch_fp8_passthrough(const DispatchArgs& args, cudaStream
 namespace {
 
 template <int kMode, int kFmt>
-cudaError_t launch_fp8_variant(const DispatchArgs& a, unsigned g, cudaStream_t stream, int64_t items, int segs) {
+cudaError_t launch_fp8_variant(const DispatchArgs& a, int64_t g, cudaStream_t stream, int64_t items, int segs) {
     const bool ov = a.overlap_layout != 0;
     if (a.scale_col_major)
         return launch_dispatch_kernel(ov, dispatch_fp8_kernel<kMode, true, kFmt>, g, stream, a, items, segs);
@@ -428,7 +429,7 @@ cudaError_t launch_fp8_variant(const DispatchArgs& a, unsigned g, cudaStream_t s
 }
 
 template <int kFmt>
-cudaError_t launch_fp8_format(const DispatchArgs& a, unsigned g, cudaStream_t stream, int64_t items, int segs) {
+cudaError_t launch_fp8_format(const DispatchArgs& a, int64_t g, cudaStream_t stream, int64_t items, int segs) {
     if (a.scale_mode == EP_SCALE_POW2) return launch_fp8_variant<EP_SCALE_POW2, kFmt>(a, g, stream, items, segs);
     if (a.scale_mode == EP_SCALE_UE8M0) return launch_fp8_variant<EP_SCALE_UE8M0, kFmt>(a, g, stream, items, segs);
     return launch_fp8_variant<EP_SCALE_FP32, kFmt>(a, g, stream, items, segs);
@@ -443,7 +444,7 @@ cudaError_t launch_dispatch_fp8(const DispatchArgs& args, cudaStream_t stream) {
     const int segs = (G + per_item - 1) / per_item;
     const int64_t items = static_cast<int64_t>(a.T) * segs;
     if (items == 0) return cudaSuccess;
-    const unsigned g = static_cast<unsigned>((items + kWarpsPerBlock - 1) / kWarpsPerBlock + a.pad_blocks);
+    const int64_t g = (items + kWarpsPerBlock - 1) / kWarpsPerBlock + a.pad_blocks;
     if (a.fp8_format == EP_DTYPE_FP8_E5M2) return launch_fp8_format<EP_DTYPE_FP8_E5M2>(a, g, stream, items, segs);
     return launch_fp8_format<EP_DTYPE_FP8_E4M3>(a, g, stream, items, segs);
 }
