@@ -550,10 +550,14 @@ def gpu_arm(args, rank, world, local):
         "kernels": {
             "layout": {"us": round(ms_layout * 1e3, 2), "bytes": b_lay},
             "dispatch_bf16": {"us": round(ms_dispatch * 1e3, 2), "bytes": b_dis,
+                              "tokens_per_s": round(T / (ms_dispatch * 1e-3), 1),
+                              "rows_per_s": round(N / (ms_dispatch * 1e-3), 1),
                               "gbs": round(b_dis / (ms_dispatch * 1e-3) / 1e9, 1),
                               "frac_of_measured": round(b_dis / (ms_dispatch * 1e-3) / 1e9 / peak, 4),
                               "frac_of_8tbs": round(b_dis / (ms_dispatch * 1e-3) / 8e12, 4)},
             "combine": {"us": round(ms_combine * 1e3, 2), "bytes": b_com,
+                        "tokens_per_s": round(T / (ms_combine * 1e-3), 1),
+                        "rows_per_s": round(N / (ms_combine * 1e-3), 1),
                         "gbs": round(b_com / (ms_combine * 1e-3) / 1e9, 1),
                         "frac_of_measured": round(b_com / (ms_combine * 1e-3) / 1e9 / peak, 4),
                         "frac_of_8tbs": round(b_com / (ms_combine * 1e-3) / 8e12, 4)},
