@@ -738,6 +738,37 @@ def other_configs(torch, ep, dev, stream, args, rank, peak, reps):
         "layout_strided_us": round(ms[0] * 1e3, 2), "dispatch_us": round(ms[1] * 1e3, 2),
         "combine_us": round(ms[2] * 1e3, 2), "tokens_per_s": round(wd.T / (sum(ms) * 1e-3), 1)}
     del t, y, flush
+
+    # the tiny workload's step (T=128, H=256, E=8, top-2), one CUDA graph per
+    # step: pure latency
+    tn = gi.make("tiny", seed=args.seed + rank)
+    wt_ = tn.w
+    t = tensors(tn, wt_.T * wt_.K)
+    with torch.cuda.stream(stream):
+        y = torch.from_numpy(tn.x.view(np.int16)).to(dev).repeat_interleave(wt_.K, dim=0)
+        h = ep.ep_layout(t["idx"], wt_.E, wt_.R, t["cnt"], t["ntr"], t["itr"], t["off"], stream=stream)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            ep.ep_layout(t["idx"], wt_.E, wt_.R, t["cnt"], t["ntr"], t["itr"], t["off"], handle=h, stream=stream)
+            ep.ep_dispatch_ex(h, t["x"], t["recv"], wt_.T * wt_.K, out_dtype=ep.EP_DTYPE_BF16, overlap_layout=True,
+                              stream=stream)
+            ep.ep_combine(h, y, t["out"], topk_weights=t["w"], stream=stream)
+        for _ in range(5):
+            g.replay()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+    stream.synchronize()
+    ms_t = ev0.elapsed_time(ev1) / reps
+    del g
+    h.destroy()
+    out["tiny_step_graph"] = {
+        "workload": f"tiny T={wt_.T} H={wt_.H} E={wt_.E} K={wt_.K} R={wt_.R}, one CUDA graph per step, warm",
+        "step_us": round(ms_t * 1e3, 2), "tokens_per_s": round(wt_.T / (ms_t * 1e-3), 1)}
+    del t, y
     return out
 
 
