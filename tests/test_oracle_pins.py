@@ -307,6 +307,42 @@ def test_combine_vs_f64(name, null_w):
     assert (out[dead] == 0).all()
 
 
+def test_combine_tokens_within_the_f64_bound():
+    """The per-token combine used for sampled checks at full size: within the
+    float64 bound, and the same rows as the full combine."""
+    inp = gi.make("skewed", 4, T=80)
+    w = inp.w
+    L = oracle.layout(inp.topk_idx, w.E, w.R)
+    toks = [0, 3, 17, 41, 79]
+    got = oracle.combine_tokens(inp.y, L["row_of_slot"], inp.topk_weights, toks)
+    yf = gi.bf16_bits_to_f32(inp.y)
+    ref = brute.combine_f64(yf, L["row_of_slot"], inp.topk_weights)[toks]
+    mag = brute.combine_f64(np.abs(yf), L["row_of_slot"], np.abs(inp.topk_weights.astype(np.float64)))[toks]
+    out = gi.bf16_bits_to_f32(got).astype(np.float64)
+    assert (np.abs(out - ref) <= w.K * 2.0**-24 * mag + 2.0**-8 * np.abs(ref) + 1e-30).all()
+    np.testing.assert_array_equal(got, oracle.combine(inp.y, L["row_of_slot"], inp.topk_weights)[toks])
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_dispatch_e5m2_rows_are_their_tokens_quantised(mode):
+    """Each used slot's row holds its token's e5m2 codes and scales (checked
+    against the quantiser, itself pinned above); unused rows stay zero."""
+    inp = gi.make("tiny", 5, with_y=False)
+    w = inp.w
+    L = oracle.layout(inp.topk_idx, w.E, w.R)
+    n = int(L["expert_offsets"][-1])
+    q, s = oracle.dispatch_e5m2(inp.x, L["row_of_slot"], n + 3, scale_mode=mode)
+    seen = np.zeros(n + 3, bool)
+    for t, k in zip(*np.nonzero(L["row_of_slot"] >= 0)):
+        r = L["row_of_slot"][t, k]
+        qt, st = oracle.quant_row_e5m2(inp.x[t], mode)
+        np.testing.assert_array_equal(q[r], qt)
+        np.testing.assert_array_equal(s[r], st)
+        seen[r] = True
+    assert seen[:n].all() and not seen[n:].any()
+    assert not q[n:].any() and not s[n:].any()
+
+
 # ------------------------------------------------------------------ alignment
 
 def test_layout_aligned_golden(golden):
