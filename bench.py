@@ -548,7 +548,10 @@ def gpu_arm(args, rank, world, local):
                      "calls with an event between each (no overlap)",
         "overlap_saved_us": round((ms_layout + ms_dispatch + ms_combine - ms_step) * 1e3, 2),
         "kernels": {
-            "layout": {"us": round(ms_layout * 1e3, 2), "bytes": b_lay},
+            "layout": {"us": round(ms_layout * 1e3, 2), "bytes": b_lay,
+                       "note": "CUDA events around the one call, after the previous step's combine, not chained: "
+                               "includes the launch of a 16-CTA cluster and ~2 us of event overhead; inside the "
+                               "timed step the layout runs beside the dispatch's prefetch of x"},
             "dispatch_bf16": {"us": round(ms_dispatch * 1e3, 2), "bytes": b_dis,
                               "tokens_per_s": round(T / (ms_dispatch * 1e-3), 1),
                               "rows_per_s": round(N / (ms_dispatch * 1e-3), 1),

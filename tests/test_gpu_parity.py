@@ -1289,7 +1289,7 @@ def test_graph_capture_replays_the_step(ep, name, fp8):
             idx.copy_(torch.from_numpy(idx_n))
             wt.copy_(torch.from_numpy(wt_n))
             y[:n].copy_(torch.from_numpy(y_n.view(np.int16)).view(torch.bfloat16))
-        g.replay()
+            g.replay()                                # on s, after the copies into the captured buffers
         s.synchronize()
         np.testing.assert_array_equal(o[3].cpu().numpy(), ref["expert_offsets"])
         np.testing.assert_array_equal(o[2].cpu().numpy(), ref["is_token_in_rank"])
@@ -1339,8 +1339,9 @@ def test_capture_refuses_host_waits_and_allocation(ep):
                 statuses.append(e.status)
         ep.ep_dispatch(h, x, ep.EP_DTYPE_BF16, full, cap)
     assert statuses == [ep.EP_ERR_INVALID_ARG] * 3
-    full.fill_(-3.0)
-    g.replay()
+    with torch.cuda.stream(s):
+        full.fill_(-3.0)
+        g.replay()
     s.synchronize()
     ref = oracle.layout(inp.topk_idx, w.E, w.R)
     n = int(ref["expert_offsets"][-1])
