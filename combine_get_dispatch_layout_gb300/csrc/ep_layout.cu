@@ -353,16 +353,18 @@ __device__ __forceinline__ unsigned rank_of(unsigned e, const LayoutPlan& p) {
 // Shared memory (ints, sized for 16 CTAs): hist[W][E] | all_tot[16][E] |
 // all_rank[16][R] | all_bad[16] | tail[max(W * ct_cap, 2E)], where the tail
 // holds the token rank masks (R <= 32) and later the offsets and CTA bases.
+// With E no larger than the CTA's thread count (and no fixed stride) each
+// thread owns one expert in the offset scan, which then runs in registers.
 __global__ void __launch_bounds__(1024, 1)
 layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
-    // launched as the preceding kernel's programmatic dependent: wait for it
-    // (and so for all earlier work) before touching memory; only then may a
-    // dispatch launched as this grid's dependent start on idle SMs (it reads
-    // the slot map only after this grid has finished)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;");
+    // Launched as the preceding kernel's programmatic dependent: it zeroes
+    // its own shared memory, then waits for that kernel (and so for all
+    // earlier work) before touching global memory; only then may a dispatch
+    // launched as this grid's dependent start on idle SMs (it reads the slot
+    // map only after this grid has finished).
     extern __shared__ int smem[];
     __shared__ int s_over;
+    __shared__ int s_scan[32];
     cg::cluster_group cluster = cg::this_cluster();
     const int cta = static_cast<int>(cluster.block_rank());
     const int C = p.cl_ctas, W = p.cl_warps, E = p.E, R = p.R, ct = p.cl_chunk_tokens;
@@ -381,14 +383,20 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
     // once every CTA of the cluster runs, so arrive now and wait before the
     // first remote store (by then every CTA has long started).
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    // this CTA's own shared state, zeroed before the wait for the preceding
+    // kernel (nothing here is memory that kernel could write)
+    int* rank_acc = all_rank + cta * R;   // this CTA's tokens per rank until the push
     for (int e = lane; e < E; e += 32) mine[e] = 0;
     if (small_r)
         for (int i = lane; i < ct; i += 32) my_mask[i] = 0u;
+    for (int r = threadIdx.x; r < R; r += blockDim.x) rank_acc[r] = 0;
     if (threadIdx.x == 0) {
         all_bad[cta] = 0;   // own entry only: peers write their own
         s_over = 0;
     }
     __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
 
     // ---- phase 1: stable local ranks, the warp's histogram, token rank masks
     const int g = cta * W + warp;
@@ -457,10 +465,6 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
             }
         }
     }
-    // reuse all_rank[cta] as this CTA's accumulator until the push
-    int* rank_acc = all_rank + cta * R;
-    for (int r = threadIdx.x; r < R; r += blockDim.x) rank_acc[r] = 0;
-    __syncthreads();
     if (small_r) {
         if (lane < R && my_rank_cnt) atomicAdd(rank_acc + lane, my_rank_cnt);
     } else {
@@ -528,59 +532,121 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
     // it, so CTAs may finish independently.
     cluster.sync();
 
-    // ---- phase 3 (local): expert totals and this CTA's base per expert
+    // ---- phase 3 (local): expert totals, this CTA's base per expert and the
+    // expert offsets
     int* offs = tail;          // the token masks are consumed: reuse the tail
     int* cta_base = tail + E;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int below = 0, total = 0;
-#pragma unroll
-        for (int c = 0; c < kMaxClusterCtas; ++c) {
-            const int v = c < C ? all_tot[c * E + e] : 0;
-            below += c < cta ? v : 0;
-            total += v;
-        }
-        cta_base[e] = below;
-        offs[e] = p.stride > 0 ? e * p.stride : round_up_to(total, p.align);
-        if (p.stride > 0 && total > p.stride) s_over = 1;
-        if (cta == 0) {
-            a.num_tokens_per_expert[e] = total;
-            if (a.h_counts) a.h_counts[e] = total;
-        }
-    }
-    // CTA 0 writes the expert offsets below; the last CTA takes the rank
-    // totals and the error word so that no CTA carries both
+    // the last CTA takes the rank totals and the error word, CTA 0 the
+    // counts and offsets, so that no CTA carries both
     if (cta == C - 1)
         for (int r = threadIdx.x; r < R; r += blockDim.x) {
             int total = 0;
             for (int c = 0; c < C; ++c) total += all_rank[c * R + r];
             a.num_tokens_per_rank[r] = total;
         }
-    __syncthreads();
-    if (cta == C - 1 && threadIdx.x == 0) {
-        int bad = 0;
-        for (int c = 0; c < C; ++c) bad |= all_bad[c];
-        a.meta[kMetaError] = bad ? EP_ERR_INVALID_EXPERT : (s_over ? EP_ERR_CAPACITY : 0);
-    }
-    if (p.stride > 0) {
-        if (cta == 0 && threadIdx.x == 0) {
-            a.expert_offsets[E] = E * p.stride;
-            if (a.h_offsets) a.h_offsets[E] = E * p.stride;
-            a.meta[kMetaRows] = E * p.stride;
+    if (p.stride == 0 && E <= static_cast<int>(blockDim.x)) {
+        // one expert per thread: its padded row count is scanned in registers
+        // (shuffles inside each warp, then the warp sums), no serial pass
+        const int e = threadIdx.x;
+        int v = 0;
+        if (e < E) {
+            int below = 0, total = 0;
+#pragma unroll
+            for (int c = 0; c < kMaxClusterCtas; ++c) {
+                const int x = c < C ? all_tot[c * E + e] : 0;
+                below += c < cta ? x : 0;
+                total += x;
+            }
+            cta_base[e] = below;
+            v = round_up_to(total, p.align);
+            if (cta == 0) {
+                a.num_tokens_per_expert[e] = total;
+                if (a.h_counts) a.h_counts[e] = total;
+            }
         }
-    } else if (warp == 0) {
-        const int n_rows = warp_exclusive_scan(offs, E, lane);
-        if (cta == 0 && lane == 0) {
-            a.expert_offsets[E] = n_rows;
-            if (a.h_offsets) a.h_offsets[E] = n_rows;
-            a.meta[kMetaRows] = n_rows;
+        int incl = v;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int u = __shfl_up_sync(kFullMask, incl, d);
+            if (lane >= d) incl += u;
         }
-    }
-    __syncthreads();
-    if (cta == 0)
+        if (lane == 31) s_scan[warp] = incl;
+        __syncthreads();
+        const int nw = static_cast<int>(blockDim.x >> 5);
+        const int ws = lane < nw ? s_scan[lane] : 0;
+        int wincl = ws;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int u = __shfl_up_sync(kFullMask, wincl, d);
+            if (lane >= d) wincl += u;
+        }
+        const int wbase = __shfl_sync(kFullMask, wincl - ws, warp);
+        const int n_rows = __shfl_sync(kFullMask, wincl, nw - 1);
+        if (e < E) {
+            const int o = wbase + incl - v;
+            offs[e] = o;
+            if (cta == 0) {
+                a.expert_offsets[e] = o;
+                if (a.h_offsets) a.h_offsets[e] = o;
+            }
+        }
+        if (threadIdx.x == 0) {
+            if (cta == 0) {
+                a.expert_offsets[E] = n_rows;
+                if (a.h_offsets) a.h_offsets[E] = n_rows;
+                a.meta[kMetaRows] = n_rows;
+            }
+            if (cta == C - 1) {
+                int bad = 0;
+                for (int c = 0; c < C; ++c) bad |= all_bad[c];
+                a.meta[kMetaError] = bad ? EP_ERR_INVALID_EXPERT : 0;
+            }
+        }
+        __syncthreads();
+    } else {
         for (int e = threadIdx.x; e < E; e += blockDim.x) {
-            a.expert_offsets[e] = offs[e];
-            if (a.h_offsets) a.h_offsets[e] = offs[e];
+            int below = 0, total = 0;
+#pragma unroll
+            for (int c = 0; c < kMaxClusterCtas; ++c) {
+                const int v = c < C ? all_tot[c * E + e] : 0;
+                below += c < cta ? v : 0;
+                total += v;
+            }
+            cta_base[e] = below;
+            offs[e] = p.stride > 0 ? e * p.stride : round_up_to(total, p.align);
+            if (p.stride > 0 && total > p.stride) s_over = 1;
+            if (cta == 0) {
+                a.num_tokens_per_expert[e] = total;
+                if (a.h_counts) a.h_counts[e] = total;
+            }
         }
+        __syncthreads();
+        if (cta == C - 1 && threadIdx.x == 0) {
+            int bad = 0;
+            for (int c = 0; c < C; ++c) bad |= all_bad[c];
+            a.meta[kMetaError] = bad ? EP_ERR_INVALID_EXPERT : (s_over ? EP_ERR_CAPACITY : 0);
+        }
+        if (p.stride > 0) {
+            if (cta == 0 && threadIdx.x == 0) {
+                a.expert_offsets[E] = E * p.stride;
+                if (a.h_offsets) a.h_offsets[E] = E * p.stride;
+                a.meta[kMetaRows] = E * p.stride;
+            }
+        } else if (warp == 0) {
+            const int n_rows = warp_exclusive_scan(offs, E, lane);
+            if (cta == 0 && lane == 0) {
+                a.expert_offsets[E] = n_rows;
+                if (a.h_offsets) a.h_offsets[E] = n_rows;
+                a.meta[kMetaRows] = n_rows;
+            }
+        }
+        __syncthreads();
+        if (cta == 0)
+            for (int e = threadIdx.x; e < E; e += blockDim.x) {
+                a.expert_offsets[e] = offs[e];
+                if (a.h_offsets) a.h_offsets[e] = offs[e];
+            }
+    }
 
     // ---- phase 4: row = expert offset + rows in lower CTAs + rows in lower
     // warps of this CTA + the slot's local rank
