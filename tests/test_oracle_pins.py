@@ -388,6 +388,77 @@ def test_layout_aligned_one_is_plain_layout():
         np.testing.assert_array_equal(a[key], b[key])
 
 
+def _slots_rows(L, key_of_slot, n_keys):
+    """Receive rows of the slots of each key (expert, or rank)."""
+    rows = L["row_of_slot"].ravel()
+    keys = key_of_slot.ravel()
+    return [set(int(r) for r in rows[(keys == k) & (rows >= 0)]) for k in range(n_keys)]
+
+
+@pytest.mark.parametrize("A", [1, 4, 128])
+@pytest.mark.parametrize("seed", range(3))
+def test_aligned_layout_follows_expand_mode_prefix_sum_recipe(A, seed):
+    """DeepEP API docs, "Prefix Sum Interpretation for Expert Token Counts",
+    expand mode: the handle's per-expert prefix sum points at the END of each
+    expert's real rows; expert i starts at align(psum[i-1], alignment) (0 for
+    i = 0) and holds end - start real rows. With the end of expert i's real
+    rows taken as offsets[i] + count[i], that recipe must give back this
+    layout's starts and counts, the real rows of expert i must be exactly
+    [start, end), and the buffer ends at align(psum[E-1], alignment). With
+    alignment 1 it is also "Computing with Handle Metadata": start =
+    psum[i-1], end = psum[i]."""
+    rng = np.random.default_rng(40 + seed)
+    T, K, E, R = 300, 6, 24, 4
+    idx = _random_routing(rng, T, K, E, drop_p=0.1)
+    L = oracle.layout_aligned(idx, E, R, A)
+    assert L["status"] == oracle.OK
+    cnt, off = L["num_tokens_per_expert"], L["expert_offsets"]
+    psum = off[:E] + cnt
+
+    def align(v):
+        return (int(v) + A - 1) // A * A
+
+    by_expert = _slots_rows(L, idx, E)
+    for i in range(E):
+        start = 0 if i == 0 else align(psum[i - 1])
+        end = int(psum[i])
+        assert start == off[i] and end - start == cnt[i]
+        assert by_expert[i] == set(range(start, end))
+        if A == 1:
+            assert start == (0 if i == 0 else psum[i - 1])
+    assert align(psum[E - 1]) == off[E]
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_nonexpand_layout_follows_inclusive_prefix_sum_recipe(seed):
+    """DeepEP API docs, "Prefix Sum Interpretation for Expert Token Counts",
+    non-expand mode: a standard inclusive prefix sum, so destination r holds
+    rows [psum[r-1], psum[r]) (from 0 for r = 0). Here one row per (token,
+    rank): the count of rank r is its number of distinct tokens, the rows of
+    the slots routed to rank r fill that range, and of one token's slots on
+    one rank only the first (lowest k) carries the row, the others -1."""
+    rng = np.random.default_rng(50 + seed)
+    T, K, E, R = 257, 5, 32, 8
+    idx = _random_routing(rng, T, K, E, drop_p=0.15)
+    L = oracle.layout_nonexpand(idx, E, R)
+    assert L["status"] == oracle.OK
+    psum = L["rank_offsets"][1:]
+    rank_of_slot = np.where(idx >= 0, idx // (E // R), -1)
+    by_rank = _slots_rows(L, rank_of_slot, R)
+    for r in range(R):
+        start = 0 if r == 0 else int(psum[r - 1])
+        end = int(psum[r])
+        distinct_tokens = len({t for t in range(T) if (rank_of_slot[t] == r).any()})
+        assert end - start == distinct_tokens == L["num_tokens_per_rank"][r]
+        assert by_rank[r] == set(range(start, end))
+    rows = L["row_of_slot"]
+    for t in range(T):
+        for r in range(R):
+            ks = np.flatnonzero(rank_of_slot[t] == r)
+            if len(ks):
+                assert rows[t, ks[0]] >= 0 and (rows[t, ks[1:]] == -1).all()
+
+
 # ------------------------------------------------------------------ backward
 
 def _small_routed(seed, T=40, K=3, E=8, R=2, H=24, drop_p=0.2):
