@@ -41,8 +41,10 @@ __device__ __forceinline__ int4 ld_stream(const int4* p) {
     return v;
 }
 
-// Wait for the preceding grid (the layout that wrote row_of_slot) when this
-// kernel was launched as its programmatic dependent; a no-op otherwise. Then
+// Wait for the preceding grid (normally the layout that wrote row_of_slot)
+// and so for all earlier work; the dispatch is always launched as that
+// grid's programmatic dependent, and the wait is a no-op when the launch had
+// to serialise anyway (an event or a copy in between). Then
 // let a kernel launched as this grid's dependent (a combine) be scheduled on
 // SMs that this grid's last wave leaves free: it waits for this grid to
 // finish before its first memory access. Triggering only after the wait keeps
@@ -148,15 +150,18 @@ dispatch_bf16_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
     const int4* src = reinterpret_cast<const int4*>(a.x) + static_cast<int64_t>(t) * H16;
     int4* dst = reinterpret_cast<int4*>(a.recv_x);
     const int j0 = seg * (32 * kBf16Unroll) + lane;
+    if (!a.overlap_layout) wait_for_layout();
     int4 v[kBf16Unroll];
 #pragma unroll
     for (int u = 0; u < kBf16Unroll; ++u) {
         const int j = j0 + u * 32;
         if (j < H16) v[u] = ld_stream(src + j);
     }
-    // x is ready before the layout starts; the slot map only after it ends
-    prefetch_x_during_layout(a, num_segments, static_cast<int64_t>(a.H) * 2, block);
-    wait_for_layout();
+    if (a.overlap_layout) {
+        // x is ready before the layout starts; the slot map only after it ends
+        prefetch_x_during_layout(a, num_segments, static_cast<int64_t>(a.H) * 2, block);
+        wait_for_layout();
+    }
     const int row = slot_row(a.row_of_slot, t, a.K, lane);
     if (seg == 0) write_side_outputs(a, t, lane, row);
     for (int k = 0; k < a.K; ++k) {
@@ -229,6 +234,7 @@ dispatch_fp8_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
     uint4 q[kFp8Unroll];
     float scale[kFp8Unroll];
     const int g0 = seg * (32 * kFp8Unroll) + lane;
+    if (!a.overlap_layout) wait_for_layout();
 #pragma unroll
     for (int u = 0; u < kFp8Unroll; ++u) {
         const int g = g0 + u * 32;
@@ -261,8 +267,10 @@ dispatch_fp8_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
             q[u] = make_uint4(w[0] | (w[1] << 16), w[2] | (w[3] << 16), w[4] | (w[5] << 16), w[6] | (w[7] << 16));
         }
     }
-    prefetch_x_during_layout(a, num_segments, static_cast<int64_t>(a.H) * 2, block);
-    wait_for_layout();
+    if (a.overlap_layout) {
+        prefetch_x_during_layout(a, num_segments, static_cast<int64_t>(a.H) * 2, block);
+        wait_for_layout();
+    }
     const int row = slot_row(a.row_of_slot, t, a.K, lane);
     if (seg == 0) write_side_outputs(a, t, lane, row);
     uint4* dst = reinterpret_cast<uint4*>(a.recv_x);
@@ -309,6 +317,7 @@ dispatch_fp8_passthrough_kernel(DispatchArgs a, int64_t num_items, int num_segme
     const int4* src = reinterpret_cast<const int4*>(a.x) + static_cast<int64_t>(t) * V;
     int4* dst = reinterpret_cast<int4*>(a.recv_x);
     const int j0 = seg * (32 * kBf16Unroll) + lane;
+    if (!a.overlap_layout) wait_for_layout();
     int4 v[kBf16Unroll];
 #pragma unroll
     for (int u = 0; u < kBf16Unroll; ++u) {
@@ -316,8 +325,10 @@ dispatch_fp8_passthrough_kernel(DispatchArgs a, int64_t num_items, int num_segme
         if (j < V) v[u] = ld_stream(src + j);
     }
     const bool ue = a.scale_mode == EP_SCALE_UE8M0;
-    prefetch_x_during_layout(a, num_segments, a.H, block);
-    wait_for_layout();
+    if (a.overlap_layout) {
+        prefetch_x_during_layout(a, num_segments, a.H, block);
+        wait_for_layout();
+    }
     const int row = slot_row(a.row_of_slot, t, a.K, lane);
     if (seg == 0) write_side_outputs(a, t, lane, row);
     for (int k = 0; k < a.K; ++k) {
@@ -351,11 +362,12 @@ fill_pad_rows_kernel(const int32_t* counts, const int32_t* offsets, int E, int m
     zero_pad_row(counts, offsets, E, max_pad, item, row_bytes, recv, sc, src, weights, threadIdx.x & 31);
 }
 
-// Launch, as a programmatic dependent of the preceding grid when asked: its
-// blocks may then start (and load x) while the layout is still running.
+// Launch as a programmatic dependent of the preceding grid: the blocks may be
+// scheduled while that grid drains. Each waits for it before touching global
+// memory, except that with overlap_layout it first loads (and quantises) its
+// slice of x, which the caller guarantees was written before the layout.
 template <typename... Params, typename... Args>
-cudaError_t launch_dispatch_kernel(bool overlap, void (*kernel)(Params...), int64_t blocks, cudaStream_t stream,
-                                   Args... args) {
+cudaError_t launch_dispatch_kernel(void (*kernel)(Params...), int64_t blocks, cudaStream_t stream, Args... args) {
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;   // beyond the grid limit: refuse
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
@@ -364,8 +376,8 @@ cudaError_t launch_dispatch_kernel(bool overlap, void (*kernel)(Params...), int6
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = overlap ? &attr : nullptr;
-    cfg.numAttrs = overlap ? 1 : 0;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
@@ -389,8 +401,7 @@ cudaError_t launch_dispatch_bf16(const DispatchArgs& args, cudaStream_t stream) 
     const int64_t items = static_cast<int64_t>(a.T) * segs;
     if (items == 0) return cudaSuccess;
     const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock + a.pad_blocks;
-    return launch_dispatch_kernel(a.overlap_layout != 0, dispatch_bf16_kernel, blocks, stream,
-                                  a, items, segs);
+    return launch_dispatch_kernel(dispatch_bf16_kernel, blocks, stream, a, items, segs);
 }
 
 cudaError_t launch_fill_pad_rows(const int32_t* counts, const int32_t* offsets, int E, int64_t row_bytes,
@@ -412,20 +423,18 @@ cudaError_t launch_dispatch_fp8_passthrough(const DispatchArgs& args, cudaStream
     const int64_t items = static_cast<int64_t>(a.T) * segs;
     if (items == 0) return cudaSuccess;
     const int64_t g = (items + kWarpsPerBlock - 1) / kWarpsPerBlock + a.pad_blocks;
-    const bool ov = a.overlap_layout != 0;
     if (a.scale_col_major)
-        return launch_dispatch_kernel(ov, dispatch_fp8_passthrough_kernel<true>, g, stream, a, items, segs);
-    return launch_dispatch_kernel(ov, dispatch_fp8_passthrough_kernel<false>, g, stream, a, items, segs);
+        return launch_dispatch_kernel(dispatch_fp8_passthrough_kernel<true>, g, stream, a, items, segs);
+    return launch_dispatch_kernel(dispatch_fp8_passthrough_kernel<false>, g, stream, a, items, segs);
 }
 
 namespace {
 
 template <int kMode, int kFmt>
 cudaError_t launch_fp8_variant(const DispatchArgs& a, int64_t g, cudaStream_t stream, int64_t items, int segs) {
-    const bool ov = a.overlap_layout != 0;
     if (a.scale_col_major)
-        return launch_dispatch_kernel(ov, dispatch_fp8_kernel<kMode, true, kFmt>, g, stream, a, items, segs);
-    return launch_dispatch_kernel(ov, dispatch_fp8_kernel<kMode, false, kFmt>, g, stream, a, items, segs);
+        return launch_dispatch_kernel(dispatch_fp8_kernel<kMode, true, kFmt>, g, stream, a, items, segs);
+    return launch_dispatch_kernel(dispatch_fp8_kernel<kMode, false, kFmt>, g, stream, a, items, segs);
 }
 
 template <int kFmt>

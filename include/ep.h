@@ -31,10 +31,12 @@
  *  - All device work is enqueued on `stream` (a cudaStream_t; NULL = the
  *    legacy default stream) and is asynchronous, except where a call says it
  *    synchronises.
- *  - The single-kernel layout and the combine are launched as programmatic
- *    dependents of the kernel before them on the stream: their blocks may be
- *    scheduled while that kernel finishes, but wait for it before their first
- *    memory access, so stream order holds as for ordinary launches. Every
+ *  - The single-kernel layout, the dispatch and the combine are launched as
+ *    programmatic dependents of the kernel before them on the stream: their
+ *    blocks may be scheduled while that kernel finishes, but wait for it
+ *    before their first global memory access (the one exception is the
+ *    dispatch's early read of x with overlap_layout, below), so stream order
+ *    holds as for ordinary launches. Every
  *    kernel here releases its dependents only after that wait, so when one
  *    starts, all work before its immediate predecessor is complete.
  *  - N (the receive rows of the last layout) and the device error word are
@@ -114,11 +116,11 @@ typedef struct {
     int overlap_layout;    /* 1: the caller enqueues this dispatch directly after the
                               ep_layout* call that built the handle, on the same stream,
                               with x complete before that layout was enqueued; the
-                              dispatch then starts on the SMs the layout leaves idle and
-                              loads x while the layout runs (programmatic dependent
-                              launch); if x is device memory its first blocks also
-                              prefetch later rows of x into L2 meanwhile.
-                              0: ordinary stream order.                               */
+                              dispatch's blocks, scheduled on the SMs the layout leaves
+                              idle, then load x while the layout runs instead of after
+                              it; if x is device memory its first blocks also prefetch
+                              later rows of x into L2 meanwhile.
+                              0: every access waits for the preceding kernel.         */
 } ep_dispatch_config_t;
 
 /* Opaque routing handle: owns the slot -> row map [T*K] int32, the layout
