@@ -52,6 +52,7 @@ __device__ __forceinline__ unsigned bf16x2(float lo, float hi) {
 
 __global__ void __launch_bounds__(kBwdThreads)
 combine_backward_kernel(CombineBackwardArgs a) {
+    dependent_entry();
     __shared__ int s_row[EP_MAX_TOPK];
     __shared__ float s_w[EP_MAX_TOPK];
     __shared__ int s_k[EP_MAX_TOPK];
@@ -142,8 +143,7 @@ combine_backward_kernel(CombineBackwardArgs a) {
 
 cudaError_t launch_combine_backward(const CombineBackwardArgs& a, cudaStream_t stream) {
     if (a.T == 0) return cudaSuccess;
-    combine_backward_kernel<<<a.T, kBwdThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(combine_backward_kernel, dim3(a.T), dim3(kBwdThreads), 0, stream, a);
 }
 
 }  // namespace ep

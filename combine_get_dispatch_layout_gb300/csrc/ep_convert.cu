@@ -43,6 +43,7 @@ inline int lanes_per_token_log2(int E) {
 __global__ void __launch_bounds__(kConvWarps * 32)
 topk_to_routing_map_vec_kernel(const int64_t* topk_idx, const float* w, int T, int K, int E, int gs,
                                uint8_t* routing_map, float* probs, int32_t* device_error) {
+    dependent_entry();
     const int G = 1 << gs;   // lanes per token
     const int lane = threadIdx.x & 31, gl = lane & (G - 1);
     const int t = ((blockIdx.x * kConvWarps + (threadIdx.x >> 5)) << (5 - gs)) + (lane >> gs);
@@ -112,6 +113,7 @@ topk_to_routing_map_vec_kernel(const int64_t* topk_idx, const float* w, int T, i
 __global__ void __launch_bounds__(kConvWarps * 32)
 routing_map_to_topk_vec_kernel(const uint8_t* routing_map, const float* probs, int T, int E, int K, int gs,
                                int64_t* topk_idx, float* topk_weights, int32_t* device_error) {
+    dependent_entry();
     const int G = 1 << gs;   // lanes per token
     const int lane = threadIdx.x & 31, gl = lane & (G - 1);
     const int t = ((blockIdx.x * kConvWarps + (threadIdx.x >> 5)) << (5 - gs)) + (lane >> gs);
@@ -169,6 +171,7 @@ routing_map_to_topk_vec_kernel(const uint8_t* routing_map, const float* probs, i
 __global__ void __launch_bounds__(kConvWarps * 32)
 topk_to_routing_map_kernel(const int64_t* topk_idx, const float* w, int T, int K, int E, uint8_t* routing_map,
                            float* probs, int32_t* device_error) {
+    dependent_entry();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kConvWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -203,6 +206,7 @@ topk_to_routing_map_kernel(const int64_t* topk_idx, const float* w, int T, int K
 __global__ void __launch_bounds__(kConvWarps * 32)
 routing_map_to_topk_kernel(const uint8_t* routing_map, const float* probs, int T, int E, int K, int64_t* topk_idx,
                            float* topk_weights, int32_t* device_error) {
+    dependent_entry();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kConvWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -237,12 +241,12 @@ cudaError_t launch_topk_to_routing_map(const int64_t* topk_idx, const float* w, 
         reinterpret_cast<uintptr_t>(probs) % 16 == 0) {
         const int gs = lanes_per_token_log2(E);
         const int per_block = kConvWarps << (5 - gs);
-        topk_to_routing_map_vec_kernel<<<static_cast<unsigned>((T + per_block - 1) / per_block), kConvWarps * 32, 0,
-                                         stream>>>(topk_idx, w, T, K, E, gs, routing_map, probs, device_error);
-    } else
-        topk_to_routing_map_kernel<<<blocks, kConvWarps * 32, 0, stream>>>(topk_idx, w, T, K, E, routing_map,
-                                                                           probs, device_error);
-    return cudaGetLastError();
+        return launch_dependent(topk_to_routing_map_vec_kernel, dim3((T + per_block - 1) / per_block),
+                                dim3(kConvWarps * 32), 0, stream, topk_idx, w, T, K, E, gs, routing_map, probs,
+                                device_error);
+    }
+    return launch_dependent(topk_to_routing_map_kernel, dim3(blocks), dim3(kConvWarps * 32), 0, stream, topk_idx, w,
+                            T, K, E, routing_map, probs, device_error);
 }
 
 cudaError_t launch_routing_map_to_topk(const uint8_t* routing_map, const float* probs, int T, int E, int K,
@@ -254,13 +258,12 @@ cudaError_t launch_routing_map_to_topk(const uint8_t* routing_map, const float* 
         reinterpret_cast<uintptr_t>(probs) % 16 == 0) {
         const int gs = lanes_per_token_log2(E);
         const int per_block = kConvWarps << (5 - gs);
-        routing_map_to_topk_vec_kernel<<<static_cast<unsigned>((T + per_block - 1) / per_block), kConvWarps * 32, 0,
-                                         stream>>>(routing_map, probs, T, E, K, gs, topk_idx, topk_weights,
-                                                   device_error);
-    } else
-        routing_map_to_topk_kernel<<<blocks, kConvWarps * 32, 0, stream>>>(routing_map, probs, T, E, K, topk_idx,
-                                                                           topk_weights, device_error);
-    return cudaGetLastError();
+        return launch_dependent(routing_map_to_topk_vec_kernel, dim3((T + per_block - 1) / per_block),
+                                dim3(kConvWarps * 32), 0, stream, routing_map, probs, T, E, K, gs, topk_idx,
+                                topk_weights, device_error);
+    }
+    return launch_dependent(routing_map_to_topk_kernel, dim3(blocks), dim3(kConvWarps * 32), 0, stream, routing_map,
+                            probs, T, E, K, topk_idx, topk_weights, device_error);
 }
 
 }  // namespace ep
@@ -280,6 +283,7 @@ namespace {
 __global__ void __launch_bounds__(256)
 nonexpand_keys_kernel(const int64_t* topk_idx, int T, int K, int E, int R, int L, int64_t* keys,
                       int32_t* expert_counts) {
+    dependent_entry();
     extern __shared__ int hist[];                  // [E]
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
     __syncthreads();
@@ -323,6 +327,7 @@ nonexpand_keys_kernel(const int64_t* topk_idx, int T, int K, int E, int R, int L
 __global__ void __launch_bounds__(kConvWarps * 32)
 nonexpand_recv_topk_kernel(const int64_t* topk_idx, const float* w, const int32_t* row_of_slot, int T, int K,
                            int E, int L, int64_t* recv_topk_idx, float* recv_topk_weights) {
+    dependent_entry();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kConvWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -352,18 +357,16 @@ nonexpand_recv_topk_kernel(const int64_t* topk_idx, const float* w, const int32_
 cudaError_t launch_nonexpand_keys(const int64_t* topk_idx, int T, int K, int E, int R, int64_t* keys,
                                   int32_t* expert_counts, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    nonexpand_keys_kernel<<<(T + 255) / 256, 256, static_cast<size_t>(E) * sizeof(int), stream>>>(
-        topk_idx, T, K, E, R, E / R, keys, expert_counts);
-    return cudaGetLastError();
+    return launch_dependent(nonexpand_keys_kernel, dim3((T + 255) / 256), dim3(256), static_cast<size_t>(E) * sizeof(int),
+                            stream, topk_idx, T, K, E, R, E / R, keys, expert_counts);
 }
 
 cudaError_t launch_nonexpand_recv_topk(const int64_t* topk_idx, const float* w, const int32_t* row_of_slot, int T,
                                        int K, int E, int R, int64_t* recv_topk_idx, float* recv_topk_weights,
                                        cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    nonexpand_recv_topk_kernel<<<(T + kConvWarps - 1) / kConvWarps, kConvWarps * 32, 0, stream>>>(
-        topk_idx, w, row_of_slot, T, K, E, E / R, recv_topk_idx, recv_topk_weights);
-    return cudaGetLastError();
+    return launch_dependent(nonexpand_recv_topk_kernel, dim3((T + kConvWarps - 1) / kConvWarps), dim3(kConvWarps * 32),
+                            0, stream, topk_idx, w, row_of_slot, T, K, E, E / R, recv_topk_idx, recv_topk_weights);
 }
 
 }  // namespace ep

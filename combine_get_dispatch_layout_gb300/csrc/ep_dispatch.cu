@@ -358,6 +358,7 @@ dispatch_fp8_passthrough_kernel(DispatchArgs a, int64_t num_items, int num_segme
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 fill_pad_rows_kernel(const int32_t* counts, const int32_t* offsets, int E, int max_pad, int64_t row_bytes,
                      char* recv, PadScales sc, int32_t* src, float* weights) {
+    dependent_entry();
     const int64_t item = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
     zero_pad_row(counts, offsets, E, max_pad, item, row_bytes, recv, sc, src, weights, threadIdx.x & 31);
 }
@@ -410,9 +411,9 @@ cudaError_t launch_fill_pad_rows(const int32_t* counts, const int32_t* offsets, 
     if (E == 0 || max_pad <= 0) return cudaSuccess;
     const int64_t items = static_cast<int64_t>(E) * max_pad;
     const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    fill_pad_rows_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(
-        counts, offsets, E, max_pad, row_bytes, static_cast<char*>(recv), scales, src, weights);
-    return cudaGetLastError();
+    return launch_dependent(fill_pad_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kWarpsPerBlock * 32), 0,
+                            stream, counts, offsets, E, max_pad, row_bytes, static_cast<char*>(recv), scales, src,
+                            weights);
 }
 
 cudaError_t launch_dispatch_fp8_passthrough(const DispatchArgs& args, cudaStream_t stream) {

@@ -10,6 +10,37 @@ namespace ep {
 
 constexpr unsigned kFullMask = 0xffffffffu;
 
+// Every kernel of the library is launched as a programmatic dependent of the
+// work before it on the stream (launch_dependent below, or the layout's and
+// dispatch's own launchers): its blocks may be scheduled while the preceding
+// grid drains. This is the first statement of such a kernel: wait for that
+// grid (and so for all earlier work) before any global memory access, then
+// let this grid's own dependent be scheduled. Releasing only after the wait
+// keeps the chain's guarantee: when a kernel starts, all work before its
+// immediate predecessor is complete. Both instructions are no-ops when the
+// launch serialised anyway (an event or a copy in between).
+__device__ __forceinline__ void dependent_entry() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+}
+
+// Launch `kernel` as a programmatic dependent of the preceding work on `stream`.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Layout of the handle's small device word block.
 enum MetaWord : int {
     kMetaRows = 0,        // N = number of valid slots

@@ -130,6 +130,7 @@ __device__ int block_exclusive_scan(int* data, int n, int* warp_tmp) {
 
 __global__ void __launch_bounds__(256)
 layout_count_kernel(LayoutPlan p, LayoutArgs a) {
+    dependent_entry();
     extern __shared__ int smem[];
     const int wpb = p.warps_per_block;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -197,6 +198,7 @@ layout_count_kernel(LayoutPlan p, LayoutArgs a) {
 // its total. Warps [E, E+R): per-rank token totals. Warp E+R: error word.
 __global__ void __launch_bounds__(256)
 layout_scan_kernel(LayoutPlan p, LayoutArgs a) {
+    dependent_entry();
     const int lane = threadIdx.x & 31;
     const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (gw < p.E) {
@@ -243,6 +245,7 @@ layout_scan_kernel(LayoutPlan p, LayoutArgs a) {
 
 __global__ void __launch_bounds__(256)
 layout_assign_kernel(LayoutPlan p, LayoutArgs a) {
+    dependent_entry();
     asm volatile("griddepcontrol.launch_dependents;");
     extern __shared__ int smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -670,6 +673,7 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
 // start at e * stride (the counts are zero, the error word stays clear).
 __global__ void strided_empty_kernel(int32_t* expert_offsets, int32_t* h_offsets, int32_t* meta, int E,
                                      int stride) {
+    dependent_entry();
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e <= E; e += gridDim.x * blockDim.x) {
         expert_offsets[e] = e * stride;
         if (h_offsets) h_offsets[e] = e * stride;
@@ -679,8 +683,8 @@ __global__ void strided_empty_kernel(int32_t* expert_offsets, int32_t* h_offsets
 
 cudaError_t launch_strided_empty(int32_t* expert_offsets, int32_t* h_offsets, int32_t* meta, int E, int stride,
                                  cudaStream_t stream) {
-    strided_empty_kernel<<<(E + 256) / 256, 256, 0, stream>>>(expert_offsets, h_offsets, meta, E, stride);
-    return cudaGetLastError();
+    return launch_dependent(strided_empty_kernel, dim3((E + 256) / 256), dim3(256), 0, stream, expert_offsets,
+                            h_offsets, meta, E, stride);
 }
 
 LayoutPlan make_layout_plan(int T, int K, int E, int R) {
@@ -833,15 +837,13 @@ cudaError_t launch_layout(const LayoutPlan& plan, const LayoutArgs& a, cudaStrea
 
     const int threads = plan.warps_per_block * 32;
     if (kernels) *kernels = 3;
-    layout_count_kernel<<<plan.num_blocks, threads, plan.smem_count, stream>>>(plan, a);
-    err = cudaGetLastError();
+    err = launch_dependent(layout_count_kernel, dim3(plan.num_blocks), dim3(threads), plan.smem_count, stream, plan, a);
     if (err != cudaSuccess) return err;
     const int scan_warps = plan.E + plan.R + 1;
-    layout_scan_kernel<<<(scan_warps + 7) / 8, 256, 0, stream>>>(plan, a);
-    err = cudaGetLastError();
+    err = launch_dependent(layout_scan_kernel, dim3((scan_warps + 7) / 8), dim3(256), 0, stream, plan, a);
     if (err != cudaSuccess) return err;
-    layout_assign_kernel<<<plan.num_blocks, threads, plan.smem_assign, stream>>>(plan, a);
-    return cudaGetLastError();
+    return launch_dependent(layout_assign_kernel, dim3(plan.num_blocks), dim3(threads), plan.smem_assign, stream, plan,
+                            a);
 }
 
 }  // namespace ep

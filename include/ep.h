@@ -31,14 +31,13 @@
  *  - All device work is enqueued on `stream` (a cudaStream_t; NULL = the
  *    legacy default stream) and is asynchronous, except where a call says it
  *    synchronises.
- *  - The single-kernel layout, the dispatch and the combine are launched as
- *    programmatic dependents of the kernel before them on the stream: their
- *    blocks may be scheduled while that kernel finishes, but wait for it
- *    before their first global memory access (the one exception is the
- *    dispatch's early read of x with overlap_layout, below), so stream order
- *    holds as for ordinary launches. Every
- *    kernel here releases its dependents only after that wait, so when one
- *    starts, all work before its immediate predecessor is complete.
+ *  - Every kernel of the library is launched as a programmatic dependent of
+ *    the kernel before it on the stream: its blocks may be scheduled while
+ *    that kernel finishes, but wait for it before their first global memory
+ *    access (the one exception is the dispatch's early read of x with
+ *    overlap_layout, below), so stream order holds as for ordinary launches.
+ *    Every kernel here releases its dependents only after that wait, so when
+ *    one starts, all work before its immediate predecessor is complete.
  *  - N (the receive rows of the last layout) and the device error word are
  *    read from the device at most once per layout: the first call that needs
  *    them (ep_handle_query, or a dispatch / combine whose buffer is smaller
