@@ -440,6 +440,38 @@ def test_handle_reuse_grow_and_shrink(ep):
     h.destroy()
 
 
+def test_handle_churn_returns_device_memory(ep):
+    """Handles created, grown and destroyed many times give all their device
+    memory back (default cudaMalloc hooks, so cudaMemGetInfo sees it)."""
+    rng = np.random.default_rng(77)
+    shapes = [(64, 2, 8, 2), (3000, 8, 256, 8), (40000, 6, 64, 4)]   # the last takes the multi-block path
+    routings = [np.argsort(rng.random((T, E)), axis=1)[:, :K].astype(np.int64) for T, K, E, R in shapes]
+    dev_idx = [_dev(r) for r in routings]
+    outs = [[torch.empty(E, dtype=torch.int32, device="cuda"), torch.empty(R, dtype=torch.int32, device="cuda"),
+             torch.empty(T, R, dtype=torch.uint8, device="cuda"), torch.empty(E + 1, dtype=torch.int32, device="cuda")]
+            for T, K, E, R in shapes]
+
+    def churn(n):
+        for i in range(n):
+            h = None
+            for j in (i % 3, (i + 1) % 3, (i + 2) % 3):   # grow and shrink in varying order
+                T, K, E, R = shapes[j]
+                h = ep.ep_layout(dev_idx[j], E, R, *outs[j], handle=h)
+            h.destroy()
+
+    churn(3)                                   # library state that lives for the process
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    churn(200)
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    assert free0 - free1 < (2 << 20), (free0, free1)   # within the driver's allocation granularity
+    ref = oracle.layout(routings[1], shapes[1][2], shapes[1][3])
+    run = Run(ep, routings[1], shapes[1][2], shapes[1][3])
+    check_layout(run, ref)
+    run.h.destroy()
+
+
 def test_layout_repeatable_on_same_handle(ep):
     """Back-to-back layouts on one handle (the done-counter reset path)."""
     inp = gi.make("skewed", 5, with_y=False)
