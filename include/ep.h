@@ -432,7 +432,8 @@ EP_API ep_status_t ep_handle_destroy(ep_handle_t handle);
 /*
  * ep_handle_layout_kernels -- number of kernels the last ep_layout on this
  * handle enqueued: 1 on the single-cluster path, 3 on the multi-block path,
- * 0 for T = 0; -1 for a NULL handle. For launch accounting only.
+ * 0 for T = 0 (1 for a strided layout, which still writes its offsets);
+ * -1 for a NULL handle. For launch accounting only.
  */
 EP_API int ep_handle_layout_kernels(ep_handle_t handle);
 
