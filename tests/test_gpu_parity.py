@@ -1517,6 +1517,37 @@ def test_random_configurations(ep, seed):
         fp8_variant(ep, inp, o["mode"], col_major=o["col"], A=o["A"], fmt=o["fmt"])
 
 
+def _random_large_config(seed):
+    """A seeded random shape toward the API's limits: E up to 4096, K up to 32,
+    up to 2^20 slots (so about one in five takes the three-kernel layout
+    path), H shrunk so the receive rows stay within 256 MB."""
+    rng = np.random.default_rng(90000 + seed)
+    R = int(rng.choice([1, 2, 4, 8, 16, 32, 64]))
+    E = R * int(rng.integers(1, 4096 // R + 1))
+    K = int(rng.integers(1, min(32, E) + 1))
+    T = int(np.exp(rng.uniform(0, np.log(max(2, (1 << 20) // K)))))
+    h_max = max(8, min(7168, (256 << 20) // max(1, 2 * T * K) // 8 * 8))
+    H = int(rng.choice([h for h in [8, 64, 128, 264, 1024, 2048, 4096, 7168] if h <= h_max] or [8]))
+    w = _workload(T, H, E, K, R, routing=str(rng.choice(["uniform", "zipf"])),
+                  drop_p=float(rng.choice([0.0, 0.02, 0.3])))
+    opts = dict(A=int(rng.choice([1, 8, 128])), mode=int(rng.integers(0, 3)), fmt=int(rng.choice([1, 2])),
+                col=bool(rng.integers(0, 2)))
+    return w, opts
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_large_configurations(ep, seed):
+    """Random large shapes through layout, dispatch (bf16, and fp8 when
+    H % 128 == 0), combine and an fp8 variant, against the oracle."""
+    w, o = _random_large_config(seed)
+    inp = gi.make(w, 3000 + seed)
+    fp8 = w.H % 128 == 0
+    full_path(ep, inp, fp8=fp8, weights=bool(seed % 3))
+    if fp8 and w.T > 0:
+        fp8_variant(ep, inp, o["mode"], col_major=o["col"], A=o["A"], fmt=o["fmt"])
+    torch.cuda.empty_cache()
+
+
 def test_empty_inputs_with_optional_outputs(ep):
     """Empty arrays arrive as null pointers: T = 0 with weights requested, and
     a dispatch backward whose receive side has no rows (every slot dropped),
