@@ -1339,6 +1339,94 @@ def test_graph_capture_replays_the_step(ep, name, fp8):
     h.destroy()
 
 
+def test_graph_capture_of_the_whole_chain(ep):
+    """Conversions, layout, a plain dispatch (which waits at entry), combine
+    and both backward passes captured into one CUDA graph, every kernel a
+    programmatic dependent of the one before, then replayed on new inputs
+    written into the captured buffers; each output against the oracle."""
+    inp = gi.make("decode", 56, with_y=False)
+    w = inp.w
+    T, K, E, R, H = w.T, w.K, w.E, w.R, w.H
+    cap = T * K
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        idx = _dev(inp.topk_idx)
+        wt = _dev(inp.topk_weights)
+        rm = torch.empty(T, E, dtype=torch.uint8, device="cuda")
+        pr = torch.empty(T, E, dtype=torch.float32, device="cuda")
+        idx2 = torch.empty(T, K, dtype=torch.int64, device="cuda")
+        wt2 = torch.empty(T, K, dtype=torch.float32, device="cuda")
+        o = [torch.empty(E, dtype=torch.int32, device="cuda"), torch.empty(R, dtype=torch.int32, device="cuda"),
+             torch.empty(T, R, dtype=torch.uint8, device="cuda"), torch.empty(E + 1, dtype=torch.int32, device="cuda")]
+        x = torch.empty(T, H, dtype=torch.int16, device="cuda")
+        y = torch.zeros(cap, H, dtype=torch.int16, device="cuda")
+        g = torch.empty(T, H, dtype=torch.int16, device="cuda")
+        grw = torch.zeros(cap, dtype=torch.float32, device="cuda")
+        recv = torch.empty(cap, H, dtype=torch.int16, device="cuda")
+        out = torch.empty(T, H, dtype=torch.int16, device="cuda")
+        gy = torch.empty(cap, H, dtype=torch.int16, device="cuda")
+        gw = torch.empty(T, K, dtype=torch.float32, device="cuda")
+        gx = torch.empty(T, H, dtype=torch.int16, device="cuda")
+        gtw = torch.empty(T, K, dtype=torch.float32, device="cuda")
+        ep.ep_topk_to_routing_map(idx, E, rm, topk_weights=wt, probs=pr)
+        ep.ep_routing_map_to_topk(rm, K, idx2, probs=pr, topk_weights=wt2)
+        h = ep.ep_layout(idx2, E, R, *o)                # creates the handle before the capture
+    s.synchronize()
+
+    def chain():
+        ep.ep_topk_to_routing_map(idx, E, rm, topk_weights=wt, probs=pr)
+        ep.ep_routing_map_to_topk(rm, K, idx2, probs=pr, topk_weights=wt2)
+        ep.ep_layout(idx2, E, R, *o, handle=h)
+        ep.ep_dispatch(h, x, ep.EP_DTYPE_BF16, recv, cap)
+        ep.ep_combine(h, y, out, topk_weights=wt2)
+        ep.ep_combine_backward(h, g, y=y, topk_weights=wt2, grad_y=gy, grad_topk_weights=gw, y_rows=cap,
+                               grad_y_capacity=cap)
+        ep.ep_dispatch_backward(h, gy, gx, grad_recv_weights=grw, grad_topk_weights=gtw, grad_rows=cap)
+
+    g_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_graph, stream=s):
+        chain()
+    rng = np.random.default_rng(57)
+    for rep in range(2):
+        idx_n = np.argsort(rng.random((T, E)), axis=1)[:, :K].astype(np.int64)
+        idx_n[rng.random((T, K)) < 0.1] = -1
+        wt_n = rng.random((T, K)).astype(np.float32)
+        x_n = gi.normal_bf16(np.random.SeedSequence(58 + rep), T, H)
+        g_n = gi.normal_bf16(np.random.SeedSequence(60 + rep), T, H)
+        rm_r, pr_r, st = oracle.topk_to_routing_map(idx_n, wt_n, E)
+        assert st == oracle.OK
+        idx2_r, wt2_r, st = oracle.routing_map_to_topk(rm_r, pr_r, K)
+        assert st == oracle.OK
+        L = oracle.layout(idx2_r, E, R)
+        rows, n = L["row_of_slot"], int(L["expert_offsets"][-1])
+        y_n = gi.normal_bf16(np.random.SeedSequence(62 + rep), n, H)
+        grw_n = rng.standard_normal(n).astype(np.float32)
+        with torch.cuda.stream(s):
+            idx.copy_(torch.from_numpy(idx_n))
+            wt.copy_(torch.from_numpy(wt_n))
+            x.copy_(torch.from_numpy(x_n.view(np.int16)))
+            g.copy_(torch.from_numpy(g_n.view(np.int16)))
+            y[:n].copy_(torch.from_numpy(y_n.view(np.int16)))
+            grw[:n].copy_(torch.from_numpy(grw_n))
+            g_graph.replay()
+        s.synchronize()
+        np.testing.assert_array_equal(rm.cpu().numpy(), rm_r)
+        np.testing.assert_array_equal(idx2.cpu().numpy(), idx2_r)
+        np.testing.assert_array_equal(o[3].cpu().numpy(), L["expert_offsets"])
+        r_x, _, _ = oracle.dispatch_bf16(x_n, rows, n)
+        np.testing.assert_array_equal(_u16(recv[:n]), r_x)
+        np.testing.assert_array_equal(_u16(out), oracle.combine(y_n, rows, wt2_r))
+        r_gy, r_gw = oracle.combine_backward(g_n, y_n, rows, wt2_r, n)
+        np.testing.assert_array_equal(_u16(gy[:n]), r_gy)
+        got_gw = gw.cpu().numpy().astype(np.float64)
+        assert (np.abs(got_gw - r_gw) <= _grad_w_bound(g_n, y_n, rows, H)).all()
+        r_gx, r_gtw = oracle.dispatch_backward(r_gy, grw_n, rows)
+        assert_combine(_u16(gx), r_gx)
+        np.testing.assert_array_equal(gtw.cpu().numpy().view(np.uint32), r_gtw.view(np.uint32))
+    del g_graph
+    h.destroy()
+
+
 def test_capture_refuses_host_waits_and_allocation(ep):
     """Inside a stream capture, calls that would allocate or wait for the
     device are refused with EP_ERR_INVALID_ARG and enqueue nothing; the rest
