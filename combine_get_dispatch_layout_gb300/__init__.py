@@ -82,10 +82,20 @@ def status_string(status: int) -> str:
 
 
 def _ptr(t):
+    """Address of a tensor argument (an int is taken as a raw address). The
+    kernels index rows as dense row-major arrays and dereference the address
+    on the GPU, so a non-empty tensor must be contiguous and either on the
+    GPU or in pinned host memory; anything else is refused here, before the
+    call."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if t.numel() > 0:
+        if not t.is_contiguous():
+            raise ValueError("tensor arguments must be contiguous")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError("tensor arguments must be CUDA tensors or pinned host tensors")
     return t.data_ptr()
 
 

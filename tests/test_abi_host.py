@@ -174,3 +174,20 @@ def test_enum_constants_match_header():
     assert {"EP_DTYPE_FP8_E5M2", "EP_SCALE_UE8M0", "EP_ERR_ALLOC"} <= set(enums)
     for name, value in enums.items():
         assert getattr(ep, name) == value, name
+
+
+def test_binding_refuses_tensors_the_kernels_cannot_index():
+    """The binding passes raw addresses: a non-contiguous view or a pageable
+    host tensor is refused before any call (empty tensors and raw ints pass)."""
+    import torch
+    import combine_get_dispatch_layout_gb300 as ep
+    base = torch.zeros(8, 16, dtype=torch.int16)
+    with pytest.raises(ValueError, match="contiguous"):
+        ep._ptr(base[:, :8])
+    with pytest.raises(ValueError, match="contiguous"):
+        ep._ptr(base.t())
+    with pytest.raises(ValueError, match="pinned"):
+        ep._ptr(base)
+    assert ep._ptr(None) is None
+    assert ep._ptr(1234) == 1234
+    assert ep._ptr(torch.empty(0, 4)) is not None
