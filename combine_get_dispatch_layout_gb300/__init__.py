@@ -99,6 +99,41 @@ def _ptr(t):
     return t.data_ptr()
 
 
+def _need(t, nbytes: int, what: str) -> None:
+    """Refuse a tensor that holds fewer bytes than the call will touch (the C
+    ABI takes raw addresses and sizes, so only the binding can see this)."""
+    if t is None or isinstance(t, int) or nbytes <= 0:
+        return
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise ValueError(f"{what}: {have} bytes, the call touches {nbytes}")
+
+
+def _int64(t, what: str) -> None:
+    if t is not None and not isinstance(t, int) and t.dtype != torch.int64:
+        raise ValueError(f"{what} must be int64, got {t.dtype}")
+
+
+def _layout_checks(topk_idx, E: int, R: int, cnt, ntr, itr, off, n_off: int) -> tuple[int, int]:
+    T, K = topk_idx.shape
+    _int64(topk_idx, "topk_idx")
+    _need(cnt, 4 * E, "num_tokens_per_expert")
+    _need(ntr, 4 * R, "num_tokens_per_rank")
+    _need(itr, T * R, "is_token_in_rank")
+    _need(off, 4 * n_off, "offsets")
+    return T, K
+
+
+def _remember(h, T: int, K: int, E: int):
+    h.T, h.K, h.E = T, K, E
+    return h
+
+
+def _tk(handle) -> tuple[int, int]:
+    """(T, K) of the handle's last layout through this binding (0, 0 if unknown)."""
+    return (handle.T or 0, handle.K or 0) if isinstance(handle, Handle) else (0, 0)
+
+
 def _stream(stream):
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -122,6 +157,7 @@ class Handle:
 
     def __init__(self):
         self.ptr = ctypes.c_void_p(None)
+        self.T = self.K = self.E = None   # routing shape of the last layout through this binding
 
     def __bool__(self):
         return bool(self.ptr.value)
@@ -146,60 +182,70 @@ def ep_layout(topk_idx, num_experts: int, num_ranks: int, num_tokens_per_expert,
 
     Reuses `handle` if given (no allocation), else creates one. Returns the handle.
     """
-    T, K = topk_idx.shape
+    T, K = _layout_checks(topk_idx, num_experts, num_ranks, num_tokens_per_expert, num_tokens_per_rank,
+                          is_token_in_rank, expert_offsets, num_experts + 1)
     h = handle if handle is not None else Handle()
     st = lib().ep_layout(_ptr(topk_idx), T, K, num_experts, num_ranks, _ptr(num_tokens_per_expert),
                          _ptr(num_tokens_per_rank), _ptr(is_token_in_rank), _ptr(expert_offsets),
                          _fnptr(alloc_fn), _fnptr(free_fn), ctypes.byref(h.ptr), _stream(stream))
     _check(st, "ep_layout")
-    return h
+    return _remember(h, T, K, num_experts)
 
 
 def ep_layout_aligned(topk_idx, num_experts: int, num_ranks: int, expert_alignment: int,
                       num_tokens_per_expert, num_tokens_per_rank, is_token_in_rank, expert_offsets,
                       handle: Handle | None = None, stream=None, alloc_fn=None, free_fn=None) -> Handle:
     """ep_layout with each expert's rows starting on a multiple of expert_alignment."""
-    T, K = topk_idx.shape
+    T, K = _layout_checks(topk_idx, num_experts, num_ranks, num_tokens_per_expert, num_tokens_per_rank,
+                          is_token_in_rank, expert_offsets, num_experts + 1)
     h = handle if handle is not None else Handle()
     st = lib().ep_layout_aligned(_ptr(topk_idx), T, K, num_experts, num_ranks, int(expert_alignment),
                                  _ptr(num_tokens_per_expert), _ptr(num_tokens_per_rank), _ptr(is_token_in_rank),
                                  _ptr(expert_offsets), _fnptr(alloc_fn), _fnptr(free_fn), ctypes.byref(h.ptr),
                                  _stream(stream))
     _check(st, "ep_layout_aligned")
-    return h
+    return _remember(h, T, K, num_experts)
 
 
 def ep_layout_strided(topk_idx, num_experts: int, num_ranks: int, expert_capacity: int,
                       num_tokens_per_expert, num_tokens_per_rank, is_token_in_rank, expert_offsets,
                       handle: Handle | None = None, stream=None, alloc_fn=None, free_fn=None) -> Handle:
     """ep_layout into the padded 3-D receive buffer [E, expert_capacity, H]."""
-    T, K = topk_idx.shape
+    T, K = _layout_checks(topk_idx, num_experts, num_ranks, num_tokens_per_expert, num_tokens_per_rank,
+                          is_token_in_rank, expert_offsets, num_experts + 1)
     h = handle if handle is not None else Handle()
     st = lib().ep_layout_strided(_ptr(topk_idx), T, K, num_experts, num_ranks, int(expert_capacity),
                                  _ptr(num_tokens_per_expert), _ptr(num_tokens_per_rank), _ptr(is_token_in_rank),
                                  _ptr(expert_offsets), _fnptr(alloc_fn), _fnptr(free_fn), ctypes.byref(h.ptr),
                                  _stream(stream))
     _check(st, "ep_layout_strided")
-    return h
+    return _remember(h, T, K, num_experts)
 
 
 def ep_layout_nonexpand(topk_idx, num_experts: int, num_ranks: int, num_tokens_per_expert,
                         num_tokens_per_rank, is_token_in_rank, rank_offsets, handle: Handle | None = None,
                         stream=None, alloc_fn=None, free_fn=None) -> Handle:
     """Layout with one receive row per (token, rank) pair, grouped by rank."""
-    T, K = topk_idx.shape
+    T, K = _layout_checks(topk_idx, num_experts, num_ranks, num_tokens_per_expert, num_tokens_per_rank,
+                          is_token_in_rank, rank_offsets, num_ranks + 1)
     h = handle if handle is not None else Handle()
     st = lib().ep_layout_nonexpand(_ptr(topk_idx), T, K, num_experts, num_ranks, _ptr(num_tokens_per_expert),
                                    _ptr(num_tokens_per_rank), _ptr(is_token_in_rank), _ptr(rank_offsets),
                                    _fnptr(alloc_fn), _fnptr(free_fn), ctypes.byref(h.ptr), _stream(stream))
     _check(st, "ep_layout_nonexpand")
-    return h
+    return _remember(h, T, K, num_experts)
 
 
 def ep_nonexpand_recv_topk(handle: Handle, topk_idx, num_experts: int, recv_topk_idx, recv_topk_weights=None,
                            topk_weights=None, recv_capacity: int | None = None, stream=None) -> None:
     """Per non-expand receive row: rank-local expert ids (or -1) and weights."""
     cap = int(recv_topk_idx.shape[0]) if recv_capacity is None else int(recv_capacity)
+    T, K = topk_idx.shape
+    _int64(topk_idx, "topk_idx")
+    _int64(recv_topk_idx, "recv_topk_idx")
+    _need(topk_weights, 4 * T * K, "topk_weights")
+    _need(recv_topk_idx, 8 * cap * K, "recv_topk_idx")
+    _need(recv_topk_weights, 4 * cap * K, "recv_topk_weights")
     st = lib().ep_nonexpand_recv_topk(handle.ptr, _ptr(topk_idx), _ptr(topk_weights), num_experts,
                                       _ptr(recv_topk_idx), _ptr(recv_topk_weights), cap, _stream(stream))
     _check(st, "ep_nonexpand_recv_topk")
@@ -209,6 +255,15 @@ def ep_dispatch(handle: Handle, x, out_dtype: int, recv_x, recv_capacity: int, r
                 recv_src_token=None, recv_weights=None, topk_weights=None, stream=None) -> None:
     """Permute x [T, H] bf16 into recv_x (bf16 [cap, H] or uint8 [cap, H] for fp8)."""
     H = x.shape[-1]
+    T, K = _tk(handle)
+    cap = int(recv_capacity)
+    _need(x, 2 * T * H, "x")
+    _need(recv_x, cap * H * (2 if out_dtype == EP_DTYPE_BF16 else 1), "recv_x")
+    if out_dtype != EP_DTYPE_BF16:
+        _need(recv_scales, 4 * cap * (H // 128), "recv_scales")
+    _need(recv_src_token, 4 * cap, "recv_src_token")
+    _need(recv_weights, 4 * cap, "recv_weights")
+    _need(topk_weights, 4 * T * K, "topk_weights")
     st = lib().ep_dispatch(handle.ptr, _ptr(x), H, out_dtype, _ptr(topk_weights), _ptr(recv_x),
                            _ptr(recv_scales), _ptr(recv_src_token), _ptr(recv_weights),
                            int(recv_capacity), _stream(stream))
@@ -222,6 +277,19 @@ def ep_dispatch_ex(handle: Handle, x, recv_x, recv_capacity: int, out_dtype: int
     """ep_dispatch with fp8 scale modes, column-major scales, fp8 input pass-through and
     overlap with the layout that precedes it on the stream."""
     H = int(x.shape[-1]) if H is None else int(H)
+    T, K = _tk(handle)
+    cap = int(recv_capacity)
+    nb = H // 128
+    sbytes = 1 if scale_mode == EP_SCALE_UE8M0 else 4
+    _need(x, T * H * (2 if in_dtype == EP_DTYPE_BF16 else 1), "x")
+    if in_dtype != EP_DTYPE_BF16:
+        _need(x_scales, sbytes * T * nb, "x_scales")
+    _need(recv_x, cap * H * (2 if out_dtype == EP_DTYPE_BF16 else 1), "recv_x")
+    if out_dtype != EP_DTYPE_BF16:
+        _need(recv_scales, sbytes * (nb * int(scales_ld) if scales_col_major else cap * nb), "recv_scales")
+    _need(recv_src_token, 4 * cap, "recv_src_token")
+    _need(recv_weights, 4 * cap, "recv_weights")
+    _need(topk_weights, 4 * T * K, "topk_weights")
     cfg = DispatchConfig(in_dtype, out_dtype, scale_mode, 1 if scales_col_major else 0, int(scales_ld),
                          1 if overlap_layout else 0)
     st = lib().ep_dispatch_ex(handle.ptr, _ptr(x), _ptr(x_scales), H, ctypes.byref(cfg), _ptr(topk_weights),
@@ -234,6 +302,10 @@ def ep_combine(handle: Handle, y, out, topk_weights=None, y_rows: int | None = N
     """out [T, H] bf16 = weighted sum over each token's slots of y [rows, H] bf16."""
     H = y.shape[-1] if y is not None else out.shape[-1]
     rows = int(y.shape[0]) if y_rows is None else int(y_rows)
+    T, K = _tk(handle)
+    _need(y, 2 * rows * H, "y")
+    _need(out, 2 * T * H, "out")
+    _need(topk_weights, 4 * T * K, "topk_weights")
     st = lib().ep_combine(handle.ptr, _ptr(y), rows, H, _ptr(topk_weights), _ptr(out), _stream(stream))
     _check(st, "ep_combine")
 
@@ -245,6 +317,12 @@ def ep_combine_backward(handle: Handle, grad_out, y=None, topk_weights=None, gra
     H = grad_out.shape[-1]
     rows = (int(y.shape[0]) if y is not None else 0) if y_rows is None else int(y_rows)
     cap = (int(grad_y.shape[0]) if grad_y is not None else 0) if grad_y_capacity is None else int(grad_y_capacity)
+    T, K = _tk(handle)
+    _need(grad_out, 2 * T * H, "grad_out")
+    _need(y, 2 * rows * H, "y")
+    _need(topk_weights, 4 * T * K, "topk_weights")
+    _need(grad_y, 2 * cap * H, "grad_y")
+    _need(grad_topk_weights, 4 * T * K, "grad_topk_weights")
     st = lib().ep_combine_backward(handle.ptr, _ptr(grad_out), _ptr(y), rows, H, _ptr(topk_weights), _ptr(grad_y),
                                    cap, _ptr(grad_topk_weights), _stream(stream))
     _check(st, "ep_combine_backward")
@@ -255,6 +333,11 @@ def ep_dispatch_backward(handle: Handle, grad_recv, grad_x, grad_recv_weights=No
     """grad_x[t] = bf16(sum_k grad_recv[row(t,k)]); grad_topk_weights[t,k] = grad_recv_weights[row]."""
     H = grad_x.shape[-1]
     rows = int(grad_recv.shape[0]) if grad_rows is None else int(grad_rows)
+    T, K = _tk(handle)
+    _need(grad_recv, 2 * rows * H, "grad_recv")
+    _need(grad_recv_weights, 4 * rows, "grad_recv_weights")
+    _need(grad_x, 2 * T * H, "grad_x")
+    _need(grad_topk_weights, 4 * T * K, "grad_topk_weights")
     st = lib().ep_dispatch_backward(handle.ptr, _ptr(grad_recv), rows, H, _ptr(grad_recv_weights), _ptr(grad_x),
                                     _ptr(grad_topk_weights), _stream(stream))
     _check(st, "ep_dispatch_backward")
@@ -264,6 +347,11 @@ def ep_topk_to_routing_map(topk_idx, num_experts: int, routing_map, topk_weights
                            device_error=None, stream=None) -> None:
     """routing_map [T, E] u8 (and probs [T, E] fp32) from topk_idx [T, K]."""
     T, K = topk_idx.shape
+    _int64(topk_idx, "topk_idx")
+    _need(topk_weights, 4 * T * K, "topk_weights")
+    _need(routing_map, T * num_experts, "routing_map")
+    _need(probs, 4 * T * num_experts, "probs")
+    _need(device_error, 4, "device_error")
     st = lib().ep_topk_to_routing_map(_ptr(topk_idx), _ptr(topk_weights), T, K, num_experts, _ptr(routing_map),
                                       _ptr(probs), _ptr(device_error), _stream(stream))
     _check(st, "ep_topk_to_routing_map")
@@ -273,6 +361,11 @@ def ep_routing_map_to_topk(routing_map, num_topk: int, topk_idx, probs=None, top
                            device_error=None, stream=None) -> None:
     """topk_idx [T, K] int64 (and weights) from routing_map [T, E], experts ascending."""
     T, E = routing_map.shape
+    _int64(topk_idx, "topk_idx")
+    _need(probs, 4 * T * E, "probs")
+    _need(topk_idx, 8 * T * num_topk, "topk_idx")
+    _need(topk_weights, 4 * T * num_topk, "topk_weights")
+    _need(device_error, 4, "device_error")
     st = lib().ep_routing_map_to_topk(_ptr(routing_map), _ptr(probs), T, E, num_topk, _ptr(topk_idx),
                                       _ptr(topk_weights), _ptr(device_error), _stream(stream))
     _check(st, "ep_routing_map_to_topk")
@@ -289,6 +382,8 @@ def ep_handle_query(handle: Handle) -> tuple[int, int]:
 
 
 def ep_handle_copy_row_of_slot(handle: Handle, dst, stream=None) -> None:
+    T, K = _tk(handle)
+    _need(dst, 4 * T * K, "dst")
     _check(lib().ep_handle_copy_row_of_slot(handle.ptr, _ptr(dst), _stream(stream)),
            "ep_handle_copy_row_of_slot")
 
@@ -299,7 +394,10 @@ def ep_layout_noalloc(topk_idx, num_experts: int, num_ranks: int, num_tokens_per
     """ep_layout without a handle or any allocation: the slot -> row map goes
     to the caller's row_of_slot [T, K] int32; scratch is the library's fixed
     array (one call at a time per device, ordered on one stream)."""
-    T, K = topk_idx.shape
+    T, K = _layout_checks(topk_idx, num_experts, num_ranks, num_tokens_per_expert, num_tokens_per_rank,
+                          is_token_in_rank, expert_offsets, num_experts + 1)
+    _need(row_of_slot, 4 * T * K, "row_of_slot")
+    _need(device_error, 4, "device_error")
     st = lib().ep_layout_noalloc(_ptr(topk_idx), T, K, num_experts, num_ranks, _ptr(num_tokens_per_expert),
                                  _ptr(num_tokens_per_rank), _ptr(is_token_in_rank), _ptr(expert_offsets),
                                  _ptr(row_of_slot), _ptr(device_error), _stream(stream))

@@ -191,3 +191,42 @@ def test_binding_refuses_tensors_the_kernels_cannot_index():
     assert ep._ptr(None) is None
     assert ep._ptr(1234) == 1234
     assert ep._ptr(torch.empty(0, 4)) is not None
+
+
+def test_binding_refuses_wrong_types_and_short_buffers():
+    """Index arrays must be int64 and every tensor must hold the bytes the
+    call will touch; the binding raises before any call into the library."""
+    import torch
+    import combine_get_dispatch_layout_gb300 as ep
+    T, K, E, R, H = 4, 2, 8, 2, 256
+    idx = torch.zeros(T, K, dtype=torch.int64)
+    i32 = lambda n: torch.zeros(n, dtype=torch.int32)
+    outs = [i32(E), i32(R), torch.zeros(T, R, dtype=torch.uint8), i32(E + 1)]
+    with pytest.raises(ValueError, match="int64"):
+        ep.ep_layout(idx.to(torch.int32), E, R, *outs)
+    with pytest.raises(ValueError, match="is_token_in_rank"):
+        ep.ep_layout(idx, E, R, outs[0], outs[1], torch.zeros(T * R - 1, dtype=torch.uint8), outs[3])
+    with pytest.raises(ValueError, match="offsets"):
+        ep.ep_layout(idx, E, R, outs[0], outs[1], outs[2], i32(E))
+    h = ep.Handle()
+    h.T, h.K, h.E = T, K, E                      # a routing shape, no library handle
+    x = torch.zeros(T, H, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="recv_x"):
+        ep.ep_dispatch(h, x, ep.EP_DTYPE_BF16, torch.zeros(T * K - 1, H, dtype=torch.bfloat16), T * K)
+    with pytest.raises(ValueError, match="recv_scales"):
+        ep.ep_dispatch_ex(h, x, torch.zeros(T * K, H, dtype=torch.uint8), T * K,
+                          recv_scales=torch.zeros(T * K, H // 128 - 1, dtype=torch.float32))
+    with pytest.raises(ValueError, match="topk_weights"):
+        ep.ep_dispatch(h, x, ep.EP_DTYPE_BF16, torch.zeros(T * K, H, dtype=torch.bfloat16), T * K,
+                       recv_weights=torch.zeros(T * K), topk_weights=torch.zeros(T, K - 1))
+    with pytest.raises(ValueError, match="out"):
+        ep.ep_combine(h, torch.zeros(T * K, H, dtype=torch.bfloat16), torch.zeros(T - 1, H, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="grad_x"):
+        ep.ep_dispatch_backward(h, torch.zeros(T * K, H, dtype=torch.bfloat16),
+                                torch.zeros(T - 1, H, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="routing_map"):
+        ep.ep_topk_to_routing_map(idx, E, torch.zeros(T, E - 1, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="topk_idx"):
+        ep.ep_routing_map_to_topk(torch.zeros(T, E, dtype=torch.uint8), K, torch.zeros(T, K, dtype=torch.int32))
+    with pytest.raises(ValueError, match="dst"):
+        ep.ep_handle_copy_row_of_slot(h, i32(T * K - 1))

@@ -966,7 +966,8 @@ def test_dispatch_ex_rejects_fp8_type_mismatch(ep, in_dt, out_dt):
     w = inp.w
     h = _layout_dev(ep, inp)
     n = w.T * w.K
-    q = torch.full((n, w.H), SENT8, dtype=torch.uint8, device="cuda")
+    # sized for the requested output type, so the call reaches the library
+    q = torch.full((n, w.H * (2 if out_dt == ep.EP_DTYPE_BF16 else 1)), SENT8, dtype=torch.uint8, device="cuda")
     sc = torch.zeros((n, w.H // 128), dtype=torch.float32, device="cuda")
     xs = torch.ones((w.T, w.H // 128), dtype=torch.float32, device="cuda")
     x = torch.zeros((w.T, w.H), dtype=torch.bfloat16, device="cuda")
