@@ -20,19 +20,28 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _SO = os.path.join(_HERE, "liboracle.so")
+# A prebuilt library to load instead (tests/test_oracle_mutations.py points
+# it at copies of oracle.c with a planted mistake); nothing is compiled then.
+_OVERRIDE = os.environ.get("ORACLE_LIBRARY") or None
 _LIB = None
 _LOCK = threading.Lock()
 
 OK, ERR_ARG, ERR_EXPERT, ERR_CAPACITY = 0, 1, 2, 3
 
 
+def compile_command(src: str, out: str) -> list[str]:
+    """gcc command that builds the oracle library from `src` into `out`."""
+    return ["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fno-fast-math",
+            "-fno-strict-aliasing", "-fPIC", "-shared", "-o", out, src, "-lm"]
+
+
 def build(force: bool = False) -> str:
     """Compile oracle.c into liboracle.so (IEEE fp32, no contraction)."""
+    if _OVERRIDE:
+        return _OVERRIDE
     if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
         tmp = _SO + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fno-fast-math",
-               "-fno-strict-aliasing", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
-        subprocess.run(cmd, check=True)
+        subprocess.run(compile_command(_SRC, tmp), check=True)
         os.replace(tmp, _SO)
     return _SO
 
@@ -41,8 +50,7 @@ def _lib():
     global _LIB
     with _LOCK:
         if _LIB is None:
-            build()
-            L = ctypes.CDLL(_SO)
+            L = ctypes.CDLL(build())
             P = ctypes.c_void_p
             i64, i32 = ctypes.c_int64, ctypes.c_int
             L.orc_layout.argtypes = [P, i64, i32, i32, i32, P, P, P, P, P]

@@ -831,3 +831,56 @@ def test_layout_nonexpand_vs_brute(case):
     r = a["row_of_slot"]
     assert np.array_equal(np.sort(r[r >= 0]), np.arange(n))
     assert n == int(a["is_token_in_rank"].sum())
+
+
+# ------------------------------------------------------------------ division, not reciprocal
+
+def _reciprocal_traps(F, values, torch_codes, limit=6):
+    """(amax, x) bf16 pairs, 0 < x <= amax, for which the fp8 code of RN(x / s)
+    differs from that of RN(x * RN(1 / s)), s = RN(amax / F) in fp32: a
+    quantiser that multiplies by the reciprocal instead of dividing gets these
+    wrong. Found with numpy's IEEE fp32 arithmetic, the fp8 code table and
+    torch's fp8 cast only: x is taken next to s times each rounding midpoint
+    of the fp8 grid, where the two quotients can fall on either side."""
+    v = np.unique(np.abs(values))
+    mids = (v[1:] + v[:-1]) / 2
+    mids = mids[mids < F]
+    e = np.arange(107, 148, dtype=np.uint32)                    # amax in [2^-20, 2^21)
+    m = (((e[:, None] << 7) | np.arange(128, dtype=np.uint32)[None, :]).ravel() << 16).view(np.float32)
+    s = m / np.float32(F)
+    r = np.float32(1.0) / s
+    found = []
+    for M in mids:
+        target = (np.float64(M) * s.astype(np.float64)).astype(np.float32).view(np.uint32) & np.uint32(0xFFFF0000)
+        for bits in (target, target + np.uint32(0x10000)):
+            x = bits.view(np.float32)
+            ok = (x > 0) & (x <= m)
+            qd, qr = x / s, x * r
+            hit = ok & (torch_codes(qd) != torch_codes(qr))
+            for i in np.flatnonzero(hit):
+                found.append((m[i], x[i], int(torch_codes(qd[i:i + 1])[0])))
+                if len(found) >= limit:
+                    return found
+    return found
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_quantiser_divides_rather_than_multiplying_by_the_reciprocal(fmt):
+    """The reading of the fp8 formula is q = fp8(x / scale) by IEEE division.
+    On blocks built around the traps above, the oracle's code for x is the
+    code of the true quotient, not of x times the rounded reciprocal."""
+    if fmt == "e4m3":
+        F, values, codes_of = 448.0, brute.e4m3_values()[1], _torch_e4m3_bits
+        quant = lambda row: oracle.quant_row_e4m3(row)
+    else:
+        F, values, codes_of = 57344.0, brute.e5m2_values()[1], _torch_e5m2_bits
+        quant = lambda row: oracle.quant_row_e5m2(row, 0)
+    traps = _reciprocal_traps(F, values, codes_of)
+    assert len(traps) >= 3, "the search should find traps in this amax range"
+    for amax, x, code in traps:
+        row = np.zeros(128, np.uint16)
+        row[0] = gi.f32_to_bf16_bits(np.array([amax], np.float32))[0]
+        row[1] = gi.f32_to_bf16_bits(np.array([x], np.float32))[0]
+        q, sc = quant(row)
+        assert sc[0] == np.float32(amax) / np.float32(F)
+        assert q[1] == code, (fmt, float(amax), float(x))
