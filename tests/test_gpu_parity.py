@@ -788,6 +788,47 @@ def _layout_dev(ep, inp, A=1):
     return ep.ep_layout_aligned(_dev(inp.topk_idx), w.E, w.R, A, *o)
 
 
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fp8_dispatch_divides_on_reciprocal_traps(ep, fmt):
+    """Blocks built around (amax, x) pairs where x / scale and x * (1 / scale)
+    give different fp8 codes (found with numpy's IEEE division and torch's fp8
+    cast): the fp8 dispatch must give the code of the true quotient, as the
+    oracle does. Random data almost never reaches these pairs."""
+    from test_oracle_pins import _reciprocal_traps, _torch_e4m3_bits, _torch_e5m2_bits
+    from oracle import brute
+    if fmt == "e4m3":
+        F, values, codes_of, dt = 448.0, brute.e4m3_values()[1], _torch_e4m3_bits, ep.EP_DTYPE_FP8_E4M3
+    else:
+        F, values, codes_of, dt = 57344.0, brute.e5m2_values()[1], _torch_e5m2_bits, ep.EP_DTYPE_FP8_E5M2
+    traps = _reciprocal_traps(F, values, codes_of)
+    assert len(traps) >= 3
+    T, H = len(traps), 256                     # two blocks per row: the trap block and its mirror
+    xf = np.zeros((T, H), np.float32)
+    for t, (amax, x, _) in enumerate(traps):
+        xf[t, 0], xf[t, 1] = amax, x
+        xf[t, 128], xf[t, 200] = -amax, -x
+    x_bits = gi.f32_to_bf16_bits(xf)
+    idx = np.zeros((T, 1), np.int64)
+    w = gi.Workload("traps", T=T, H=H, E=1, K=1, R=1)
+    inp = gi.Inputs(w=w, seed=0, x=x_bits, topk_idx=idx, topk_weights=np.ones((T, 1), np.float32), y=None,
+                    num_valid=T)
+    h = _layout_dev(ep, inp)
+    q = torch.full((T, H), SENT8, dtype=torch.uint8, device="cuda")
+    sc = torch.zeros((T, H // 128), dtype=torch.float32, device="cuda")
+    ep.ep_dispatch_ex(h, _dev(x_bits.view(np.int16), torch.bfloat16), q, T, out_dtype=dt, recv_scales=sc)
+    torch.cuda.synchronize()
+    rows = np.arange(T, dtype=np.int32)[:, None]
+    if fmt == "e4m3":
+        r_q, r_s, _, _ = oracle.dispatch_e4m3(x_bits, rows, T)
+    else:
+        r_q, r_s = oracle.dispatch_e5m2(x_bits, rows, T, 0)
+    got = q.cpu().numpy()
+    np.testing.assert_array_equal(got, r_q)
+    np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint32), r_s.view(np.uint32))
+    assert [int(got[t, 1]) for t in range(T)] == [c for _, _, c in traps]
+    h.destroy()
+
+
 def fp8_variant(ep, inp, mode, col_major=False, A=1, fmt=1):
     w = inp.w
     ref = oracle.layout_aligned(inp.topk_idx, w.E, w.R, A)
