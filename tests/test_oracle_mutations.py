@@ -16,7 +16,9 @@ import oracle
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "oracle.c")
 
-# (name, text in oracle.c, replacement, which occurrence)
+# (name, text in oracle.c, replacement, which occurrence). Left out because no
+# input can tell it apart: removing the e4m3 encoder's final clamp of codes
+# above 0x7E (below 448 the grid step is 32, so nothing there rounds past 448).
 MUTATIONS = [
     ("bf16 ties round up", "(lo == 0x8000u && (hi & 1u))", "(lo == 0x8000u)", 0),
     ("e4m3 ties round up", "double m = rint(ldexp(a, 3 - E));", "double m = floor(ldexp(a, 3 - E) + 0.5);", 0),
@@ -62,6 +64,33 @@ MUTATIONS = [
      "for (int e = E - 1; e >= 0; --e) {\n            if (!routing_map[t * E + e]) continue;", 0),
     ("non-expand row for every slot of a rank", "if (ej >= 0 && ej < E && ej / L == r) { first = 0; break; }",
      "if (0) { first = 0; break; }", 0),
+    ("alignment pads exact multiples", "run += (c + A - 1) / A * A;", "run += (c + A) / A * A;", 0),
+    ("e4m3 saturates to NaN", "if (a >= 448.0) return (uint8_t)(sign | 0x7E);",
+     "if (a >= 448.0) return (uint8_t)(sign | 0x7F);", 0),
+    ("e5m2 saturates to infinity", "if (a >= 57344.0) return (uint8_t)(sign | 0x7B);",
+     "if (a >= 57344.0) return (uint8_t)(sign | 0x7C);", 0),
+    ("zero block gets scale 1", "srow[b] = 0.0f;", "srow[b] = 1.0f;", 0),
+    ("source token is the slot index", "if (recv_src_token) recv_src_token[row] = (int32_t)t;",
+     "if (recv_src_token) recv_src_token[row] = (int32_t)k;", 0),
+    ("missing weights read as zero", "float wk = w ? w[k] : 1.0f;", "float wk = w ? w[k] : 0.0f;", 0),
+    ("invalid expert id not reported", "if (e < -1 || e >= E) { status = ORC_ERR_EXPERT; continue; }",
+     "if (e < -1 || e >= E) { continue; }", 0),
+    ("routing map without probs gives zero weights",
+     "topk_weights[t * K + k] = probs ? probs[t * E + e] : 1.0f;",
+     "topk_weights[t * K + k] = probs ? probs[t * E + e] : 0.0f;", 0),
+    ("strided capacity off by one", "if (rank_in_expert >= cap) {", "if (rank_in_expert > cap) {", 0),
+    ("strided overflow not reported", "if (status == ORC_OK) status = ORC_ERR_CAPACITY;", ";", 0),
+    ("pad rows keep source 0", "if (src) src[r] = -1;", "if (src) src[r] = 0;", 0),
+    ("pad rows half zeroed", "memset(recv + r * row_bytes, 0, (size_t)row_bytes);",
+     "memset(recv + r * row_bytes, 0, (size_t)row_bytes / 2);", 0),
+    ("probs keep the last weight instead of the sum", "probs[t * E + e] += w[t * K + k];",
+     "probs[t * E + e] = w[t * K + k];", 0),
+    ("non-expand rank offsets inclusive",
+     "for (int r = 0; r < R; ++r) { rank_offsets[r] = (int32_t)run; run += num_tokens_per_rank[r]; }",
+     "for (int r = 0; r < R; ++r) { run += num_tokens_per_rank[r]; rank_offsets[r] = (int32_t)run; }", 0),
+    ("dropped slot gets weight gradient 1",
+     "grad_topk_weights[s] = row >= 0 ? grad_recv_weights[row] : 0.0f;",
+     "grad_topk_weights[s] = row >= 0 ? grad_recv_weights[row] : 1.0f;", 0),
 ]
 
 

@@ -766,6 +766,24 @@ def test_routing_map_round_trip_vs_numpy(seed):
         np.testing.assert_array_equal(a[key], b[key])
 
 
+def test_routing_map_repeated_expert_and_no_probs():
+    """Hand-worked: a token naming expert 1 twice gets one map entry whose
+    probability is the sum of both weights in ascending k (nccl_ep.cc,
+    ncclEpDispatch: sparse_to_dense_prob, read as a sum over the slots naming
+    the expert): 0.25 + 0.5 = 0.75. A map given without probabilities converts
+    back with unit weights, the unweighted convention of the combine (no
+    weights means 1), and -1 / 0 in the unused slots."""
+    idx = np.array([[1, 1, 3]], np.int64)
+    w = np.array([[0.25, 0.5, 0.125]], np.float32)
+    rm, pr, st = oracle.topk_to_routing_map(idx, w, 4)
+    assert st == oracle.OK
+    assert rm.tolist() == [[0, 1, 0, 1]]
+    assert pr.tolist() == [[0.0, 0.75, 0.0, 0.125]]
+    bi, bw, st = oracle.routing_map_to_topk(rm, None, 3)
+    assert st == oracle.OK
+    assert bi.tolist() == [[1, 3, -1]] and bw.tolist() == [[1.0, 1.0, 0.0]]
+
+
 def test_routing_map_too_many_experts():
     rm = np.ones((2, 8), np.uint8)
     _, _, st = oracle.routing_map_to_topk(rm, None, 4)
