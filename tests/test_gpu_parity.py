@@ -1095,6 +1095,25 @@ def test_routing_map_vector_and_scalar_forms(ep, E, K, T, offset):
     assert (st != oracle.OK) == over          # the oracle flags the same inputs
 
 
+@pytest.mark.parametrize("E", [64, 700])       # vector and scalar kernel forms
+def test_routing_map_to_topk_without_probs_gives_unit_weights(ep, E):
+    """A map given without probabilities converts to its experts with unit
+    weights and 0 in the unused slots, as the oracle does."""
+    rng = np.random.default_rng(E)
+    T, K = 300, 6
+    dense = ((rng.random((T, E)) < 3.0 / E) * rng.integers(1, 256, (T, E))).astype(np.uint8)
+    dense[(dense != 0).sum(axis=1) > K] = 0            # keep every row within K experts
+    r_idx, r_w, st = oracle.routing_map_to_topk(dense, None, K)
+    assert st == oracle.OK
+    out_i = torch.full((T, K), -9, dtype=torch.int64, device="cuda")
+    out_w = torch.full((T, K), -1.0, dtype=torch.float32, device="cuda")
+    ep.ep_routing_map_to_topk(_dev(dense), K, out_i, topk_weights=out_w)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out_i.cpu().numpy(), r_idx)
+    np.testing.assert_array_equal(out_w.cpu().numpy().view(np.uint32), r_w.view(np.uint32))
+    assert set(np.unique(r_w).tolist()) <= {0.0, 1.0}
+
+
 def test_routing_map_errors(ep):
     idx = torch.tensor([[0, 9], [1, -3]], dtype=torch.int64, device="cuda")
     rm = torch.empty((2, 8), dtype=torch.uint8, device="cuda")
