@@ -116,15 +116,14 @@ def outcomes(tmp_path_factory):
     jobs = [("unmodified", src)] + [(name, _mutate(src, old, new, occ)) for name, old, new, occ in MUTATIONS]
 
     def one(job):
-        name, text = job
-        tag = str(abs(hash(name)))
-        c, so = str(d / f"m{tag}.c"), str(d / f"m{tag}.so")
+        i, (name, text) = job
+        c, so = str(d / f"m{i}.c"), str(d / f"m{i}.so")
         open(c, "w").write(text)
         subprocess.run(oracle.compile_command(c, so), check=True)
         return name, _run_pins(so)
 
     with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
-        return dict(ex.map(one, jobs))
+        return dict(ex.map(one, enumerate(jobs)))
 
 
 def test_mutations_apply_to_the_source():
