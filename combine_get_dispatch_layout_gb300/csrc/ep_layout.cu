@@ -11,7 +11,8 @@
 // inside an expert are in ascending (token, k) order, which makes the
 // permutation deterministic.
 //
-// GPU design (three short launches, no host sync, no memset):
+// GPU design for large routings (three short launches, each a programmatic
+// dependent of the one before; no host sync, no memset):
 //   count  : each warp owns a chunk of consecutive tokens and builds its
 //            chunk's expert histogram with warp-aggregated updates
 //            (lanes with the same expert found with one ballot per key bit;
