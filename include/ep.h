@@ -27,7 +27,12 @@
  *    mapped into the unified address space (cudaHostAlloc / cudaHostRegister;
  *    on GB300 the kernels then stream it over NVLink-C2C, which is how a
  *    caller with host-resident tokens avoids a separate copy). The caller
- *    owns them; the library never frees caller memory.
+ *    owns them; the library never frees caller memory. The library sees
+ *    addresses and sizes only: every buffer must hold at least the elements
+ *    its call documents (rows x row length for the sizes passed), in the
+ *    stated element type, or kernels read or write past it. Alignment is
+ *    checked (EP_ERR_INVALID_ARG); lengths cannot be. The Python binding
+ *    checks both against the tensors it is given.
  *  - All device work is enqueued on `stream` (a cudaStream_t; NULL = the
  *    legacy default stream) and is asynchronous, except where a call says it
  *    synchronises.
