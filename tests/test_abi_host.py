@@ -230,3 +230,28 @@ def test_binding_refuses_wrong_types_and_short_buffers():
         ep.ep_routing_map_to_topk(torch.zeros(T, E, dtype=torch.uint8), K, torch.zeros(T, K, dtype=torch.int32))
     with pytest.raises(ValueError, match="dst"):
         ep.ep_handle_copy_row_of_slot(h, i32(T * K - 1))
+
+
+def test_header_is_plain_c99_and_links(tmp_path):
+    """include/ep.h compiles as strict C99 (no C++ constructs) and a C program
+    links against libep.so and calls it (ep_status_string needs no GPU)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not found")
+    import combine_get_dispatch_layout_gb300 as ep
+    ep.lib()                                             # built in-tree
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    libdir = os.path.join(root, "combine_get_dispatch_layout_gb300")
+    src = tmp_path / "use_ep.c"
+    src.write_text('#include <string.h>\n#include "ep.h"\n'
+                   'int main(void) {\n'
+                   '    ep_handle_t h = 0;\n'
+                   '    (void)h;\n'
+                   '    return strcmp(ep_status_string(EP_OK), ep_status_string(EP_ERR_INVALID_ARG)) == 0;\n'
+                   '}\n')
+    exe = tmp_path / "use_ep"
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(root, "include"),
+                    str(src), "-L", libdir, "-lep", f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    assert subprocess.run([str(exe)]).returncode == 0
