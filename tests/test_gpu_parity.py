@@ -6,6 +6,8 @@ scales, receive-side token ids and weights are bit-exact; combine is within
 1 bf16 ulp per element (the stated tolerance; both sides use the same fp32
 fused multiply-add order, so the test also reports exact matches).
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -438,6 +440,45 @@ def test_handle_reuse_grow_and_shrink(ep):
         h = run.h
         check_layout(run, oracle.layout(idx, E, R))
     h.destroy()
+
+
+def test_c_program_runs_the_step_through_the_abi(ep, tmp_path):
+    """tests/c_abi_step.c links libep.so and the CUDA runtime directly, with
+    no Python between the caller and the library, and runs layout -> bf16
+    dispatch -> combine on device buffers it allocates itself; its outputs
+    match the oracle."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not found")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    libdir = os.path.join(root, "combine_get_dispatch_layout_gb300")
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    exe = str(tmp_path / "c_abi_step")
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(root, "include"),
+                    "-I", os.path.join(cuda, "include"), os.path.join(root, "tests", "c_abi_step.c"),
+                    "-L", libdir, "-lep", "-L", os.path.join(cuda, "lib64"), "-lcudart",
+                    f"-Wl,-rpath,{libdir}", f"-Wl,-rpath,{os.path.join(cuda, 'lib64')}", "-o", exe], check=True)
+    inp = gi.make("decode", 71)
+    w = inp.w
+    T, K, E, R, H = w.T, w.K, w.E, w.R, w.H
+    n = inp.num_valid
+    y = np.zeros((T * K, H), np.uint16)
+    y[:n] = inp.y
+    inp.topk_idx.astype(np.int64).tofile(tmp_path / "topk_idx.bin")
+    inp.x.astype(np.uint16).tofile(tmp_path / "x.bin")
+    y.tofile(tmp_path / "y.bin")
+    inp.topk_weights.astype(np.float32).tofile(tmp_path / "w.bin")
+    r = subprocess.run([exe, str(T), str(K), str(E), str(R), str(H), str(tmp_path)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    ref = oracle.layout(inp.topk_idx, E, R)
+    np.testing.assert_array_equal(np.fromfile(tmp_path / "counts.bin", np.int32), ref["num_tokens_per_expert"])
+    np.testing.assert_array_equal(np.fromfile(tmp_path / "offsets.bin", np.int32), ref["expert_offsets"])
+    r_x, _, _ = oracle.dispatch_bf16(inp.x, ref["row_of_slot"], n)
+    np.testing.assert_array_equal(np.fromfile(tmp_path / "recv.bin", np.uint16).reshape(n, H), r_x)
+    r_out = oracle.combine(inp.y, ref["row_of_slot"], inp.topk_weights)
+    np.testing.assert_array_equal(np.fromfile(tmp_path / "out.bin", np.uint16).reshape(T, H), r_out)
 
 
 def test_handle_churn_returns_device_memory(ep):
