@@ -53,7 +53,8 @@ constexpr int kRoundsInFlight = 4;   // 32-slot rounds whose loads are issued to
 constexpr int kMaxKeyBits = 13;      // E + 1 <= 4097 distinct keys (EP_MAX_EXPERTS = 4096)
 constexpr size_t kClusterSmemBudget = 200 * 1024;
 constexpr int kMaxClusterCtas = 16;
-constexpr int kMaxRounds = 8;        // cluster path: slots per warp <= 8 * 32
+constexpr int kMaxRounds = 16;       // cluster path: slots per warp <= 16 * 32
+constexpr int kSmallRounds = 8;      // up to this many rounds keys and ranks stay unpacked
 constexpr int64_t kClusterMaxSlots = int64_t{1} << 18;   // larger routings use the multi-block path
 
 __device__ __forceinline__ unsigned lanemask_lt() {
@@ -352,15 +353,21 @@ __device__ __forceinline__ unsigned rank_of(unsigned e, const LayoutPlan& p) {
 }
 
 // Single-launch layout by one cluster of p.cl_ctas CTAs, p.cl_warps warps each.
-// Warp g (CTA-major) owns tokens [g*ct, (g+1)*ct), at most kMaxRounds rounds
-// of 32 slots, whose keys and stable local ranks stay in registers.
+// Warp g (CTA-major) owns tokens [g*ct, (g+1)*ct), at most kRounds rounds
+// of 32 slots, whose keys and stable local ranks stay in registers: as two
+// arrays for up to kSmallRounds rounds, else packed one per round as
+// (key + 1) | (local rank << 13) (keys take 13 bits for E <= 4096, local
+// ranks 9 for at most 512 slots a warp), which fits 16 rounds in the same
+// registers.
 // Shared memory (ints, sized for 16 CTAs): hist[W][E] | all_tot[16][E] |
 // all_rank[16][R] | all_bad[16] | tail[max(W * ct_cap, 2E)], where the tail
 // holds the token rank masks (R <= 32) and later the offsets and CTA bases.
 // With E no larger than the CTA's thread count (and no fixed stride) each
 // thread owns one expert in the offset scan, which then runs in registers.
+template <int kRounds>
 __global__ void __launch_bounds__(1024, 1)
 layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
+    constexpr bool kPacked = kRounds > kSmallRounds;
     // Launched as the preceding kernel's programmatic dependent: it zeroes
     // its own shared memory, then waits for that kernel (and so for all
     // earlier work) before touching global memory; only then may a dispatch
@@ -407,12 +414,13 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
     const int t0 = min(p.T, g * ct);
     const int t1 = min(p.T, t0 + ct);
     const int64_t s0 = static_cast<int64_t>(t0) * p.K, s1 = static_cast<int64_t>(t1) * p.K;
-    const int nr = static_cast<int>((s1 - s0 + 31) / 32);   // <= kMaxRounds (host check)
+    const int nr = static_cast<int>((s1 - s0 + 31) / 32);   // <= kRounds (host check)
     const unsigned lt = lanemask_lt();
-    int key_r[kMaxRounds], loc_r[kMaxRounds];
+    int key_r[kPacked ? 1 : kRounds], loc_r[kPacked ? 1 : kRounds];
+    unsigned kl_r[kPacked ? kRounds : 1];
     bool any_bad = false;
 #pragma unroll
-    for (int j0 = 0; j0 < kMaxRounds; j0 += kRoundsInFlight) {
+    for (int j0 = 0; j0 < kRounds; j0 += kRoundsInFlight) {
         if (j0 >= nr) break;
         int64_t e_r[kRoundsInFlight];
 #pragma unroll
@@ -439,8 +447,12 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
             __syncwarp();
             if (key >= 0 && lane == __ffs(peers) - 1) mine[key] += __popc(peers);
             __syncwarp();
-            key_r[j0 + j] = key;
-            loc_r[j0 + j] = loc;
+            if constexpr (kPacked) {
+                kl_r[j0 + j] = key >= 0 ? (static_cast<unsigned>(key + 1) | (static_cast<unsigned>(loc) << 13)) : 0u;
+            } else {
+                key_r[j0 + j] = key;
+                loc_r[j0 + j] = loc;
+            }
         }
     }
     const bool warp_bad = __any_sync(kFullMask, any_bad);
@@ -655,13 +667,20 @@ layout_cluster_kernel(LayoutPlan p, LayoutArgs a) {
     // ---- phase 4: row = expert offset + rows in lower CTAs + rows in lower
     // warps of this CTA + the slot's local rank
 #pragma unroll
-    for (int j = 0; j < kMaxRounds; ++j) {
+    for (int j = 0; j < kRounds; ++j) {
         if (j >= nr) break;
         const int64_t s = s0 + j * 32 + lane;
-        const int key = key_r[j];
+        int key, loc;
+        if constexpr (kPacked) {
+            key = static_cast<int>(kl_r[j] & 0x1fffu) - 1;
+            loc = static_cast<int>(kl_r[j] >> 13);
+        } else {
+            key = key_r[j];
+            loc = loc_r[j];
+        }
         int row = -1;
         if (key >= 0) {
-            const int local = cta_base[key] + mine[key] + loc_r[j];   // rank inside the expert
+            const int local = cta_base[key] + mine[key] + loc;   // rank inside the expert
             row = (p.stride > 0 && local >= p.stride) ? -1 : offs[key] + local;
         }
         if (s < s1) a.row_of_slot[s] = row;
@@ -748,10 +767,12 @@ cudaError_t set_kernel_attributes(DeviceLaunchState& st) {
     cudaError_t err = cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
     if (err == cudaSuccess)
         err = cudaFuncSetAttribute(layout_assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
-    if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(layout_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
-    if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(layout_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    for (auto kernel : {layout_cluster_kernel<kSmallRounds>, layout_cluster_kernel<kMaxRounds>}) {
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    }
     if (err == cudaSuccess) st.attrs_set = true;
     return err;
 }
@@ -776,7 +797,7 @@ int cluster_ctas_for(DeviceLaunchState& st, int warps, size_t smem) {
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, layout_cluster_kernel, &cfg) == cudaSuccess && n > 0) {
+        if (cudaOccupancyMaxActiveClusters(&n, layout_cluster_kernel<kMaxRounds>, &cfg) == cudaSuccess && n > 0) {
             found = c;
             break;
         }
@@ -832,7 +853,10 @@ cudaError_t launch_layout(const LayoutPlan& plan, const LayoutArgs& a, cudaStrea
             cfg.attrs = attr;
             cfg.numAttrs = 2;
             if (kernels) *kernels = 1;
-            return cudaLaunchKernelEx(&cfg, layout_cluster_kernel, p, a);
+            // the unpacked instance while each warp needs at most kSmallRounds rounds
+            if (static_cast<int64_t>(ct) * plan.K <= kSmallRounds * 32)
+                return cudaLaunchKernelEx(&cfg, layout_cluster_kernel<kSmallRounds>, p, a);
+            return cudaLaunchKernelEx(&cfg, layout_cluster_kernel<kMaxRounds>, p, a);
         }
     }
 

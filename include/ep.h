@@ -174,7 +174,7 @@ typedef int (*ep_free_fn)(void* ptr);
  *                         that reads the handle must be on `stream` or
  *                         finished.
  * Writes every element of the four outputs; needs no zeroed memory.
- * One kernel (a single thread-block cluster) for routings up to 2^17 slots
+ * One kernel (a single thread-block cluster) for routings up to 2^18 slots
  * whose plan fits its shared memory, else three (count, scan, assign);
  * ep_handle_layout_kernels says which. No host synchronisation except on
  * creation or growth.

@@ -223,8 +223,11 @@ def _workload(T, H, E, K, R, **kw):
     _workload(200, 136, 4096, 8, 1024),                  # maximum E and R
     _workload(300, 128, 512, 8, 64),                     # R > 32 on the single-cluster path
     _workload(500, 128, 256, 8, 32, drop_p=0.1),         # R = 32: every rank bit in use
-    _workload(21504, 64, 64, 6, 4, routing="zipf"),      # K = 6: largest single-cluster chunk
-    _workload(21505, 64, 64, 6, 4, routing="zipf"),      # one token more: multi-block path
+    _workload(21504, 64, 64, 6, 4, routing="zipf"),      # K = 6: largest routing of the 8-round cluster kernel
+    _workload(21505, 64, 64, 6, 4, routing="zipf"),      # one token more: its packed 16-round instance
+    _workload(43520, 64, 64, 6, 4, routing="zipf"),      # K = 6: largest single-cluster routing (512 slots a warp)
+    _workload(43521, 64, 64, 6, 4, routing="zipf"),      # one token more: multi-block path
+    _workload(32768, 64, 256, 8, 8, drop_p=0.02),        # 2^18 slots on the single cluster
     _workload(8000, 128, 4096, 8, 1024, drop_p=0.02),    # maximum E and R, 64k slots (multi-block)
     _workload(9000, 128, 2048, 32, 256, drop_p=0.02),    # maximum top-k above 2^18 slots
 ])
