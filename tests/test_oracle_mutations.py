@@ -91,6 +91,20 @@ MUTATIONS = [
     ("dropped slot gets weight gradient 1",
      "grad_topk_weights[s] = row >= 0 ? grad_recv_weights[row] : 0.0f;",
      "grad_topk_weights[s] = row >= 0 ? grad_recv_weights[row] : 1.0f;", 0),
+    ("e4m3 dispatch scales at the token's row",
+     "memcpy(recv_scales + (int64_t)row * nb, s, (size_t)nb * sizeof(float));",
+     "memcpy(recv_scales + t * nb, s, (size_t)nb * sizeof(float));", 0),
+    ("e4m3 dispatch codes at the token's row", "memcpy(recv_q + (int64_t)row * H, q, (size_t)H);",
+     "memcpy(recv_q + t * H, q, (size_t)H);", 0),
+    ("e4m3 dispatch weight of the next slot",
+     "if (recv_weights && topk_weights) recv_weights[row] = topk_weights[t * K + k];",
+     "if (recv_weights && topk_weights) recv_weights[row] = topk_weights[t * K + (k + 1) % K];", 1),
+    ("bf16 dispatch weight of the next slot",
+     "if (recv_weights && topk_weights) recv_weights[row] = topk_weights[t * K + k];",
+     "if (recv_weights && topk_weights) recv_weights[row] = topk_weights[t * K + (k + 1) % K];", 0),
+    ("non-expand weight of the row's slot for every entry", "on && w ? w[t * K + j] : 0.0f;",
+     "on && w ? w[t * K + k] : 0.0f;", 0),
+    ("non-expand weight kept on an off-rank slot", "on && w ? w[t * K + j] : 0.0f;", "w ? w[t * K + j] : 0.0f;", 0),
 ]
 
 

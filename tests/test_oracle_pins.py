@@ -179,6 +179,28 @@ def test_e4m3_encoder_vs_brute_search():
     np.testing.assert_array_equal(oracle.f32_to_e4m3(f), brute.e4m3_encode(f))
 
 
+_SWEEP_RANGES = [
+    (0x00000000, 1 << 18),                 # +0 and fp32 subnormals
+    (0x3A800000 - (1 << 17), 0x3A800000 + (1 << 17)),   # around 2^-10 (fp8 subnormals)
+    (0x3F800000 - (1 << 18), 0x3F800000 + (1 << 18)),   # around 1.0
+    (0x43E00000 - (1 << 19), 0x43E00000 + (1 << 19)),   # around 448 (e4m3 saturation)
+    (0x47600000 - (1 << 19), 0x47600000 + (1 << 19)),   # around 57344 (e5m2 saturation)
+    (0xBF800000 - (1 << 18), 0xBF800000 + (1 << 18)),   # around -1.0
+    (0x7F7FFFFF - (1 << 16), 0x7F800000),               # the largest finite values
+]
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fp8_sweep_encodes_each_bit_pattern(fmt):
+    """The range encoders the GPU conversion sweep compares against give, for
+    each fp32 bit pattern in [lo, hi), torch's saturating cast of that value."""
+    sweep = oracle.e4m3_sweep if fmt == "e4m3" else oracle.e5m2_sweep
+    for lo, hi in _SWEEP_RANGES:
+        f = np.arange(lo, hi, dtype=np.uint64).astype(np.uint32).view(np.float32)
+        want = _torch_e4m3_bits(f) if fmt == "e4m3" else _torch_e5m2_bits(f)
+        np.testing.assert_array_equal(sweep(lo, hi), want, err_msg=f"{fmt} [{lo:#x}, {hi:#x})")
+
+
 def test_e4m3_decode_roundtrip():
     codes, vals = brute.e4m3_values()
     dec = oracle.e4m3_to_f32(codes)
@@ -341,6 +363,53 @@ def test_dispatch_e5m2_rows_are_their_tokens_quantised(mode):
         seen[r] = True
     assert seen[:n].all() and not seen[n:].any()
     assert not q[n:].any() and not s[n:].any()
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_dispatch_e4m3_rows_are_their_tokens_quantised(seed):
+    """The e4m3 quantise-permute (nccl_ep.cc, ncclEpDispatch, low-latency
+    branch: fp32 scales one per 128 channels, [rows, hidden/128]; DeepEP API
+    docs, dispatch(): recv_topk_weights) places, for every used slot (t, k),
+    token t's codes and scale row at receive row row_of_slot[t, k], writes
+    source t and weight w[t, k] there, and leaves every other row untouched.
+    The routing has dropped slots, an all-dropped token and repeated experts,
+    and each token's weights are distinct, so a weight taken from another
+    slot shows; codes and scales are checked against the quantiser, which the
+    fixtures and closed forms above pin."""
+    rng = np.random.default_rng(40 + seed)
+    T, K, E, R, H = 37, 3, 8, 2, 256
+    idx = _random_routing(rng, T, K, E, drop_p=0.25, distinct=False)
+    idx[5] = -1
+    x = gi.f32_to_bf16_bits((rng.standard_normal((T, H)) * 3).astype(np.float32))
+    x[7, :128] = 0                         # one all-zero block: scale 0, zero codes
+    w = (rng.permutation(T * K).reshape(T, K) + 1).astype(np.float32) / 128.0
+    L = oracle.layout(idx, E, R)
+    n = int(L["expert_offsets"][-1])
+    spare = 4
+    q, s, src, rw = oracle.dispatch_e4m3(x, L["row_of_slot"], n + spare, w)
+    seen = np.zeros(n + spare, bool)
+    for t in range(T):
+        qt, st = oracle.quant_row_e4m3(x[t])
+        for k in range(K):
+            r = L["row_of_slot"][t, k]
+            if r < 0:
+                continue
+            np.testing.assert_array_equal(q[r], qt)
+            np.testing.assert_array_equal(s[r].view(np.uint32), st.view(np.uint32))
+            assert src[r] == t and rw[r] == w[t, k], (t, k, r)
+            assert not seen[r]
+            seen[r] = True
+    assert seen[:n].all() and not seen[n:].any()
+    # the rows no slot names keep what the caller put there
+    assert not q[n:].any() and np.isnan(s[n:]).all() and (src[n:] == -1).all() and np.isnan(rw[n:]).all()
+    # the all-zero block: scale 0 and zero codes in each of token 7's rows
+    for r in L["row_of_slot"][7][L["row_of_slot"][7] >= 0]:
+        assert s[r, 0] == 0.0 and not q[r, :128].any()
+    # without weights the optional weight output is not written
+    q2, s2, src2, rw2 = oracle.dispatch_e4m3(x, L["row_of_slot"], n)
+    assert rw2 is None
+    np.testing.assert_array_equal(q2, q[:n])
+    np.testing.assert_array_equal(src2, src[:n])
 
 
 # ------------------------------------------------------------------ alignment
@@ -589,6 +658,28 @@ def test_fp8_pow2_closed_forms():
             np.testing.assert_array_equal(qu[b*128:(b+1)*128], want_u)
 
 
+@pytest.mark.parametrize("ue8m0", [False, True])
+def test_dispatch_e4m3_pow2_rows_are_their_tokens_quantised(ue8m0):
+    """Each used slot's row holds its token's power-of-two-scale codes and
+    scales (checked against the quantiser pinned above); unused rows stay zero."""
+    rng = np.random.default_rng(6)
+    T, K, E, R, H = 29, 3, 8, 4, 256
+    idx = _random_routing(rng, T, K, E, drop_p=0.2, distinct=False)
+    x = gi.f32_to_bf16_bits((rng.standard_normal((T, H)) * 5).astype(np.float32))
+    L = oracle.layout(idx, E, R)
+    n = int(L["expert_offsets"][-1])
+    q, s = oracle.dispatch_e4m3_pow2(x, L["row_of_slot"], n + 2, ue8m0)
+    seen = np.zeros(n + 2, bool)
+    for t, k in zip(*np.nonzero(L["row_of_slot"] >= 0)):
+        r = L["row_of_slot"][t, k]
+        qt, st = oracle.quant_row_e4m3_pow2(x[t], ue8m0)
+        np.testing.assert_array_equal(q[r], qt)
+        np.testing.assert_array_equal(s[r], st)
+        seen[r] = True
+    assert seen[:n].all() and not seen[n:].any()
+    assert not q[n:].any() and not s[n:].any()
+
+
 # ------------------------------------------------------------------ e5m2
 
 def _torch_e5m2_bits(f32):
@@ -831,8 +922,13 @@ def test_layout_nonexpand_golden(golden):
     np.testing.assert_array_equal(L["rank_offsets"], _ints(g["rank_offsets"]))
     np.testing.assert_array_equal(L["row_of_slot"].ravel(), _ints(g["row_of_slot"]))
     n = int(L["rank_offsets"][-1])
-    ri, _ = oracle.nonexpand_recv_topk(idx, None, L["row_of_slot"], E, R, n)
+    ri, rw0 = oracle.nonexpand_recv_topk(idx, None, L["row_of_slot"], E, R, n)
     np.testing.assert_array_equal(ri.ravel(), _ints(g["recv_topk_idx"]))
+    assert (rw0 == 0).all()                 # no weights given: every entry 0
+    w = np.array([float(v) for v in g["topk_weights"]], np.float32).reshape(T, K)
+    ri2, rw = oracle.nonexpand_recv_topk(idx, w, L["row_of_slot"], E, R, n)
+    np.testing.assert_array_equal(ri2, ri)
+    np.testing.assert_array_equal(rw.ravel(), np.array([float(v) for v in g["recv_topk_weights"]], np.float32))
 
 
 @pytest.mark.parametrize("case", CORNERS)
