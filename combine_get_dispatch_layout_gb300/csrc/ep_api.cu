@@ -20,7 +20,9 @@ struct ep_handle {
     ep_alloc_fn alloc_fn = nullptr;
     ep_free_fn free_fn = nullptr;
     // routing of the last ep_layout
-    int T = 0, K = 0, E = 0, R = 0;
+    int T = 0, K = 0, E = 0, R = 0;   // E: the layout's key space (R for a non-expand layout)
+    int routing_E = 0;          // the experts of the routing the last layout was given
+    bool nonexpand = false;     // the last layout was ep_layout_nonexpand
     int align = 1;              // expert row alignment of the last layout
     int stride = 0;             // > 0: fixed rows per expert (strided layout)
     ep::LayoutPlan plan{};
@@ -236,10 +238,13 @@ ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int
             delete h;
         } else {
             h->T = 0;   // the old block is gone: later calls on this handle move nothing
+            h->nonexpand = false;
         }
         return st;
     }
     h->T = T; h->K = K; h->E = KE; h->R = R;
+    h->routing_E = E;
+    h->nonexpand = nonexpand;
     h->align = align;
     h->stride = stride;
     h->plan = plan;
@@ -366,6 +371,9 @@ ep_status_t ep_nonexpand_recv_topk(ep_handle_t handle, const int64_t* topk_idx, 
     ApiRange range("ep_nonexpand_recv_topk");
     if (!handle) return EP_ERR_INVALID_ARG;
     const int T = handle->T, K = handle->K, R = handle->R;
+    // the rank-local ids come from E / R: only the E the layout itself was
+    // given, on a non-expand layout's handle, gives the rows' true ids
+    if (!handle->nonexpand || E != handle->routing_E) return EP_ERR_INVALID_ARG;
     if (E < 1 || E > EP_MAX_EXPERTS || E % R != 0 || recv_capacity < 0) return EP_ERR_INVALID_ARG;
     if (T > 0 && !topk_idx) return EP_ERR_INVALID_ARG;
     if (recv_capacity > 0 && !recv_topk_idx) return EP_ERR_INVALID_ARG;

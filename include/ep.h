@@ -263,7 +263,9 @@ EP_API ep_status_t ep_layout_nonexpand(const int64_t* topk_idx, int T, int K, in
  * the weight is topk_weights[t, k] there, else 0. topk_idx / topk_weights are
  * the ones given to ep_layout_nonexpand (weights may be NULL);
  * recv_topk_idx int64 [cap, K], recv_topk_weights fp32 [cap, K] or NULL.
- * Rows >= N are not written.
+ * Rows >= N are not written. Returns EP_ERR_INVALID_ARG, enqueuing nothing,
+ * when the handle's last layout was not ep_layout_nonexpand or when E differs
+ * from the E that layout was given (the rank-local ids depend on it).
  */
 EP_API ep_status_t ep_nonexpand_recv_topk(ep_handle_t handle, const int64_t* topk_idx, const float* topk_weights,
                                           int E, int64_t* recv_topk_idx, float* recv_topk_weights,
@@ -455,11 +457,14 @@ EP_API int ep_handle_layout_kernels(ep_handle_t handle);
  *
  * Instead of a handle it uses one fixed scratch array compiled into the
  * library, EP_NOALLOC_SCRATCH_BYTES (2 MiB) of device memory that every GPU
- * which loads the library keeps until the process exits. The scratch holds
- * E * C + R * B + 64 int32 words, where C <= 256 is the number of token
- * chunks and B the number of count blocks (B = C/8 when E <= 2730), so
- * roughly (E + R) * 256 words; routings that need more are rejected with
- * EP_ERR_CAPACITY before anything is enqueued.
+ * which loads the library keeps until the process exits. The limit is that
+ * of the three-kernel layout path, whose tables live there: E * C + R * B +
+ * 64 int32 words, where C <= 256 is the number of token chunks and B the
+ * number of count blocks (B = C/8 when E <= 2730), so roughly (E + R) * 256
+ * words. The single-cluster path uses only the 64 state words, but which
+ * path runs is decided at launch from what the GPU can co-schedule, so the
+ * check is applied to every routing: one that would need more is rejected
+ * with EP_ERR_CAPACITY before anything is enqueued.
  *
  * Arguments and outputs are those of ep_layout, plus:
  *  row_of_slot    device, int32 [T, K]: receive row of each slot, -1 if
@@ -467,7 +472,12 @@ EP_API int ep_handle_layout_kernels(ep_handle_t handle);
  *                 handle); the caller owns it.
  *  device_error   device, int32 [1] or NULL: set to 0, or to
  *                 EP_ERR_INVALID_EXPERT if an id outside [-1, E) was seen
- *                 (those slots are treated as unused).
+ *                 (those slots are treated as unused). It is filled by a
+ *                 4-byte device-to-device copy enqueued after the layout
+ *                 kernels, so a kernel launched next on the stream as a
+ *                 programmatic dependent starts after that copy rather than
+ *                 overlapping the layout's last wave; pass NULL when that
+ *                 overlap matters more than the error word.
  *
  * Calls share the one scratch array, which keeps the last call's contents;
  * each call clears the words that must start at zero. Calls whose work

@@ -1287,6 +1287,41 @@ def test_nonexpand_workloads(ep, name, T):
     nonexpand_path(ep, gi.make(name, 15, T=T, with_y=False))
 
 
+def test_nonexpand_recv_topk_refuses_other_handles_and_experts(ep):
+    """The rank-local ids depend on E / R, so ep_nonexpand_recv_topk takes only
+    a non-expand layout's handle and the E that layout was given; anything
+    else is refused before a launch and leaves the outputs untouched."""
+    rng = np.random.default_rng(12)
+    T, K, E, R = 50, 4, 16, 4
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :K].astype(np.int64)
+    o = [torch.empty(E, dtype=torch.int32, device="cuda"), torch.empty(R, dtype=torch.int32, device="cuda"),
+         torch.empty((T, R), dtype=torch.uint8, device="cuda"), torch.empty(E + 1, dtype=torch.int32, device="cuda")]
+    ri = torch.full((T * K, K), -9, dtype=torch.int64, device="cuda")
+    h = ep.ep_layout(_dev(idx), E, R, *o)                 # an expand layout
+    with pytest.raises(ep.EPError) as e:
+        ep.ep_nonexpand_recv_topk(h, _dev(idx), E, ri, recv_capacity=T * K)
+    assert e.value.status == ep.EP_ERR_INVALID_ARG
+    ep.ep_layout_nonexpand(_dev(idx), E, R, o[0], o[1], o[2], o[3][:R + 1], handle=h)
+    for bad_E in (2 * E, E // 2, R):                      # all divisible by R: only the layout's E is right
+        with pytest.raises(ep.EPError) as e:
+            ep.ep_nonexpand_recv_topk(h, _dev(idx), bad_E, ri, recv_capacity=T * K)
+        assert e.value.status == ep.EP_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert (ri.cpu().numpy() == -9).all()
+    ep.ep_nonexpand_recv_topk(h, _dev(idx), E, ri, recv_capacity=T * K)
+    ref = oracle.layout_nonexpand(idx, E, R)
+    n = int(ref["rank_offsets"][-1])
+    r_ri, _ = oracle.nonexpand_recv_topk(idx, None, ref["row_of_slot"], E, R, n)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(ri.cpu().numpy()[:n], r_ri)
+    # a later expand layout on the same handle is refused again
+    ep.ep_layout(_dev(idx), E, R, *o, handle=h)
+    with pytest.raises(ep.EPError) as e:
+        ep.ep_nonexpand_recv_topk(h, _dev(idx), E, ri, recv_capacity=T * K)
+    assert e.value.status == ep.EP_ERR_INVALID_ARG
+    h.destroy()
+
+
 @pytest.mark.parametrize("w", [
     _workload(300, 128, 512, 8, 64),                                  # R > 32
     _workload(40000, 64, 64, 8, 4, routing="zipf", drop_p=0.05),      # multi-block layout path
