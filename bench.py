@@ -189,6 +189,87 @@ def aggregate_over_ranks(local_ms: float, local_bytes: int, device=None):
     return float(t.item()), int(b.item())
 
 
+# ---------------------------------------------------------------- device timing
+
+class L2Flush:
+    """Empties L2 of the workload: writes one buffer twice the L2 size, then
+    reads another of that size, so L2 is left holding clean lines of the
+    second (no dirty line is left for the next kernel to write back). Call it
+    with `stream` current; it is never inside a timed interval."""
+
+    def __init__(self, torch, dev, stream):
+        l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or L2_BYTES
+        with torch.cuda.stream(stream):
+            self.w = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+            self.r = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
+            self.acc = torch.empty((), dtype=torch.float32, device=dev)
+        self.torch = torch
+        self.mib = 2 * l2 >> 20
+
+    def __call__(self):
+        self.w.fill_(1.0)
+        self.torch.sum(self.r, dim=0, out=self.acc)
+
+
+def graph_us(torch, stream, body, n=20, replays=10):
+    """Device time (us) of one body() from a CUDA graph of n copies of it,
+    replayed between two events: no host launch cost, and the library's
+    kernels keep their programmatic edges inside the graph (so one copy's
+    first kernel may start while the previous copy's last one drains)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        body()
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(n):
+                body()
+        for _ in range(3):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(replays):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    del g
+    return e0.elapsed_time(e1) / (n * replays) * 1e3
+
+
+def graph_prefix_us(torch, stream, bodies, n=20, rounds=30):
+    """Device time (us) per copy of each body in `bodies`, each captured n
+    times into its own CUDA graph. The graphs are replayed round-robin
+    `rounds` times with events around every replay, and the median replay
+    time is taken, so slow drift of the clock or the memory system affects
+    all bodies alike. Bodies that extend one another (flush; flush + layout;
+    flush + layout + dispatch; ...) give each kernel's marginal cost inside
+    the step as the difference of neighbours."""
+    graphs = []
+    with torch.cuda.stream(stream):
+        for body in bodies:
+            body()
+        stream.synchronize()
+        for body in bodies:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(n):
+                    body()
+            g.replay()
+            graphs.append(g)
+        stream.synchronize()
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in graphs]
+              for _ in range(rounds)]
+        for r in range(rounds):
+            for j, g in enumerate(graphs):
+                ev[r][j][0].record(stream)
+                g.replay()
+                ev[r][j][1].record(stream)
+    stream.synchronize()
+    out = [float(np.median([ev[r][j][0].elapsed_time(ev[r][j][1]) for r in range(rounds)])) * 1e3 / n
+           for j in range(len(graphs))]
+    del graphs
+    return out
+
+
 # ---------------------------------------------------------------- GPU arm
 
 def gpu_arm(args, rank, world, local):
@@ -397,27 +478,10 @@ def gpu_arm(args, rank, world, local):
         w_back = torch.empty(T, K, dtype=torch.float32, device=dev)
     # each conversion captured 20 times into a CUDA graph and replayed, so the
     # GPU time is not hidden behind the host cost of launching a ~5 us kernel
-    def graph_us(fn, n=20, replays=10):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            fn()
-            stream.synchronize()
-            with torch.cuda.graph(g, stream=stream):
-                for _ in range(n):
-                    fn()
-            g.replay()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(replays):
-                g.replay()
-            e1.record(stream)
-        stream.synchronize()
-        del g
-        return e0.elapsed_time(e1) / (n * replays)
-
-    ms_t2m = graph_us(lambda: ep.ep_topk_to_routing_map(idx, E, rmap, topk_weights=wt, probs=probs, stream=stream))
-    ms_m2t = graph_us(lambda: ep.ep_routing_map_to_topk(rmap, K, idx_back, probs=probs, topk_weights=w_back,
-                                                        stream=stream))
+    ms_t2m = graph_us(torch, stream, lambda: ep.ep_topk_to_routing_map(idx, E, rmap, topk_weights=wt, probs=probs,
+                                                                       stream=stream)) / 1e3
+    ms_m2t = graph_us(torch, stream, lambda: ep.ep_routing_map_to_topk(rmap, K, idx_back, probs=probs,
+                                                                       topk_weights=w_back, stream=stream)) / 1e3
     b_t2m = 12 * T * K + 5 * T * E
     b_m2t = 5 * T * E + 12 * T * K
     del rmap, probs, idx_back, w_back
@@ -469,41 +533,6 @@ def gpu_arm(args, rank, world, local):
     b_ne = 2 * T * H + 2 * n_ne * H + 4 * T * K
     h_ne.destroy()
     del recv_ne
-
-    # decode shape through the low-latency padded 3-D layout [E, cap, H]
-    # (cap = T: every token could pick one expert); ~33 MB, L2-resident
-    dec = gi.make("decode", seed=args.seed + rank)
-    wd = dec.w
-    cap = wd.T
-    with torch.cuda.stream(stream):
-        d_idx = torch.from_numpy(dec.topk_idx).to(dev)
-        d_x = torch.from_numpy(dec.x.view(np.int16)).to(dev)
-        d_w = torch.from_numpy(dec.topk_weights).to(dev)
-        d_y = torch.randn(wd.E * cap, wd.H, device=dev).to(torch.bfloat16).view(torch.int16)
-        d_recv = torch.empty(wd.E * cap, wd.H, dtype=torch.int16, device=dev)
-        d_out = torch.empty(wd.T, wd.H, dtype=torch.int16, device=dev)
-        d_cnt = torch.empty(wd.E, dtype=torch.int32, device=dev)
-        d_ntr = torch.empty(wd.R, dtype=torch.int32, device=dev)
-        d_itr = torch.empty(wd.T, wd.R, dtype=torch.uint8, device=dev)
-        d_off = torch.empty(wd.E + 1, dtype=torch.int32, device=dev)
-    h_d = ep.ep_layout_strided(d_idx, wd.E, wd.R, cap, d_cnt, d_ntr, d_itr, d_off, stream=stream)
-    ev_d = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps_b)]
-    for i in range(-3, reps_b):
-        if i >= 0:
-            ev_d[i][0].record(stream)
-        ep.ep_layout_strided(d_idx, wd.E, wd.R, cap, d_cnt, d_ntr, d_itr, d_off, handle=h_d, stream=stream)
-        if i >= 0:
-            ev_d[i][1].record(stream)
-        ep.ep_dispatch(h_d, d_x, ep.EP_DTYPE_BF16, d_recv, wd.E * cap, stream=stream)
-        if i >= 0:
-            ev_d[i][2].record(stream)
-        ep.ep_combine(h_d, d_y, d_out, topk_weights=d_w, stream=stream)
-        if i >= 0:
-            ev_d[i][3].record(stream)
-    stream.synchronize()
-    ms_d = [float(np.mean([e[j].elapsed_time(e[j + 1]) for e in ev_d])) for j in range(3)]
-    h_d.destroy()
-    del d_y, d_recv
 
     others = other_configs(torch, ep, dev, stream, args, rank, peak, reps_b)
 
@@ -592,11 +621,6 @@ def gpu_arm(args, rank, world, local):
                                         "us": round(ms_ne[1] * 1e3, 2), "bytes": b_ne,
                                         "gbs": round(b_ne / (ms_ne[1] * 1e-3) / 1e9, 1),
                                         "frac_of_measured": round(b_ne / (ms_ne[1] * 1e-3) / 1e9 / peak, 4)},
-            "decode_ll_step": {"workload": "decode T=256 H=7168 E=256 K=8 R=8, strided layout cap=256, "
-                                           "L2-resident (33 MB), warm",
-                               "layout_strided_us": round(ms_d[0] * 1e3, 2),
-                               "dispatch_us": round(ms_d[1] * 1e3, 2), "combine_us": round(ms_d[2] * 1e3, 2),
-                               "tokens_per_s": round(wd.T / (sum(ms_d) * 1e-3), 1)},
             **others,
             "combine_backward": {"us": round(ms_cbw * 1e3, 2), "bytes": b_cbw,
                                  "gbs": round(b_cbw / (ms_cbw * 1e-3) / 1e9, 1),
@@ -634,16 +658,14 @@ def gpu_arm(args, rank, world, local):
 
 
 def other_configs(torch, ep, dev, stream, args, rank, peak, reps):
-    """The skewed workload's step (T=16384, H=4096, E=64, top-6 with drops)
-    and the decode step with L2 flushed before every iteration."""
+    """The skewed workload's step (T=16384, H=4096, E=64, top-6 with drops),
+    and the decode (T=256, H=7168, E=256, top-8) and tiny (T=128, H=256, E=8,
+    top-2) steps with device times L2-cold and warm."""
     out = {}
 
-    def split_loop(calls, flush=None):
+    def split_loop(calls):
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(reps)]
         for i in range(-3, reps):
-            if flush is not None:
-                with torch.cuda.stream(stream):
-                    flush.fill_(i)
             for j, call in enumerate(calls):
                 if i >= 0:
                     ev[i][j].record(stream)
@@ -695,87 +717,115 @@ def other_configs(torch, ep, dev, stream, args, rank, peak, reps):
         "tokens_per_s": round(ws.T / (sum(ms) * 1e-3), 1)}
     del t, y
 
-    # decode through the strided layout [E, cap, H], L2 flushed first: a
-    # buffer twice the L2 size is written before every iteration (untimed)
+    flush = L2Flush(torch, dev, stream)
+
+    # decode as configured (T=256, H=7168, E=256, top-8): expand layout,
+    # dispatch, combine of y [T*K, H] in dispatch order
     dec = gi.make("decode", seed=args.seed + rank)
-    wd, cap = dec.w, dec.w.T
+    wd, Nd = dec.w, dec.num_valid
+    t = tensors(dec, Nd)
+    with torch.cuda.stream(stream):
+        y = torch.from_numpy(dec.y.view(np.int16)).to(dev)
+    h = ep.ep_layout(t["idx"], wd.E, wd.R, t["cnt"], t["ntr"], t["itr"], t["off"], stream=stream)
+    out["decode_step"] = small_step_report(
+        torch, stream, flush, peak, wd, Nd,
+        f"decode T={wd.T} H={wd.H} E={wd.E} K={wd.K} R={wd.R}: ep_layout (expand) + ep_dispatch(bf16) + "
+        f"ep_combine, y [T*K, H] in dispatch order, N={Nd}",
+        lambda: ep.ep_layout(t["idx"], wd.E, wd.R, t["cnt"], t["ntr"], t["itr"], t["off"], handle=h, stream=stream),
+        lambda: ep.ep_dispatch(h, t["x"], ep.EP_DTYPE_BF16, t["recv"], Nd, stream=stream),
+        lambda: ep.ep_dispatch_ex(h, t["x"], t["recv"], Nd, out_dtype=ep.EP_DTYPE_BF16, overlap_layout=True,
+                                  stream=stream),
+        lambda: ep.ep_combine(h, y, t["out"], topk_weights=t["w"], stream=stream))
+    h.destroy()
+    del t, y
+
+    # the same decode routing through the padded 3-D low-latency layout
+    # [E, cap, H], cap = T (every token could pick one expert)
+    cap = wd.T
     t = tensors(dec, wd.E * cap)
-    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or (128 << 20)
     with torch.cuda.stream(stream):
         y = torch.randn(wd.E * cap, wd.H, device=dev).to(torch.bfloat16).view(torch.int16)
-        flush = torch.empty(2 * l2 // 4, dtype=torch.int32, device=dev)
     h = ep.ep_layout_strided(t["idx"], wd.E, wd.R, cap, t["cnt"], t["ntr"], t["itr"], t["off"], stream=stream)
-    ms = split_loop([
-        lambda: ep.ep_layout_strided(t["idx"], wd.E, wd.R, cap, t["cnt"], t["ntr"], t["itr"], t["off"],
-                                     handle=h, stream=stream),
+    out["decode_ll_step"] = small_step_report(
+        torch, stream, flush, peak, wd, Nd,
+        f"decode T={wd.T} H={wd.H} E={wd.E} K={wd.K} R={wd.R}: ep_layout_strided (cap={cap}) + ep_dispatch(bf16) "
+        "+ ep_combine",
+        lambda: ep.ep_layout_strided(t["idx"], wd.E, wd.R, cap, t["cnt"], t["ntr"], t["itr"], t["off"], handle=h,
+                                     stream=stream),
         lambda: ep.ep_dispatch(h, t["x"], ep.EP_DTYPE_BF16, t["recv"], wd.E * cap, stream=stream),
-        lambda: ep.ep_combine(h, y, t["out"], topk_weights=t["w"], stream=stream)], flush=flush)
+        lambda: ep.ep_dispatch_ex(h, t["x"], t["recv"], wd.E * cap, out_dtype=ep.EP_DTYPE_BF16, overlap_layout=True,
+                                  stream=stream),
+        lambda: ep.ep_combine(h, y, t["out"], topk_weights=t["w"], stream=stream))
     h.destroy()
-    # the same step captured once into a CUDA graph (kernels chained by
-    # programmatic edges) and replayed: no host launch cost per step, warm L2
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        h = ep.ep_layout_strided(t["idx"], wd.E, wd.R, cap, t["cnt"], t["ntr"], t["itr"], t["off"], stream=stream)
-        stream.synchronize()
-        with torch.cuda.graph(g, stream=stream):
-            ep.ep_layout_strided(t["idx"], wd.E, wd.R, cap, t["cnt"], t["ntr"], t["itr"], t["off"], handle=h,
-                                 stream=stream)
-            ep.ep_dispatch_ex(h, t["x"], t["recv"], wd.E * cap, out_dtype=ep.EP_DTYPE_BF16, overlap_layout=True,
-                              stream=stream)
-            ep.ep_combine(h, y, t["out"], topk_weights=t["w"], stream=stream)
-        for _ in range(5):
-            g.replay()
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        for _ in range(reps):
-            g.replay()
-        ev1.record(stream)
-    stream.synchronize()
-    ms_g = ev0.elapsed_time(ev1) / reps
-    del g
-    h.destroy()
-    out["decode_ll_step_graph"] = {
-        "workload": f"decode T={wd.T} H={wd.H} E={wd.E} K={wd.K} R={wd.R}, strided layout cap={cap}, "
-                    "one CUDA graph per step (layout, overlapped dispatch, combine), warm L2",
-        "step_us": round(ms_g * 1e3, 2), "tokens_per_s": round(wd.T / (ms_g * 1e-3), 1)}
-    out["decode_ll_step_l2_flushed"] = {
-        "workload": f"decode T={wd.T} H={wd.H} E={wd.E} K={wd.K} R={wd.R}, strided layout cap={cap}, "
-                    f"L2 flushed ({2 * l2 >> 20} MiB written) before each iteration",
-        "layout_strided_us": round(ms[0] * 1e3, 2), "dispatch_us": round(ms[1] * 1e3, 2),
-        "combine_us": round(ms[2] * 1e3, 2), "tokens_per_s": round(wd.T / (sum(ms) * 1e-3), 1)}
-    del t, y, flush
-
-    # the tiny workload's step (T=128, H=256, E=8, top-2), one CUDA graph per
-    # step: pure latency
-    tn = gi.make("tiny", seed=args.seed + rank)
-    wt_ = tn.w
-    t = tensors(tn, wt_.T * wt_.K)
-    with torch.cuda.stream(stream):
-        y = torch.from_numpy(tn.x.view(np.int16)).to(dev).repeat_interleave(wt_.K, dim=0)
-        h = ep.ep_layout(t["idx"], wt_.E, wt_.R, t["cnt"], t["ntr"], t["itr"], t["off"], stream=stream)
-        stream.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            ep.ep_layout(t["idx"], wt_.E, wt_.R, t["cnt"], t["ntr"], t["itr"], t["off"], handle=h, stream=stream)
-            ep.ep_dispatch_ex(h, t["x"], t["recv"], wt_.T * wt_.K, out_dtype=ep.EP_DTYPE_BF16, overlap_layout=True,
-                              stream=stream)
-            ep.ep_combine(h, y, t["out"], topk_weights=t["w"], stream=stream)
-        for _ in range(5):
-            g.replay()
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        for _ in range(reps):
-            g.replay()
-        ev1.record(stream)
-    stream.synchronize()
-    ms_t = ev0.elapsed_time(ev1) / reps
-    del g
-    h.destroy()
-    out["tiny_step_graph"] = {
-        "workload": f"tiny T={wt_.T} H={wt_.H} E={wt_.E} K={wt_.K} R={wt_.R}, one CUDA graph per step, warm",
-        "step_us": round(ms_t * 1e3, 2), "tokens_per_s": round(wt_.T / (ms_t * 1e-3), 1)}
     del t, y
+
+    # the tiny workload (T=128, H=256, E=8, top-2): the identity expert, so the
+    # combine reads the dispatched rows
+    tn = gi.make("tiny", seed=args.seed + rank)
+    wt_, Nt = tn.w, tn.num_valid
+    t = tensors(tn, Nt)
+    h = ep.ep_layout(t["idx"], wt_.E, wt_.R, t["cnt"], t["ntr"], t["itr"], t["off"], stream=stream)
+    out["tiny_step"] = small_step_report(
+        torch, stream, flush, peak, wt_, Nt,
+        f"tiny T={wt_.T} H={wt_.H} E={wt_.E} K={wt_.K} R={wt_.R}: ep_layout + ep_dispatch(bf16) + ep_combine of the "
+        "dispatched rows (identity expert)",
+        lambda: ep.ep_layout(t["idx"], wt_.E, wt_.R, t["cnt"], t["ntr"], t["itr"], t["off"], handle=h,
+                             stream=stream),
+        lambda: ep.ep_dispatch(h, t["x"], ep.EP_DTYPE_BF16, t["recv"], Nt, stream=stream),
+        lambda: ep.ep_dispatch_ex(h, t["x"], t["recv"], Nt, out_dtype=ep.EP_DTYPE_BF16, overlap_layout=True,
+                                  stream=stream),
+        lambda: ep.ep_combine(h, t["recv"], t["out"], topk_weights=t["w"], stream=stream))
+    h.destroy()
+    del t, flush
     return out
+
+
+def small_step_report(torch, stream, flush, peak, w, N, workload, lay, dis, dis_overlap, com):
+    """Device times of a small step (layout, dispatch as the layout's
+    programmatic dependent, combine) and of its kernels, from CUDA graphs of
+    20 copies replayed round-robin (graph_prefix_us):
+      cold: L2 emptied before every step (x, y and the routing come from
+            HBM); each kernel's time is its marginal cost inside the step,
+            the difference between the graphs of [flush, layout, ...] up to
+            and without it; the step's is [flush, step] minus [flush];
+      warm: the same without the flush (every byte already in L2), steps
+            chained back to back;
+      alone: 20 launches of that kernel alone, chained, warm.
+    GB/s counts the algorithmic bytes; the HBM fraction is of the measured
+    copy rate (a warm figure above 1 means L2 served the bytes)."""
+    T, K, H, E, R = w.T, w.K, w.H, w.E, w.R
+    nbytes = {"layout": bytes_layout(T, K, E, R), "dispatch": bytes_dispatch_bf16(T, K, H, N),
+              "combine": bytes_combine(T, K, H, N)}
+    nbytes["step"] = sum(nbytes.values())
+    f_, fl, fld, flc = graph_prefix_us(torch, stream, [
+        flush, lambda: (flush(), lay()), lambda: (flush(), lay(), dis_overlap()),
+        lambda: (flush(), lay(), dis_overlap(), com())])
+    wl, wld, wlc = graph_prefix_us(torch, stream, [lay, lambda: (lay(), dis_overlap()),
+                                                   lambda: (lay(), dis_overlap(), com())])
+    al, ad, ac = graph_prefix_us(torch, stream, [lay, dis, com])
+    cold = {"layout": fl - f_, "dispatch": fld - fl, "combine": flc - fld, "step": flc - f_}
+    warm = {"layout": wl, "dispatch": wld - wl, "combine": wlc - wld, "step": wlc}
+    alone = {"layout": al, "dispatch": ad, "combine": ac}
+    rep = {"workload": workload, "N": N,
+           "timing": "CUDA graphs of 20 copies, replayed round-robin 30 times, median; cold = L2 emptied "
+                     f"({flush.mib} MiB written, then {flush.mib} MiB read) before every step, kernel times are "
+                     "marginal costs inside the step; warm = no flush, steps chained; alone = 20 chained launches "
+                     "of one kernel, warm",
+           "flush_us": round(f_, 2)}
+    for name in ("layout", "dispatch", "combine", "step"):
+        b = nbytes[name]
+        r = {"bytes": b}
+        kinds = [("cold", cold[name]), ("warm", warm[name])] + ([("alone_warm", alone[name])] if name in alone else [])
+        for kind, us in kinds:
+            r[f"us_{kind}"] = round(us, 2)
+            if name != "layout":
+                r[f"gbs_{kind}"] = round(b / us / 1e3, 1)
+                r[f"frac_of_measured_hbm_{kind}"] = round(b / us / 1e3 / peak, 4)
+        if name == "step":
+            r["tokens_per_s_cold"] = round(T / (cold[name] * 1e-6), 1)
+            r["tokens_per_s_warm"] = round(T / (warm[name] * 1e-6), 1)
+        rep[name] = r
+    return rep
 
 
 def e2e_measure(torch, ep, dev, inp, args, stream):
@@ -901,6 +951,58 @@ def reference_arm(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def case_arm(args):
+    """One workload's plain step only (layout, dispatch -- fp8 e4m3 for the fp8
+    recipe, bf16 otherwise -- and combine), W + K times with a synchronize
+    around the K: a small, single-workload program for profiler captures. It
+    prints the mean step time; it is not the benchmark line."""
+    import torch
+
+    import combine_get_dispatch_layout_gb300 as ep
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    ep.lib()
+    inp = gi.make(args.case, seed=args.seed, T=args.tokens)
+    w, N = inp.w, inp.num_valid
+    fp8 = args.case == "fp8"
+    s = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s):
+        idx = torch.from_numpy(inp.topk_idx).to(dev)
+        x = torch.from_numpy(inp.x.view(np.int16)).to(dev)
+        wt = torch.from_numpy(inp.topk_weights).to(dev)
+        y = torch.from_numpy(inp.y.view(np.int16)).to(dev) if w.y != "identity" else None
+        o = [torch.empty(w.E, dtype=torch.int32, device=dev), torch.empty(w.R, dtype=torch.int32, device=dev),
+             torch.empty(w.T, w.R, dtype=torch.uint8, device=dev), torch.empty(w.E + 1, dtype=torch.int32, device=dev)]
+        recv = torch.empty(N, w.H, dtype=torch.uint8 if fp8 else torch.int16, device=dev)
+        sc = torch.empty(N, w.H // 128, dtype=torch.float32, device=dev) if fp8 else None
+        out = torch.empty(w.T, w.H, dtype=torch.int16, device=dev)
+    s.synchronize()
+    h = ep.ep_layout(idx, w.E, w.R, *o, stream=s)
+
+    def step():
+        ep.ep_layout(idx, w.E, w.R, *o, handle=h, stream=s)
+        if fp8:
+            ep.ep_dispatch(h, x, ep.EP_DTYPE_FP8_E4M3, recv, N, recv_scales=sc, stream=s)
+        else:
+            ep.ep_dispatch(h, x, ep.EP_DTYPE_BF16, recv, N, stream=s)
+        ep.ep_combine(h, recv if y is None else y, out, topk_weights=wt, y_rows=N, stream=s)
+
+    for _ in range(args.warmup):
+        step()
+    s.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(args.steps):
+        step()
+    e1.record(s)
+    s.synchronize()
+    h.destroy()
+    print(json.dumps({"case": args.case, "T": w.T, "H": w.H, "E": w.E, "K": w.K, "R": w.R, "N": N,
+                      "steps": args.steps, "us_per_step": round(e0.elapsed_time(e1) / args.steps * 1e3, 2),
+                      "note": "profiling driver: one workload's plain step, events around all steps"}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -908,8 +1010,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--tokens", type=int, default=gi.WORKLOADS[WORKLOAD].T,
-                    help="token count of the prefill recipe (smaller only for profiling captures)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="token count of the recipe (default: the recipe's own; smaller only for profiling captures)")
+    ap.add_argument("--case", choices=sorted(gi.WORKLOADS),
+                    help="profiling driver: run only this workload's plain step (with --tokens, a smaller T)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -917,7 +1021,9 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_env()
-    if args.impl == "reference":
+    if args.case:
+        case_arm(args)
+    elif args.impl == "reference":
         reference_arm(args, rank, world)
     else:
         gpu_arm(args, rank, world, local)
