@@ -29,7 +29,7 @@ class DispatchConfig(ctypes.Structure):
 EXPORTS = ("ep_layout", "ep_layout_aligned", "ep_layout_strided", "ep_layout_nonexpand",
            "ep_nonexpand_recv_topk", "ep_dispatch", "ep_dispatch_ex", "ep_combine", "ep_combine_backward",
            "ep_dispatch_backward", "ep_topk_to_routing_map", "ep_routing_map_to_topk", "ep_handle_query",
-           "ep_handle_copy_row_of_slot", "ep_handle_destroy", "ep_handle_layout_kernels",
+           "ep_handle_copy_row_of_slot", "ep_handle_destroy", "ep_handle_layout_kernels", "ep_layout_cluster_ctas",
            "ep_layout_noalloc", "ep_status_string")
 
 _lib = None
@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
         L.ep_handle_destroy.argtypes = [P]
         L.ep_handle_layout_kernels.argtypes = [P]
         L.ep_handle_layout_kernels.restype = i32
+        L.ep_layout_cluster_ctas.argtypes = [i32, i32, i32, i32]
+        L.ep_layout_cluster_ctas.restype = i32
         L.ep_layout_noalloc.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, P]
         L.ep_status_string.argtypes = [i32]
         L.ep_status_string.restype = ctypes.c_char_p
@@ -407,6 +409,12 @@ def ep_layout_noalloc(topk_idx, num_experts: int, num_ranks: int, num_tokens_per
 def ep_handle_layout_kernels(handle: Handle) -> int:
     """Kernels the last ep_layout on `handle` enqueued (1 or 3; 0 for T = 0)."""
     return int(lib().ep_handle_layout_kernels(handle.ptr))
+
+
+def ep_layout_cluster_ctas(T: int, K: int, E: int, R: int) -> int:
+    """CTAs per cluster of the single-launch layout of such a routing on the
+    current device, 0 for the three-kernel path, -1 for invalid arguments."""
+    return int(lib().ep_layout_cluster_ctas(T, K, E, R))
 
 
 def ep_handle_destroy(handle: Handle) -> None:

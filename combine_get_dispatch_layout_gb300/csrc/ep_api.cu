@@ -628,4 +628,12 @@ const char* ep_status_string(ep_status_t status) {
     return "EP_ERR_UNKNOWN";
 }
 
+int ep_layout_cluster_ctas(int T, int K, int E, int R) {
+    if (T < 0 || K < 1 || K > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS || R < 1 || R > EP_MAX_RANKS || E % R != 0)
+        return -1;
+    if (static_cast<int64_t>(T) * K >= (int64_t{1} << 31)) return -1;
+    if (T == 0) return 0;
+    return ep::layout_cluster_ctas(ep::make_layout_plan(T, K, E, R));
+}
+
 }  // extern "C"

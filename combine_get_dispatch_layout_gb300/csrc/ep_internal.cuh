@@ -91,6 +91,9 @@ struct LayoutArgs {
 // Launches the layout; *kernels (if not null) receives the number of kernels
 // enqueued (1 on the single-cluster path, 3 on the multi-block path).
 cudaError_t launch_layout(const LayoutPlan& p, const LayoutArgs& a, cudaStream_t stream, int* kernels = nullptr);
+// CTAs per cluster of the single-launch layout of `p` on the current device;
+// 0 when the routing takes the three-kernel path, -1 on a CUDA error.
+int layout_cluster_ctas(const LayoutPlan& p);
 // The offsets and row count of a strided layout with no tokens (after the
 // outputs and state words have been zeroed): offsets[e] = e * stride, N = E * stride.
 cudaError_t launch_strided_empty(int32_t* expert_offsets, int32_t* h_offsets, int32_t* meta, int E, int stride,

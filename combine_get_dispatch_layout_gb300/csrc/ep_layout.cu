@@ -807,10 +807,11 @@ int cluster_ctas_for(DeviceLaunchState& st, int warps, size_t smem) {
     return found;
 }
 
-}  // namespace
-
-cudaError_t launch_layout(const LayoutPlan& plan, const LayoutArgs& a, cudaStream_t stream, int* kernels) {
-    if (kernels) *kernels = 0;
+// The single-launch geometry for `plan` on the current device: CTAs per
+// cluster (0 = the routing takes the three-kernel path) and tokens per warp.
+cudaError_t choose_cluster(const LayoutPlan& plan, int* ctas_out, int* chunk_tokens_out) {
+    *ctas_out = 0;
+    *chunk_tokens_out = 0;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -825,39 +826,56 @@ cudaError_t launch_layout(const LayoutPlan& plan, const LayoutArgs& a, cudaStrea
         if (err != cudaSuccess) return err;
         if (try_cluster && plan.num_blocks > 0) ctas = cluster_ctas_for(st, plan.cl_warps, plan.smem_cluster);
     }
+    if (!try_cluster || ctas == 0) return cudaSuccess;
+    const int warps = ctas * plan.cl_warps;
+    const int ct = (plan.T + warps - 1) / warps;
+    // each warp's chunk must fit kMaxRounds rounds (and the token-mask area)
+    if (static_cast<int64_t>(ct) * plan.K > kMaxRounds * 32) return cudaSuccess;
+    *ctas_out = ctas;
+    *chunk_tokens_out = ct;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+int layout_cluster_ctas(const LayoutPlan& plan) {
+    int ctas = 0, ct = 0;
+    return choose_cluster(plan, &ctas, &ct) == cudaSuccess ? ctas : -1;
+}
+
+cudaError_t launch_layout(const LayoutPlan& plan, const LayoutArgs& a, cudaStream_t stream, int* kernels) {
+    if (kernels) *kernels = 0;
+    int ctas = 0, ct = 0;
+    cudaError_t err = choose_cluster(plan, &ctas, &ct);
+    if (err != cudaSuccess) return err;
     if (plan.num_blocks == 0) return cudaSuccess;
 
-    if (try_cluster) {
-        const int warps = ctas * plan.cl_warps;
-        const int ct = warps > 0 ? (plan.T + warps - 1) / warps : 0;
-        // each warp's chunk must fit kMaxRounds rounds (and the token-mask area)
-        if (ctas > 0 && static_cast<int64_t>(ct) * plan.K <= kMaxRounds * 32) {
-            LayoutPlan p = plan;
-            p.cl_ctas = ctas;
-            p.cl_chunk_tokens = ct;
-            p.itr_words = (p.R % 4 == 0 && reinterpret_cast<uintptr_t>(a.is_token_in_rank) % 4 == 0) ? 1 : 0;
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(ctas);
-            cfg.blockDim = dim3(p.cl_warps * 32);
-            cfg.dynamicSmemBytes = p.smem_cluster;
-            cfg.stream = stream;
-            cudaLaunchAttribute attr[2];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = ctas;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            // may be scheduled while the preceding kernel drains; it waits for
-            // that kernel before its first memory access
-            attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            attr[1].val.programmaticStreamSerializationAllowed = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 2;
-            if (kernels) *kernels = 1;
-            // the unpacked instance while each warp needs at most kSmallRounds rounds
-            if (static_cast<int64_t>(ct) * plan.K <= kSmallRounds * 32)
-                return cudaLaunchKernelEx(&cfg, layout_cluster_kernel<kSmallRounds>, p, a);
-            return cudaLaunchKernelEx(&cfg, layout_cluster_kernel<kMaxRounds>, p, a);
-        }
+    if (ctas > 0) {
+        LayoutPlan p = plan;
+        p.cl_ctas = ctas;
+        p.cl_chunk_tokens = ct;
+        p.itr_words = (p.R % 4 == 0 && reinterpret_cast<uintptr_t>(a.is_token_in_rank) % 4 == 0) ? 1 : 0;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(ctas);
+        cfg.blockDim = dim3(p.cl_warps * 32);
+        cfg.dynamicSmemBytes = p.smem_cluster;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = ctas;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        // may be scheduled while the preceding kernel drains; it waits for
+        // that kernel before its first memory access
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        if (kernels) *kernels = 1;
+        // the unpacked instance while each warp needs at most kSmallRounds rounds
+        if (static_cast<int64_t>(ct) * plan.K <= kSmallRounds * 32)
+            return cudaLaunchKernelEx(&cfg, layout_cluster_kernel<kSmallRounds>, p, a);
+        return cudaLaunchKernelEx(&cfg, layout_cluster_kernel<kMaxRounds>, p, a);
     }
 
     const int threads = plan.warps_per_block * 32;

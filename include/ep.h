@@ -445,6 +445,18 @@ EP_API ep_status_t ep_handle_destroy(ep_handle_t handle);
 EP_API int ep_handle_layout_kernels(ep_handle_t handle);
 
 /*
+ * ep_layout_cluster_ctas -- which path ep_layout (and ep_layout_noalloc)
+ * takes for a routing of T tokens, top-K, E experts and R ranks on the
+ * current device: the number of CTAs in the thread-block cluster of the
+ * single-launch path (16 where the GPU co-schedules 16, else 8), or 0 when
+ * the routing takes the three-kernel path (more than 2^18 slots, a plan
+ * beyond the cluster's shared memory, or more slots per warp than the
+ * cluster kernel holds). -1 for invalid arguments or a CUDA error. Enqueues
+ * nothing. For tests and launch accounting.
+ */
+EP_API int ep_layout_cluster_ctas(int T, int K, int E, int R);
+
+/*
  * ep_layout_noalloc -- the routing layout of ep_layout, for callers that
  * cannot allocate device memory.
  *

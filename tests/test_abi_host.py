@@ -133,6 +133,14 @@ def test_new_calls_reject_null_handle(L):
     assert L.ep_handle_layout_kernels(None) == -1
 
 
+def test_cluster_query_rejects_bad_routings_without_a_device(L):
+    # argument checks come before any device query
+    for args in [(-1, 8, 256, 8), (16, 0, 256, 8), (16, 33, 256, 8), (16, 8, 0, 8), (16, 8, 256, 0),
+                 (16, 8, 255, 8), (16, 8, 8192, 8), (1 << 30, 8, 256, 8)]:
+        assert L.ep_layout_cluster_ctas(*args) == -1, args
+    assert L.ep_layout_cluster_ctas(0, 8, 256, 8) == 0      # no tokens: nothing is launched
+
+
 @pytest.mark.parametrize("args", [
     (16, None, 4, 0, 8),        # K = 0
     (16, None, 4, 33, 8),       # K > 32

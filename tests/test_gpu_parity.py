@@ -236,6 +236,29 @@ def test_edge_shapes(ep, w):
     full_path(ep, inp, fp8=(w.H % 128 == 0))
 
 
+@pytest.mark.parametrize("T,K,E,R,kernels", [
+    (21504, 6, 64, 4, 1),     # 8 rounds a warp: the unpacked cluster instance
+    (21505, 6, 64, 4, 1),     # 9 rounds: the packed 16-round instance
+    (43520, 6, 64, 4, 1),     # 16 rounds: the largest single-cluster routing at top-6
+    (43521, 6, 64, 4, 3),     # one token more: the three-kernel path
+    (32768, 8, 256, 8, 1),    # 2^18 slots: the largest single-cluster routing
+    (32769, 8, 256, 8, 3),    # above 2^18 slots
+])
+def test_layout_path_at_the_boundaries(ep, T, K, E, R, kernels):
+    """The boundary routings take the path their size implies. These limits
+    assume 16-CTA clusters; on a GPU that co-schedules only 8 the cluster
+    holds half as many slots and the test is skipped."""
+    if ep.ep_layout_cluster_ctas(1024, 8, 256, 8) < 16:
+        pytest.skip("this GPU does not co-schedule 16-CTA clusters")
+    assert ep.ep_layout_cluster_ctas(T, K, E, R) == (16 if kernels == 1 else 0)
+    w = _workload(T, 64, E, K, R, routing="zipf")
+    inp = gi.make(w, 13, with_y=False)
+    run = Run(ep, inp.topk_idx, E, R)
+    assert ep.ep_handle_layout_kernels(run.h) == kernels
+    check_layout(run, oracle.layout(inp.topk_idx, E, R))
+    run.h.destroy()
+
+
 def test_large_routing_multiblock_path(ep):
     """Routings above 2^18 slots take the multi-block layout path."""
     w = _workload(40000, 128, 64, 8, 4, routing="zipf", drop_p=0.05)

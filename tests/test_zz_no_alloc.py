@@ -46,14 +46,15 @@ def _with_handle(ep, idx, E, R):
     return {k: v.cpu().numpy() for k, v in o.items()}, err
 
 
-def _no_alloc(ep, idx, E, R):
+def _no_alloc(ep, idx, E, R, with_error=True):
     T, K = idx.shape
     o = _outs(T, K, E, R)
     err = torch.full((1,), -1, dtype=torch.int32, device="cuda")
     ep.ep_layout_noalloc(idx, E, R, o["num_tokens_per_expert"], o["num_tokens_per_rank"],
-                         o["is_token_in_rank"], o["expert_offsets"], o["row_of_slot"], device_error=err)
+                         o["is_token_in_rank"], o["expert_offsets"], o["row_of_slot"],
+                         device_error=err if with_error else None)
     torch.cuda.synchronize()
-    return {k: v.cpu().numpy() for k, v in o.items()}, int(err.item())
+    return {k: v.cpu().numpy() for k, v in o.items()}, int(err.item()) if with_error else None
 
 
 def _cases():
@@ -64,8 +65,11 @@ def _cases():
     bad[3, 2], bad[77, 0] = 16, -5
     large = gi.make(gi.Workload("large", T=40000, H=128, E=64, K=8, R=4, routing="zipf", drop_p=0.05),
                     3, with_y=False)
+    # 2^18 slots on one cluster: 16 rounds a warp, the packed instance of the cluster kernel
+    packed = gi.make(gi.Workload("packed", T=32768, H=64, E=256, K=8, R=8, drop_p=0.02), 4, with_y=False)
     return [(prefill.topk_idx, 256, 8), (skewed.topk_idx, 64, 4), (bad, 16, 4),
-            (large.topk_idx, 64, 4), (gi.make("decode", 2, with_y=False).topk_idx, 256, 8)]
+            (large.topk_idx, 64, 4), (gi.make("decode", 2, with_y=False).topk_idx, 256, 8),
+            (packed.topk_idx, 256, 8)]
 
 
 def test_no_alloc_matches_layout_on_consecutive_calls(ep):
@@ -89,3 +93,22 @@ def test_no_alloc_rejects_routings_beyond_the_scratch(ep):
         ep.ep_layout_noalloc(idx, E, R, o["num_tokens_per_expert"], o["num_tokens_per_rank"],
                              o["is_token_in_rank"], o["expert_offsets"], o["row_of_slot"])
     assert e.value.status == ep.EP_ERR_CAPACITY
+
+
+def test_no_alloc_without_error_word_and_with_no_tokens(ep):
+    # device_error may be NULL; T = 0 zeroes the counts and offsets, as the handle path does
+    idx_np = gi.make("tiny", 3, with_y=False).topk_idx
+    idx = torch.from_numpy(idx_np).cuda()
+    want, _ = _with_handle(ep, idx, 8, 2)
+    got, _ = _no_alloc(ep, idx, 8, 2, with_error=False)
+    for k in want:
+        np.testing.assert_array_equal(got[k], want[k], err_msg=k)
+    empty = torch.zeros((0, 2), dtype=torch.int64, device="cuda")
+    want0, err0 = _with_handle(ep, empty, 8, 2)
+    for with_error in (True, False):
+        got0, e = _no_alloc(ep, empty, 8, 2, with_error=with_error)
+        for k in ("num_tokens_per_expert", "num_tokens_per_rank", "expert_offsets"):
+            np.testing.assert_array_equal(got0[k], want0[k], err_msg=k)
+        assert not got0["expert_offsets"].any()
+        if with_error:
+            assert e == err0 == 0
