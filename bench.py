@@ -152,18 +152,19 @@ def smi_id(local: int) -> str:
     return str(local)
 
 
-def read_traffic(kernel: str, T: int):
-    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if
-    the capture was of this token count and the kernel source has not changed
-    since (else None)."""
+def read_traffic(kernel: str, T: int, case: str = "prefill"):
+    """Per-launch DRAM bytes of `kernel` on workload `case` from the committed
+    ncu summary profiles/dram_traffic_<case>_T<T>.md, if the capture was of
+    this token count and the kernel source has not changed since (else None)."""
     import hashlib
     import re
 
-    path = os.path.join(ROOT, "profiles", "dram_traffic_prefill_T8192.md")
+    path = os.path.join(ROOT, "profiles", f"dram_traffic_{case}_T{T}.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
-    m = re.search(rf"<!-- traffic kernel={kernel} T=(\d+) bytes=(\d+) src_sha256=([0-9a-f]+) -->", txt)
+    m = re.search(rf"<!-- traffic kernel={kernel}(?: case={case})? T=(\d+) bytes=(\d+) src_sha256=([0-9a-f]+) -->",
+                  txt)
     if not m or int(m.group(1)) != T:
         return None
     src = {"dispatch_bf16": "ep_dispatch.cu", "combine": "ep_combine.cu"}.get(kernel)
@@ -714,7 +715,11 @@ def other_configs(torch, ep, dev, stream, args, rank, peak, reps):
         "dispatch_frac_of_measured": round(bd / (ms[1] * 1e-3) / 1e9 / peak, 4),
         "combine_us": round(ms[2] * 1e3, 2), "combine_gbs": round(bc / (ms[2] * 1e-3) / 1e9, 1),
         "combine_frac_of_measured": round(bc / (ms[2] * 1e-3) / 1e9 / peak, 4),
-        "tokens_per_s": round(ws.T / (sum(ms) * 1e-3), 1)}
+        "tokens_per_s": round(ws.T / (sum(ms) * 1e-3), 1),
+        "dispatch_traffic": read_traffic("dispatch_bf16", ws.T, "skewed"),
+        "combine_traffic": read_traffic("combine", ws.T, "skewed"),
+        "traffic_note": "per-launch DRAM read + write bytes from one ncu pass (profiles/dram_traffic_skewed_T16384.md), "
+                        "null if the kernel source changed since"}
     del t, y
 
     flush = L2Flush(torch, dev, stream)
