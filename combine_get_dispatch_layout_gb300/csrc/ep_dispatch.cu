@@ -20,10 +20,15 @@
 // and the scale and codes are computed once per token and reused for all K
 // copies. Item sizes won sweeps on the prefill shape: 2 vectors per lane for
 // bf16 (of 1 to 8), one 512-channel group per item for fp8 (16 channels per
-// lane beat 8 by 6-11%); small items shorten the last wave.
+// lane beat 8 by 6-11%); small items shorten the last wave. A bf16 grid of
+// less than one wave (the decode shapes) takes one vector per lane instead,
+// so twice as many warps share the stores: 0.4 us off the T=256 step, none
+// lost at the prefill shape, which keeps two.
 // The slot map is read only after griddepcontrol.wait: launched as the
 // layout's programmatic dependent, a block loads (and quantises) its x slice
 // on an SM the layout leaves idle, then waits for the layout to finish.
+#include <atomic>
+
 #include "ep_internal.cuh"
 
 namespace ep {
@@ -94,7 +99,7 @@ __device__ __forceinline__ bool pad_block(const DispatchArgs& a, int64_t row_byt
     return true;
 }
 
-constexpr int kPrefetchCtas = 512;                   // blocks that issue the x prefetch
+constexpr int kPrefetchCtas = 1024;                   // blocks that issue the x prefetch
 constexpr int64_t kPrefetchWindow = int64_t{96} << 20;   // bytes of x prefetched past theirs
 
 // HBM is idle while the layout runs. In a dispatch launched as the layout's
@@ -104,10 +109,15 @@ constexpr int64_t kPrefetchWindow = int64_t{96} << 20;   // bytes of x prefetche
 // registers or shared memory. Later blocks then find their rows in L2 (the
 // receive stores are evict-first, so the prefetched lines survive until
 // read), which takes those bytes off the dispatch's critical path. A hint
-// only: results do not depend on it. On the prefill shape it shortened the
-// step by ~5 us; windows of 64 to 128 MB and 256 to 1024 blocks were within
-// 1 us of each other, and an evict-last cache policy was slower (and kept x
-// in L2 past the dispatch).
+// only: results do not depend on it. Prefill step (300 chained steps):
+// 321.6 us without it; a 96 MB window from 512 blocks 315.9 us, from 1024
+// blocks 314.3 us. Windows of 24 / 48 / 64 / 128 MB from 512 blocks gave
+// 317.9 / 317.4 / 316.9 / 315.5 us, and 2048 or 4096 blocks 320-322 us (the
+// blocks past the first wave start only after the layout, so their prefetch
+// competes with the dispatch itself). Part of the prefetched x is evicted
+// and read again before use, but fetching it while HBM is otherwise idle
+// still wins. An evict-last cache policy was slower (and kept x in L2 past
+// the dispatch).
 __device__ __forceinline__ void prefetch_x_during_layout(const DispatchArgs& a, int num_segments,
                                                          int64_t row_bytes, int64_t block) {
     if (!a.prefetch_x || block >= kPrefetchCtas || threadIdx.x != 0) return;
@@ -136,6 +146,7 @@ __device__ __forceinline__ void write_side_outputs(const DispatchArgs& a, int t,
     }
 }
 
+template <int kUnroll>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 dispatch_bf16_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
     const int lane = threadIdx.x & 31;
@@ -149,11 +160,11 @@ dispatch_bf16_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
 
     const int4* src = reinterpret_cast<const int4*>(a.x) + static_cast<int64_t>(t) * H16;
     int4* dst = reinterpret_cast<int4*>(a.recv_x);
-    const int j0 = seg * (32 * kBf16Unroll) + lane;
+    const int j0 = seg * (32 * kUnroll) + lane;
     if (!a.overlap_layout) wait_for_layout();
-    int4 v[kBf16Unroll];
+    int4 v[kUnroll];
 #pragma unroll
-    for (int u = 0; u < kBf16Unroll; ++u) {
+    for (int u = 0; u < kUnroll; ++u) {
         const int j = j0 + u * 32;
         if (j < H16) v[u] = ld_stream(src + j);
     }
@@ -169,7 +180,7 @@ dispatch_bf16_kernel(DispatchArgs a, int64_t num_items, int num_segments) {
         if (r < 0) continue;
         int4* d = dst + static_cast<int64_t>(r) * H16;
 #pragma unroll
-        for (int u = 0; u < kBf16Unroll; ++u) {
+        for (int u = 0; u < kUnroll; ++u) {
             const int j = j0 + u * 32;
             if (j < H16) __stcs(d + j, v[u]);
         }
@@ -392,6 +403,28 @@ DispatchArgs with_pad_blocks(const DispatchArgs& a) {
     return b;
 }
 
+// Warps the GPU holds at once for the bf16 dispatch (SMs x resident blocks x
+// warps per block), per device, looked up once (any thread may store it:
+// every lookup gives the same value).
+int64_t resident_dispatch_warps() {
+    static std::atomic<int64_t> warps[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int64_t w = warps[dev].load(std::memory_order_relaxed);
+    if (w == 0) {
+        int sms = 0, per_sm = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_bf16_kernel<kBf16Unroll>,
+                                                          kWarpsPerBlock * 32, 0) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        w = static_cast<int64_t>(sms) * per_sm * kWarpsPerBlock;
+        warps[dev].store(w, std::memory_order_relaxed);
+    }
+    return w;
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch_bf16(const DispatchArgs& args, cudaStream_t stream) {
@@ -401,8 +434,16 @@ cudaError_t launch_dispatch_bf16(const DispatchArgs& args, cudaStream_t stream) 
     const int segs = (H16 + per_item - 1) / per_item;
     const int64_t items = static_cast<int64_t>(a.T) * segs;
     if (items == 0) return cudaSuccess;
+    // a grid of less than one wave leaves SMs short of warps: halve the items
+    // (one 16-byte vector per lane) so twice as many warps share the stores
+    if (items < resident_dispatch_warps()) {
+        const int segs1 = (H16 + 31) / 32;
+        const int64_t items1 = static_cast<int64_t>(a.T) * segs1;
+        const int64_t blocks1 = (items1 + kWarpsPerBlock - 1) / kWarpsPerBlock + a.pad_blocks;
+        return launch_dispatch_kernel(dispatch_bf16_kernel<1>, blocks1, stream, a, items1, segs1);
+    }
     const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock + a.pad_blocks;
-    return launch_dispatch_kernel(dispatch_bf16_kernel, blocks, stream, a, items, segs);
+    return launch_dispatch_kernel(dispatch_bf16_kernel<kBf16Unroll>, blocks, stream, a, items, segs);
 }
 
 cudaError_t launch_fill_pad_rows(const int32_t* counts, const int32_t* offsets, int E, int64_t row_bytes,
