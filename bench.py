@@ -726,10 +726,9 @@ def other_configs(torch, ep, dev, stream, args, rank, peak, reps):
         "combine_us": round(ms[2] * 1e3, 2), "combine_gbs": round(bc / (ms[2] * 1e-3) / 1e9, 1),
         "combine_frac_of_measured": round(bc / (ms[2] * 1e-3) / 1e9 / peak, 4),
         "tokens_per_s": round(ws.T / (sum(ms) * 1e-3), 1),
-        "dispatch_traffic": read_traffic("dispatch_bf16", ws.T, "skewed"),
         "combine_traffic": read_traffic("combine", ws.T, "skewed"),
-        "traffic_note": "per-launch DRAM read + write bytes from one ncu pass (profiles/dram_traffic_skewed_T16384.md), "
-                        "null if the kernel source changed since"}
+        "traffic_note": "the combine's per-launch DRAM read + write bytes from one ncu pass "
+                        "(profiles/dram_traffic_skewed_T16384.md), null if its source changed since"}
     del t, y
 
     flush = L2Flush(torch, dev, stream)
