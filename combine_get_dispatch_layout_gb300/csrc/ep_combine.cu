@@ -10,15 +10,16 @@
 //
 // GPU design: the work item is (token, column segment), one warp per item.
 // The warp compacts the token's used slots (ballot + popc) into shared memory
-// in ascending k, then for its 16-byte column vector issues the loads of a
-// group of slots at once before accumulating them in k order. Items are small
-// (256 channels) and blocks are 2 warps, so many warps per SM keep the
-// gather's bytes in flight and the last wave is short; a sweep of vectors per
-// lane (1, 2, 4), slots per load group (3 to 8) and warps per block (1 to 8)
-// picked this point. The group is K split into the fewest round trips of at
-// most 6 slots, in equal parts: 4 + 4 for top-8, one trip of 6 for top-6
-// (groups of 4 there cost 5% on a 4 + 2 split; groups of 8 for top-8 cost 2%
-// in occupancy).
+// in ascending k, then for its two 16-byte column vectors issues the loads of
+// a group of slots at once before accumulating them in k order. Items are
+// 512 channels and blocks are 2 warps. The group is K split into the fewest
+// round trips of at most 6 slots, in equal parts: 4 + 4 for top-8, one trip
+// of 6 for top-6 (groups of 4 there cost 5% on a 4 + 2 split; groups of 8
+// for top-8 cost 2% in occupancy). Vectors per lane, A/B on one box, three
+// interleaved rounds: two instead of one took the skewed step (top-6) from
+// 298.2 to 292.4 us, the decode step (T=256) from 14.08 to 13.72 us warm and
+// the prefill step from 314.4 to 313.5 us; four lost on all three (the top-6
+// instance then needs 152 registers); 1 or 4 warps per block lost to 2.
 #include <cuda_bf16.h>
 
 #include "ep_internal.cuh"
@@ -28,7 +29,7 @@ namespace ep {
 namespace {
 
 constexpr int kWarpsPerBlock = 2;   // small blocks: fine-grained scheduling
-constexpr int kUnroll = 1;      // 16-byte column vectors per lane per item
+constexpr int kUnroll = 2;      // 16-byte column vectors per lane per item
 constexpr int kMaxGroup = 6;    // most slots whose loads are issued together
 
 __device__ __forceinline__ int4 ld_stream(const int4* p) {

@@ -236,6 +236,18 @@ def test_edge_shapes(ep, w):
     full_path(ep, inp, fp8=(w.H % 128 == 0))
 
 
+@pytest.mark.parametrize("T", [480, 521, 522, 560])
+def test_dispatch_across_its_item_size_switch(ep, T):
+    """A bf16 dispatch grid below one wave of resident warps moves one 16-byte
+    vector per lane instead of two. At H=7168 the two-vector grid has 14 items
+    a token, so on a 152-SM GB300 (7296 resident warps) the switch falls
+    between 521 and 522 tokens; both sides, with fp8 and the aligned layout's
+    pad rows, must match the oracle."""
+    inp = gi.make("prefill", 21, T=T)
+    full_path(ep, inp, fp8=True)
+    full_path_aligned(ep, gi.make("prefill", 22, T=T), 64)
+
+
 @pytest.mark.parametrize("T,K,E,R,kernels", [
     (21504, 6, 64, 4, 1),     # 8 rounds a warp: the unpacked cluster instance
     (21505, 6, 64, 4, 1),     # 9 rounds: the packed 16-round instance
