@@ -827,6 +827,18 @@ cudaError_t choose_cluster(const LayoutPlan& plan, int* ctas_out, int* chunk_tok
         if (try_cluster && plan.num_blocks > 0) ctas = cluster_ctas_for(st, plan.cl_warps, plan.smem_cluster);
     }
     if (!try_cluster || ctas == 0) return cudaSuccess;
+    // A small routing takes fewer CTAs: the smallest power of two (at least
+    // 4) that gives each warp at most one 32-slot round. Fewer CTAs mean
+    // fewer shared-memory pushes to wait for at the cluster barrier.
+    // Graph-chained layout / warm step, E=256 top-8: at T=256 (2048 slots)
+    // 8 CTAs took 3.90 / 12.59 us against 4.43 / 13.65 with 16; at T=64,
+    // 4 CTAs 3.69 / 8.30 against 4.00 / 8.81; 1024 tokens and more stay at 16.
+    {
+        const int64_t per_cta = static_cast<int64_t>(plan.cl_warps) * 32;
+        int want = 4;
+        while (want < ctas && static_cast<int64_t>(want) * per_cta < slots) want <<= 1;
+        if (want < ctas) ctas = want;
+    }
     const int warps = ctas * plan.cl_warps;
     const int ct = (plan.T + warps - 1) / warps;
     // each warp's chunk must fit kMaxRounds rounds (and the token-mask area)

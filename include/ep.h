@@ -448,7 +448,9 @@ EP_API int ep_handle_layout_kernels(ep_handle_t handle);
  * ep_layout_cluster_ctas -- which path ep_layout (and ep_layout_noalloc)
  * takes for a routing of T tokens, top-K, E experts and R ranks on the
  * current device: the number of CTAs in the thread-block cluster of the
- * single-launch path (16 where the GPU co-schedules 16, else 8), or 0 when
+ * single-launch path (up to 16 where the GPU co-schedules 16, else up to 8;
+ * small routings take fewer, at least 4, so that each warp holds at most
+ * one 32-slot round), or 0 when
  * the routing takes the three-kernel path (more than 2^18 slots, a plan
  * beyond the cluster's shared memory, or more slots per warp than the
  * cluster kernel holds). -1 for invalid arguments or a CUDA error. Enqueues

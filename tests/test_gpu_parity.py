@@ -248,6 +248,25 @@ def test_dispatch_across_its_item_size_switch(ep, T):
     full_path_aligned(ep, gi.make("prefill", 22, T=T), 64)
 
 
+@pytest.mark.parametrize("T,K,E,R,ctas", [
+    (128, 2, 8, 2, 4),        # the tiny routing: 256 slots
+    (64, 8, 256, 8, 4),       # 512 slots
+    (256, 8, 256, 8, 8),      # the decode routing: 2048 slots, one round for each of 64 warps
+    (512, 8, 256, 8, 16),     # 4096 slots
+])
+def test_small_routings_take_smaller_clusters(ep, T, K, E, R, ctas):
+    """A small routing runs on the fewest CTAs (at least 4) that give each warp
+    at most one 32-slot round; its outputs still match the oracle."""
+    if ep.ep_layout_cluster_ctas(1024, 8, 256, 8) < 16:
+        pytest.skip("this GPU does not co-schedule 16-CTA clusters")
+    assert ep.ep_layout_cluster_ctas(T, K, E, R) == ctas
+    idx = np.argsort(np.random.default_rng(T).random((T, E)), axis=1)[:, :K].astype(np.int64)
+    run = Run(ep, idx, E, R)
+    assert ep.ep_handle_layout_kernels(run.h) == 1
+    check_layout(run, oracle.layout(idx, E, R))
+    run.h.destroy()
+
+
 @pytest.mark.parametrize("T,K,E,R,kernels", [
     (21504, 6, 64, 4, 1),     # 8 rounds a warp: the unpacked cluster instance
     (21505, 6, 64, 4, 1),     # 9 rounds: the packed 16-round instance
