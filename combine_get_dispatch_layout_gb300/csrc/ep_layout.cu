@@ -726,12 +726,15 @@ LayoutPlan make_layout_plan(int T, int K, int E, int R) {
     p.num_blocks = p.num_chunks > 0 ? (p.num_chunks + wpb - 1) / wpb : 0;
     p.smem_count = (static_cast<size_t>(wpb) * E + R) * sizeof(int);
     p.smem_assign = (static_cast<size_t>(wpb + 1) * E + 33) * sizeof(int);
-    // single-cluster geometry (CTA count fixed at launch): as many warps per
-    // CTA as shared memory allows, up to 32
-    // about four 32-slot rounds per warp on a 16-CTA cluster, 8 to 32 warps,
-    // fewer if shared memory does not fit; smem_cluster = 0 disables the path
+    // single-cluster geometry (CTA count fixed at launch), warps per CTA
+    // counted on a 16-CTA cluster: 8 while that gives each warp at most one
+    // 32-slot round, else 16, doubling (to 32) while a warp would have more
+    // than about four rounds; fewer if shared memory does not fit, and
+    // smem_cluster = 0 disables the path. Graph-chained layouts (top-8): 16
+    // warps beat 8 at T=1024 and 2048 by 0.3 and 0.7 us, 8 stay best below,
+    // 32 at 2^16 slots.
     const int64_t slots = static_cast<int64_t>(T) * K;
-    int cw = 8;
+    int cw = slots > static_cast<int64_t>(16) * 8 * 32 ? 16 : 8;
     while (cw < 32 && slots > static_cast<int64_t>(16) * cw * 32 * kRoundsInFlight) cw <<= 1;
     auto cluster_smem = [&](int w) {
         const size_t ct_cap = static_cast<size_t>(kMaxRounds * 32 / K);
