@@ -715,6 +715,21 @@ def other_configs(torch, ep, dev, stream, args, rank, peak, reps):
         lambda: ep.ep_layout(t["idx"], ws.E, ws.R, t["cnt"], t["ntr"], t["itr"], t["off"], handle=h, stream=stream),
         lambda: ep.ep_dispatch(h, t["x"], ep.EP_DTYPE_BF16, t["recv"], cap, stream=stream),
         lambda: ep.ep_combine(h, y, t["out"], topk_weights=t["w"], stream=stream)])
+
+    def sk_step():
+        ep.ep_layout(t["idx"], ws.E, ws.R, t["cnt"], t["ntr"], t["itr"], t["off"], handle=h, stream=stream)
+        ep.ep_dispatch_ex(h, t["x"], t["recv"], cap, out_dtype=ep.EP_DTYPE_BF16, overlap_layout=True, stream=stream)
+        ep.ep_combine(h, y, t["out"], topk_weights=t["w"], stream=stream)
+
+    for _ in range(3):
+        sk_step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        sk_step()
+    e1.record(stream)
+    stream.synchronize()
+    ms_sk_step = e0.elapsed_time(e1) / reps
     h.destroy()
     bd, bc = bytes_dispatch_bf16(ws.T, ws.K, ws.H, Ns), bytes_combine(ws.T, ws.K, ws.H, Ns)
     out["skewed_step"] = {
@@ -726,6 +741,11 @@ def other_configs(torch, ep, dev, stream, args, rank, peak, reps):
         "combine_us": round(ms[2] * 1e3, 2), "combine_gbs": round(bc / (ms[2] * 1e-3) / 1e9, 1),
         "combine_frac_of_measured": round(bc / (ms[2] * 1e-3) / 1e9 / peak, 4),
         "tokens_per_s": round(ws.T / (sum(ms) * 1e-3), 1),
+        "step_us_chained": round(ms_sk_step * 1e3, 2),
+        "step_gbs_chained": round((bytes_layout(ws.T, ws.K, ws.E, ws.R) + bd + bc) / (ms_sk_step * 1e-3) / 1e9, 1),
+        "step_frac_of_measured_chained": round((bytes_layout(ws.T, ws.K, ws.E, ws.R) + bd + bc) / (ms_sk_step * 1e-3)
+                                               / 1e9 / peak, 4),
+        "tokens_per_s_chained": round(ws.T / (ms_sk_step * 1e-3), 1),
         "combine_traffic": read_traffic("combine", ws.T, "skewed"),
         "traffic_note": "the combine's per-launch DRAM read + write bytes from one ncu pass "
                         "(profiles/dram_traffic_skewed_T16384.md), null if its source changed since"}

@@ -179,6 +179,19 @@ def test_e4m3_encoder_vs_brute_search():
     np.testing.assert_array_equal(oracle.f32_to_e4m3(f), brute.e4m3_encode(f))
 
 
+def test_encoders_on_every_bf16_bit_pattern():
+    """Every bf16 value (the dispatch's inputs are bf16) through the oracle's
+    encoders: bf16 gives back the same bits, e4m3 and e5m2 give torch's
+    saturating casts; NaN patterns are outside the contract."""
+    u = (np.arange(1 << 16, dtype=np.uint32) << np.uint32(16))
+    f = u.view(np.float32)
+    fin = np.isfinite(f)
+    np.testing.assert_array_equal(oracle.f32_to_bf16(f[fin]), (u[fin] >> 16).astype(np.uint16))
+    np.testing.assert_array_equal(oracle.f32_to_e4m3(f[fin]), _torch_e4m3_bits(f[fin]))
+    np.testing.assert_array_equal(oracle.f32_to_e5m2(f[fin]), _torch_e5m2_bits(f[fin]))
+    assert fin.sum() == (1 << 16) - 2 * 128    # all but the 2 x 128 infinity / NaN patterns
+
+
 _SWEEP_RANGES = [
     (0x00000000, 1 << 18),                 # +0 and fp32 subnormals
     (0x3A800000 - (1 << 17), 0x3A800000 + (1 << 17)),   # around 2^-10 (fp8 subnormals)
