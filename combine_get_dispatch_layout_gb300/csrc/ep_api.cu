@@ -209,6 +209,7 @@ ep_status_t layout_impl(const int64_t* topk_idx, int T, int K, int E, int R, int
         if (cudaGetDevice(&h->device) != cudaSuccess) { delete h; return EP_ERR_CUDA; }
         h->alloc_fn = alloc_fn ? alloc_fn : default_alloc;
         h->free_fn = free_fn ? free_fn : default_free;
+        ep::prime_dispatch_launch_state();
         if (cudaMallocHost(reinterpret_cast<void**>(&h->host_meta), sizeof(int32_t) * ep::kMetaWords) !=
             cudaSuccess) {
             delete h;

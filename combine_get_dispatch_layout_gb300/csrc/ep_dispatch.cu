@@ -427,6 +427,8 @@ int64_t resident_dispatch_warps() {
 
 }  // namespace
 
+void prime_dispatch_launch_state() { resident_dispatch_warps(); }
+
 cudaError_t launch_dispatch_bf16(const DispatchArgs& args, cudaStream_t stream) {
     const DispatchArgs a = with_pad_blocks(args);
     const int H16 = a.H / 8;

@@ -135,6 +135,10 @@ struct DispatchArgs {
 };
 
 cudaError_t launch_dispatch_bf16(const DispatchArgs& a, cudaStream_t stream);
+// Look up, for the current device, what the dispatch launchers query once
+// (the resident warps that pick the item size), so that the first dispatch
+// never makes that query inside a stream capture. Called at handle creation.
+void prime_dispatch_launch_state();
 cudaError_t launch_dispatch_fp8(const DispatchArgs& a, cudaStream_t stream);
 // fp8 input: codes [T, H] bytes and scale rows moved unchanged to every slot's row
 cudaError_t launch_dispatch_fp8_passthrough(const DispatchArgs& a, cudaStream_t stream);

@@ -1533,6 +1533,64 @@ def test_graph_capture_replays_the_step(ep, name, fp8):
     h.destroy()
 
 
+_FIRST_CALLS_IN_CAPTURE = r"""
+import sys
+import numpy as np
+import torch
+sys.path.insert(0, sys.argv[1])
+import combine_get_dispatch_layout_gb300 as ep
+import oracle
+from gen import inputs as gi
+
+inp = gi.make("decode", 61)
+w = inp.w
+cap = w.T * w.K
+s = torch.cuda.Stream()
+with torch.cuda.stream(s):
+    idx = torch.from_numpy(inp.topk_idx).cuda()
+    x = torch.from_numpy(inp.x.view(np.int16)).cuda().view(torch.bfloat16)
+    wt = torch.from_numpy(inp.topk_weights).cuda()
+    y = torch.from_numpy(inp.y.view(np.int16)).cuda().view(torch.bfloat16)
+    o = [torch.empty(w.E, dtype=torch.int32, device="cuda"), torch.empty(w.R, dtype=torch.int32, device="cuda"),
+         torch.empty(w.T, w.R, dtype=torch.uint8, device="cuda"), torch.empty(w.E + 1, dtype=torch.int32, device="cuda")]
+    recv = torch.empty(cap, w.H, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
+    h = ep.ep_layout(idx, w.E, w.R, *o)
+s.synchronize()
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g, stream=s):      # this process's first dispatch and combine
+    ep.ep_layout(idx, w.E, w.R, *o, handle=h)
+    ep.ep_dispatch_ex(h, x, recv, cap, out_dtype=ep.EP_DTYPE_BF16, overlap_layout=True)
+    ep.ep_combine(h, y, out, topk_weights=wt)
+with torch.cuda.stream(s):
+    g.replay()
+s.synchronize()
+ref = oracle.layout(inp.topk_idx, w.E, w.R)
+n = int(ref["expert_offsets"][-1])
+r_x, _, _ = oracle.dispatch_bf16(inp.x, ref["row_of_slot"], n)
+assert np.array_equal(recv[:n].view(torch.int16).cpu().numpy().view(np.uint16), r_x)
+assert np.array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16),
+                      oracle.combine(inp.y, ref["row_of_slot"], inp.topk_weights))
+h.destroy()
+print("ok")
+"""
+
+
+def test_first_dispatch_of_a_process_inside_a_capture(ep, tmp_path):
+    """The library's one-time launch queries must not fall inside a user's
+    stream capture: in a fresh process, with only the handle-creating layout
+    run eagerly, the first dispatch and combine are captured into a graph,
+    replayed, and checked against the oracle."""
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    script = tmp_path / "first_calls.py"
+    script.write_text(_FIRST_CALLS_IN_CAPTURE)
+    r = subprocess.run([sys.executable, str(script), root], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
+
+
 def test_graph_capture_of_the_whole_chain(ep):
     """Conversions, layout, a plain dispatch (which waits at entry), combine
     and both backward passes captured into one CUDA graph, every kernel a
