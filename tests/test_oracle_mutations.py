@@ -105,6 +105,15 @@ MUTATIONS = [
     ("non-expand weight of the row's slot for every entry", "on && w ? w[t * K + j] : 0.0f;",
      "on && w ? w[t * K + k] : 0.0f;", 0),
     ("non-expand weight kept on an off-rank slot", "on && w ? w[t * K + j] : 0.0f;", "w ? w[t * K + j] : 0.0f;", 0),
+    ("non-expand ids left global", "recv_topk_idx[(int64_t)row * K + j] = on ? ej - r * L : -1;",
+     "recv_topk_idx[(int64_t)row * K + j] = on ? ej : -1;", 0),
+    ("row permute reads the row index as the token",
+     "if (row >= 0) memcpy(recv + (int64_t)row * row_bytes, src + t * row_bytes, (size_t)row_bytes);",
+     "if (row >= 0) memcpy(recv + (int64_t)row * row_bytes, src + (row % T) * row_bytes, (size_t)row_bytes);", 0),
+    ("strided offsets one block late", "for (int e = 0; e <= E; ++e) expert_offsets[e] = e * cap;",
+     "for (int e = 0; e <= E; ++e) expert_offsets[e] = (e + 1) * cap;", 0),
+    ("strided rows from the packed offset", "row_of_slot[s] = (int32_t)(e * cap) + rank_in_expert;",
+     "row_of_slot[s] = packed[e] + rank_in_expert;", 0),
 ]
 
 
